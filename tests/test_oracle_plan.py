@@ -1,0 +1,216 @@
+"""Pins for oracle.plan: brute force on tiny inputs, E(M) preservation under
+several physical tilings, class invariants and the schedule order."""
+import functools
+
+import numpy as np
+import pytest
+
+from oracle import mask as M
+from oracle import plan as P
+from block_sparse_masked_gb300 import workloads as W
+
+
+def _tiny_interval_workload(seed, B, S, nfunc, Hmask=1, H=2, varlen_lens=None):
+    import torch
+    if varlen_lens is None:
+        mf = W.random_intervals(seed, B, S, S, nfunc, Hmask)
+        w = W.Workload("fuzz", W.LAYOUT_BSHD, B, S, S, H, H, 8,
+                       torch.zeros(B, S, H, 8, dtype=torch.bfloat16),
+                       torch.zeros(B, S, H, 8, dtype=torch.bfloat16),
+                       torch.zeros(B, S, H, 8, dtype=torch.bfloat16), 1.0, "intervals",
+                       mask_func=mf)
+        return w
+    lens = np.array(varlen_lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tot = int(lens.sum())
+    mf = W.random_intervals(seed, len(lens), 0, 0, nfunc, Hmask, lens_q=lens, lens_k=lens)
+    mx = int(lens.max())
+    return W.Workload("fuzz_varlen", W.LAYOUT_THD, len(lens), mx, mx, H, H, 8,
+                      torch.zeros(tot, H, 8, dtype=torch.bfloat16),
+                      torch.zeros(tot, H, 8, dtype=torch.bfloat16),
+                      torch.zeros(tot, H, 8, dtype=torch.bfloat16), 1.0, "intervals",
+                      mask_func=mf, cu_seqlens_q=cu, cu_seqlens_k=cu.copy())
+
+
+def _brute_plan(w, T_Q, T_KV):
+    """Per-element Python loops: classes, ascending CSR lists and payload words."""
+    out = {}
+    for hm in range(w.Hmask):
+        for b, (qo, ql, ko, kl) in enumerate(w.sample_bounds()):
+            vis = M.visible_rows(w, hm, b, np.arange(ql))
+            nq, nk = -(-ql // T_Q), -(-kl // T_KV)
+            for i in range(nq):
+                plist, flist, pays = [], [], []
+                for j in range(nk):
+                    cnt, inb = 0, 0
+                    words = []
+                    for r in range(T_Q):
+                        row_words = []
+                        for wd in range(-(-T_KV // 32)):
+                            word = 0
+                            for l in range(32):
+                                c = wd * 32 + l
+                                qq, kk = i * T_Q + r, j * T_KV + c
+                                if c < T_KV and qq < ql and kk < kl:
+                                    inb += 1
+                                    if vis[qq, kk]:
+                                        cnt += 1
+                                        word |= 1 << l
+                            row_words.append(word)
+                        words.append(row_words)
+                    if cnt == 0:
+                        continue
+                    if cnt == T_Q * T_KV:
+                        flist.append(j)
+                    else:
+                        plist.append(j)
+                        pays.append(words)
+                out[(hm, b, i)] = (plist, flist, pays)
+    return out
+
+
+@pytest.mark.parametrize("T", [(64, 64), (128, 128), (64, 32)])
+@pytest.mark.parametrize("case", [
+    dict(seed=1, B=1, S=200, nfunc=1),
+    dict(seed=2, B=2, S=130, nfunc=3),
+    dict(seed=3, B=1, S=257, nfunc=5, Hmask=2),
+    dict(seed=4, B=0, S=0, nfunc=3, varlen_lens=[70, 1, 129, 64]),
+])
+def test_plan_matches_brute_force(T, case):
+    w = _tiny_interval_workload(**case)
+    p = P.build_plan(w, *T)
+    ref = _brute_plan(w, *T)
+    for hm in range(w.Hmask):
+        for r in range(p.rows):
+            b, m = int(p.row_batch[r]), int(p.row_mblock[r])
+            plist, flist, pays = ref[(hm, b, m)]
+            f = hm * p.rows + r
+            pi = p.partial_idx[p.partial_offset[f]:p.partial_offset[f + 1]].tolist()
+            fi = p.full_idx[p.full_offset[f]:p.full_offset[f + 1]].tolist()
+            assert pi == plist and fi == flist
+            got = p.payload[p.partial_offset[f]:p.partial_offset[f + 1]].tolist()
+            assert got == pays
+    assert p.header[:3] == [p.rows, p.partial_idx.size, p.full_idx.size]
+
+
+@pytest.mark.parametrize("T", [(64, 64), (128, 128), (128, 64), (64, 128), (32, 96)])
+@pytest.mark.parametrize("geom", [(64, 64), (48, 80), (128, 32)])
+def test_block_plan_preserves_EM(T, geom):
+    """"A plan built from block geometry reproduces E(M) exactly under any physical tiling."""
+    import torch
+    BQ, BKV = geom
+    S = 700
+    nbq, nbk = -(-S // BQ), -(-S // BKV)
+    bm = W.random_block_mask(11, 2, nbq, nbk, 0.3)
+    w = W.Workload("blk", W.LAYOUT_BSHD, 1, S, S, 2, 2, 8,
+                   torch.zeros(1, S, 2, 8), torch.zeros(1, S, 2, 8), torch.zeros(1, S, 2, 8),
+                   1.0, "blocks", block_mask=bm, block_q=BQ, block_kv=BKV)
+    p = P.build_plan(w, *T)
+    for hm in range(2):
+        rec = P.visible_from_plan(p, hm, 0, S, S)
+        em = np.kron(bm[hm], np.ones((BQ, BKV), np.uint8))[:S, :S].astype(bool)
+        assert np.array_equal(rec, em)
+
+
+def test_interval_plan_preserves_visibility_and_counts():
+    w = _tiny_interval_workload(seed=9, B=0, S=0, nfunc=5, Hmask=2,
+                                varlen_lens=[300, 5, 128, 257])
+    p = P.build_plan(w, 128, 128)
+    total = 0
+    for hm in range(2):
+        for b, (qo, ql, ko, kl) in enumerate(w.sample_bounds()):
+            vis = M.visible_rows(w, hm, b, np.arange(ql))
+            assert np.array_equal(P.visible_from_plan(p, hm, b, ql, kl), vis)
+            total += int(vis.sum())
+    # sum over full tiles of T_Q*T_KV plus payload popcount == visible pairs
+    pop = int(np.unpackbits(p.payload.view(np.uint8)).sum())
+    assert p.full_idx.size * 128 * 128 + pop == total == p.visible_pairs
+
+
+def test_each_tile_exactly_one_class_and_tail_never_full():
+    w = _tiny_interval_workload(seed=12, B=0, S=0, nfunc=3,
+                                varlen_lens=[129, 256, 200, 1, 383])
+    p = P.build_plan(w, 128, 128)
+    for r in range(p.rows):
+        b = int(p.row_batch[r])
+        pi = set(p.partial_idx[p.partial_offset[r]:p.partial_offset[r + 1]].tolist())
+        fi = set(p.full_idx[p.full_offset[r]:p.full_offset[r + 1]].tolist())
+        assert not (pi & fi)
+        assert all(0 <= j < p.k_tiles[b] for j in pi | fi)
+        kl = w.sample_bounds()[b][3]
+        if p.row_qvalid[r] < 128:
+            assert not fi
+        for j in fi:
+            assert (j + 1) * 128 <= kl
+        lst = p.partial_idx[p.partial_offset[r]:p.partial_offset[r + 1]].tolist()
+        assert lst == sorted(lst)
+
+
+def test_payload_bit_layout_single_element():
+    """One visible element at (row 5, col 70) of a tile lands in word 2, bit 6."""
+    import torch
+    S = 128
+    ends = np.zeros((1, 3, S), np.int32)
+    ends[0, :, :] = 0
+    ends[0, 1, 5] = 70     # row 5: [0,0) U [70,71)
+    ends[0, 2, 5] = 71
+    ends[0, 1, :] = np.maximum(ends[0, 1, :], ends[0, 0, :])
+    ends[0, 2, :] = np.maximum(ends[0, 2, :], ends[0, 1, :])
+    w = W.Workload("one", W.LAYOUT_BSHD, 1, S, S, 1, 1, 8, torch.zeros(1, S, 1, 8),
+                   torch.zeros(1, S, 1, 8), torch.zeros(1, S, 1, 8), 1.0, "intervals",
+                   mask_func=ends)
+    p = P.build_plan(w)
+    assert p.partial_idx.tolist() == [0] and p.full_idx.size == 0
+    want = np.zeros((128, 4), np.uint32)
+    want[5, 2] = 1 << 6
+    assert np.array_equal(p.payload[0], want)
+
+
+def test_malformed_inputs_raise():
+    w = _tiny_interval_workload(seed=1, B=1, S=64, nfunc=3)
+    w.mask_func[0, 1, 10] = w.mask_func[0, 0, 10] - 1 if w.mask_func[0, 0, 10] > 0 else 65
+    with pytest.raises(M.MaskError):
+        P.build_plan(w)
+    w = _tiny_interval_workload(seed=1, B=1, S=64, nfunc=1)
+    w.mask_func[0, 0, 3] = 65
+    with pytest.raises(M.MaskError):
+        P.build_plan(w)
+
+
+def test_schedule_brute_force_comparator():
+    w = _tiny_interval_workload(seed=21, B=0, S=0, nfunc=3, Hmask=2, H=2,
+                                varlen_lens=[300, 40, 520])
+    p = P.build_plan(w, 128, 128)
+    # enumerate tasks and compare with a comparator written from the §4.8 rules
+    items = []
+    for r in range(p.rows):
+        for h in range(2):
+            c = int(p.partial_count[h, r] + p.full_count[h, r])
+            items.append((int(p.row_batch[r]), h, int(p.row_mblock[r]), c, int(p.row_qvalid[r])))
+
+    def cmp(a, b):
+        if (a[3] > 0) != (b[3] > 0):
+            return -1 if a[3] > 0 else 1
+        if a[3] > 0:
+            sa, sb = a[0] * 2 + a[1], b[0] * 2 + b[1]
+            if sa != sb:
+                return -1 if sa < sb else 1
+            if a[3] != b[3]:
+                return -1 if a[3] > b[3] else 1
+        ta, tb = (a[0], a[1], a[2]), (b[0], b[1], b[2])
+        return (ta > tb) - (ta < tb)
+
+    items.sort(key=functools.cmp_to_key(cmp))
+    want = [(m, h, b, qv) for (b, h, m, c, qv) in items]
+    assert [tuple(x) for x in p.work_desc.tolist()] == want
+
+
+def test_sequence_desc_and_workload_shapes():
+    w = W.varlen_doc_causal(0)
+    lens = np.diff(w.cu_seqlens_q)
+    assert w.total_q == 16384 and lens.min() >= 256 and len(lens) == 8
+    w2 = W.tiny_causal(0)
+    p = P.build_plan(w2)
+    assert p.sequence_desc.tolist() == [[0, 0, 256, 256, 0, 2, 2, 0]]
+    assert p.partial_idx.tolist() == [0, 1] and p.full_idx.tolist() == [0]
+    assert p.visible_pairs == 256 * 257 // 2
