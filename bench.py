@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the masked-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch: plan build from the
+mask (host checks, GPU planner, one header readback, exact allocation,
+CSR + payload + schedule) followed by the masked forward.  Metric: TFLOPS on
+visible (q, k) pairs (4 * d FLOPs per visible pair), per step, with the plan
+build time reported beside it.  Default workload: sliding window (1024) +
+4-key sink, B=4, H=16, S=4096, d=128, bf16.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on bounded samples of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "masked attn fwd TFLOPS on visible pairs, % of GB300 BF16 roofline; plan build µs"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_DESC = {
+    "tiny_causal": "tiny causal B=1 H=2 S=256 d=64 BSHD",
+    "sliding_sink": "sliding window 1024 + sink 4, B=4 H=16 S=4096 d=128 BSHD",
+    "varlen_doc_causal": "varlen document-causal THD 16384 tokens / 8 docs, H=16 d=128",
+    "video_block_sparse": "block-sparse 64x64 blocks 10% + diagonal, B=1 H=24 S=32768 d=128",
+    "prefix_alibi_softcap": "prefixLM + ALiBi + softcap 50, B=2 H=32 S=8192 d=128",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sliding_sink", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "block_sparse_masked_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def known_traffic(workload: str):
+    """DRAM bytes per forward launch from a committed ncu summary, if it matches this kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kh = kernel_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == kh:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def visible_flops(info: dict, Hq: int, d: int) -> float:
+    vp = info["visible_pairs"]
+    heads = Hq if info["mask_heads"] == 1 else 1
+    return 4.0 * d * vp * heads
+
+
+def cpu_baseline(w, budget_s: float):
+    """Oracle (fp64, numpy) attention on a bounded sample of rows, visible TFLOPS."""
+    import numpy as np
+    from oracle import attention as OA
+    from oracle import mask as OM
+
+    rng = np.random.default_rng(0)
+    bounds = w.sample_bounds()
+    t0 = time.perf_counter()
+    flops = 0.0
+    rows_done = 0
+    pairs = 0
+    while time.perf_counter() - t0 < budget_s:
+        b = int(rng.integers(0, len(bounds)))
+        _, q_len, _, _ = bounds[b]
+        if q_len == 0:
+            continue
+        h = int(rng.integers(0, w.Hq))
+        start = int(rng.integers(0, max(1, q_len - 128)))
+        rows = np.arange(start, min(q_len, start + 128))
+        hm = 0 if w.Hmask == 1 else h
+        vis = OM.visible_rows(w, hm, b, rows)
+        OA.attention_rows(w, b, h, rows)
+        flops += 4.0 * w.d * float(vis.sum())
+        rows_done += rows.size
+        pairs += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{pairs} blocks of up to 128 consecutive Q rows of random (sample, head), "
+                      f"{rows_done} rows, all visible keys, fp64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    from block_sparse_masked_gb300 import workloads as W
+    w = W.make(args.workload, args.seed)
+    per_step = max(0.5, min(3.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, per_step / 4)
+    vals = []
+    t0 = time.perf_counter()
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline(w, per_step)
+        vals.append(last["value"])
+    wall = time.perf_counter() - t0
+    v = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from block_sparse_masked_gb300 import build as fb
+
+    if world > 1:
+        if local == 0:
+            fb.build()
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist.barrier()
+    else:
+        fb.build()
+    torch.cuda.set_device(local)
+    import block_sparse_masked_gb300 as fa
+    from block_sparse_masked_gb300 import runner
+    from block_sparse_masked_gb300 import workloads as W
+
+    w = W.make(args.workload, args.seed + rank)
+    dp = runner.to_device(w)
+    stream = torch.cuda.current_stream()
+    plan = runner.build_plan(dp)
+    info = fa.fa_plan_info_get(plan, count_visible=True)
+    plan.free()
+    flops_step = visible_flops(info, w.Hq, w.d)
+    launches_per_step = 8 + (1 if info["header"][1] > 0 else 0) + 1  # planner kernels + forward
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        p = runner.build_plan(dp)
+        if ev is not None:
+            ev[1].record(stream)
+        runner.forward(dp, p)
+        if ev is not None:
+            ev[2].record(stream)
+        bu = fa.fa_plan_info_get(p)["build_us"]
+        p.free()
+        return bu
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    build_us = []
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush outside the per-step events
+        build_us.append(step(evs[i]))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+    fwd_mean = statistics.mean(fwd_ms)
+    fwd_tflops = flops_step / (fwd_mean * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D inputs, plan, forward, D2H output
+    hq = [t.pin_memory() for t in (w.q, w.k, w.v)]
+    hmask = torch.from_numpy(np.ascontiguousarray(
+        w.mask_func if w.mask_kind == "intervals" else w.block_mask)).pin_memory()
+    ho = torch.empty(dp.o.shape, dtype=dp.o.dtype).pin_memory()
+    hl = torch.empty(dp.lse.shape, dtype=dp.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hq) + hmask.numel() * hmask.element_size()
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        for dst, src in zip((dp.q, dp.k, dp.v, dp.mask), (*hq, hmask)):
+            dst.copy_(src, non_blocking=True)
+        p = runner.build_plan(dp)
+        runner.forward(dp, p)
+        ho.copy_(dp.o, non_blocking=True)
+        hl.copy_(dp.lse, non_blocking=True)
+        p.free()
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ksteps = max(5, args.steps // 2)
+    e0.record(stream)
+    for _ in range(ksteps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / ksteps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
+    assert fa.fa_device_error_flags() == 0, "device error flags set"
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    traffic = known_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "seed": args.seed,
+                   "step": "plan build + masked forward",
+                   "l2": "256 MB buffer written between timed steps; inputs 201 MB > L2"
+                   if args.workload == "sliding_sink" else "256 MB buffer written between timed steps"},
+        "plan_build_us": statistics.median(build_us),
+        "plan_gpu_ms": statistics.median(plan_ms),
+        "fwd_ms": fwd_mean,
+        "fwd_tflops": fwd_tflops,
+        "visible_pairs": info["visible_pairs"] * (w.Hq if info["mask_heads"] == 1 else 1),
+        "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": fwd_tflops / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone per event pair)",
+                     "kernel": "k_fwd (attention forward)"},
+        "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+// internal.h -- host-side plan object and kernel launchers shared by the
+// C ABI (fa_api.cu), the planner (planner.cu) and the attention forward
+// (attn_fwd*.cu).  Not part of the public interface.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/fa.h"
+
+namespace bsm {
+
+constexpr int kTile = 128;            // physical tile, Q rows and K columns
+constexpr int kPayloadWords = 4;      // uint32 words per tile row
+constexpr int kMaxHeads = 256;        // heads_q limit of the forward kernel parameters
+
+enum PlanErr : uint32_t { PLANERR_MASK = 1u, PLANERR_SEQLENS = 2u, PLANERR_OVERFLOW = 4u };
+enum MaskKind : int { MASK_INTERVALS = 0, MASK_BLOCKS = 1 };
+
+// Consumer signature ("Flex Attention Mask Plan Design" §7): every field
+// that fixes how the plan's topology and payload are laid out for the one
+// consumer this library ships.
+struct Signature {
+  int32_t arch = 103;        // sm_103a
+  int32_t direction = 0;     // forward
+  int32_t kernel_family = 1; // tcgen05/TMEM forward, one Q tile per CTA
+  int32_t tile_q = kTile, tile_k = kTile;
+  int32_t q_stage = 1, cta_group = 1, pack_gqa = 0;
+  int32_t payload_layout = 1;   // one TMEM lane per row, 4 words, bit l = column 32w+l
+  int32_t scheduler_layout = 1; // work_desc in execution order, one task per CTA
+  uint64_t hash() const;
+};
+
+struct Geometry {
+  int32_t layout, batch, seqlen_q, seqlen_k, total_q, total_k, heads_q, heads_k, head_dim, dtype;
+};
+
+struct DeviceMem {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace bsm
+
+struct fa_plan {
+  bsm::Geometry geom;
+  int32_t Hmask = 1;
+  int32_t mask_kind = 0;
+  int64_t rows = 0, P = 0, F = 0, tasks = 0;
+  int64_t header[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint64_t signature = 0;
+  int device = 0;
+  double build_us = 0;
+  fa_allocator alloc{};
+  bool custom_alloc = false;
+  bsm::DeviceMem mem;
+  // views into mem
+  int32_t* cu_q_rows = nullptr;     // [B+1]
+  int32_t* seq_desc = nullptr;      // [B*8]
+  int32_t* p_off = nullptr;         // [Hmask*rows+1]
+  int32_t* f_off = nullptr;
+  int32_t* p_idx = nullptr;         // [P]
+  int32_t* f_idx = nullptr;         // [F]
+  uint32_t* payload = nullptr;      // [P*128*4]
+  int32_t* work_desc = nullptr;     // [tasks*4]
+  int32_t* cu_seqlens_q = nullptr;  // clones (THD)
+  int32_t* cu_seqlens_k = nullptr;
+};
+
+namespace bsm {
+
+// ---- planner launchers (planner.cu) -------------------------------------
+struct PlanWorkspace {
+  uint32_t* err;
+  long long* header;      // 8 values
+  int32_t* cu_rows;       // [B+1]
+  int32_t* seq;           // [B*8]
+  int32_t* row_batch;     // [rows_ub]
+  uint32_t* vis_bits;     // [Hmask*rows_ub*words]
+  uint32_t* full_bits;
+  int32_t* p_cnt;         // [Hmask*rows_ub]
+  int32_t* f_cnt;
+  int32_t* p_off;         // [Hmask*rows_ub+1]
+  int32_t* f_off;
+  int rows_ub, kt_ub, words;
+};
+
+struct MaskArgs {
+  int kind;
+  const int32_t* mask_func;   // intervals
+  int nfunc;
+  const uint8_t* block_mask;  // blocks
+  int block_q, block_kv, nbq, nbk;
+  int Hmask;
+};
+
+cudaError_t launch_geometry(const Geometry& g, const int32_t* cu_q, const int32_t* cu_k,
+                            const PlanWorkspace& ws, cudaStream_t st);
+cudaError_t launch_classify(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
+                            cudaStream_t st);
+cudaError_t launch_scan_header(const Geometry& g, int Hmask, const PlanWorkspace& ws,
+                               cudaStream_t st);
+// After the header: CSR lists, the entry->row map, payloads and the schedule.
+cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
+                               fa_plan* plan, int32_t* entry_row, cudaStream_t st);
+cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, fa_plan* plan,
+                            int32_t* hist, int32_t* cursors, int num_sections, int max_cost,
+                            cudaStream_t st);
+cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, cudaStream_t st);
+
+// ---- forward (attn_fwd*.cu) ---------------------------------------------
+struct FwdLaunch {
+  const fa_plan* plan;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  float scale;
+  int flags;
+  float softcap;
+  const float* slopes;  // host, heads_q
+};
+cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why);
+cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why);
+uint32_t* fwd_error_word();  // device address of the forward kernels' error word
+
+}  // namespace bsm

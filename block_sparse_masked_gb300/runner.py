@@ -1,0 +1,65 @@
+"""Convenience marshalling for a Workload: device copies, geometry, plan, forward.
+
+Used by the tests, the smoke check and the benchmark.  It only moves tensors
+and forwards arguments to the C ABI; all computation is in the library.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import (FA_LAYOUT_BSHD, FaGeometry, Plan, fa_fwd, fa_plan_build_blocks,
+               fa_plan_build_intervals, geometry)
+from .workloads import Workload
+
+
+@dataclasses.dataclass
+class DeviceProblem:
+    w: Workload
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    mask: torch.Tensor
+    cu_q: Optional[torch.Tensor]
+    cu_k: Optional[torch.Tensor]
+    geom: FaGeometry
+    o: torch.Tensor
+    lse: torch.Tensor
+
+
+def to_device(w: Workload, device="cuda") -> DeviceProblem:
+    q, k, v = (t.to(device).contiguous() for t in (w.q, w.k, w.v))
+    if w.mask_kind == "intervals":
+        mask = torch.from_numpy(np.ascontiguousarray(w.mask_func)).to(device)
+    else:
+        mask = torch.from_numpy(np.ascontiguousarray(w.block_mask)).to(device)
+    cu_q = cu_k = None
+    if w.layout == FA_LAYOUT_BSHD:
+        g = geometry(FA_LAYOUT_BSHD, w.B, w.Sq, w.Sk, w.Hq, w.Hk, w.d)
+    else:
+        cu_q = torch.from_numpy(w.cu_seqlens_q.astype(np.int32)).to(device)
+        cu_k = torch.from_numpy(w.cu_seqlens_k.astype(np.int32)).to(device)
+        g = geometry(w.layout, w.B, w.Sq, w.Sk, w.Hq, w.Hk, w.d, total_q=w.total_q,
+                     total_k=w.total_k, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.Hq, w.total_q, dtype=torch.float32, device=device)
+    return DeviceProblem(w, q, k, v, mask, cu_q, cu_k, g, o, lse)
+
+
+def build_plan(dp: DeviceProblem, stream=None) -> Plan:
+    w = dp.w
+    if w.mask_kind == "intervals":
+        return fa_plan_build_intervals(dp.geom, dp.mask, w.mask_func.shape[0], w.mask_func.shape[1],
+                                       stream=stream)
+    return fa_plan_build_blocks(dp.geom, dp.mask, w.block_mask.shape[0], w.block_q, w.block_kv,
+                                stream=stream)
+
+
+def forward(dp: DeviceProblem, plan: Plan, stream=None):
+    w = dp.w
+    fa_fwd(plan, dp.q, dp.k, dp.v, dp.o, dp.lse, dp.geom, w.scale, softcap=w.softcap,
+           alibi_slopes=w.alibi_slopes, stream=stream)
+    return dp.o, dp.lse

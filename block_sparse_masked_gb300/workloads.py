@@ -78,6 +78,15 @@ class Workload:
         m = self.mask_func if self.mask_kind == "intervals" else self.block_mask
         return int(m.shape[0])
 
+    def mask_only(self) -> "Workload":
+        """Copy with zero-width Q/K/V (same leading shapes): cheap to pickle."""
+        z = lambda t: torch.empty(tuple(t.shape[:-1]) + (0,), dtype=t.dtype)
+        c = dataclasses.replace(self, q=z(self.q), k=z(self.k), v=z(self.v))
+        for extra in ("prefix",):
+            if hasattr(self, extra):
+                setattr(c, extra, getattr(self, extra))
+        return c
+
     def sample_bounds(self):
         """[(q_offset, q_len, k_offset, k_len)] per sample, in token rows."""
         if self.layout == LAYOUT_BSHD:

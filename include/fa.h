@@ -1,0 +1,240 @@
+/*
+ * fa.h -- C ABI of the interval-masked / block-sparse attention forward
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * Two steps, both on one GPU:
+ *
+ *   1. A GPU planner turns a mask into an immutable, reusable MaskPlan
+ *      ("Flex Attention Mask Plan Design", cuDNN frontend documentation,
+ *      §4 Planner Overview, §8 Plan Ownership and Reuse).
+ *   2. fa_fwd consumes the plan and computes
+ *          O = softmax(mod(Q K^T * scale)) V   and   LSE = ln sum exp(mod(.))
+ *      (FlexAttention Eq. 1, and the same page §6.1 Forward for the
+ *      consumption protocol).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" must point to memory of the current CUDA
+ *     device; pointers marked "host" to ordinary host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All GPU work is enqueued on it.
+ *   - Return value: FA_OK (0) or a negative FA_ERR_* code.  On error no
+ *     output is produced (`*out` stays NULL) and nothing leaks;
+ *     fa_last_error() gives a message for the calling thread.
+ *   - Head dimension 64 or 128, bf16 Q/K/V/O, fp32 LSE, physical tiles of
+ *     128 x 128 (Q rows x K columns).
+ */
+#ifndef BSM_FA_H
+#define BSM_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,     /* host-side structural check failed           */
+  FA_ERR_INVALID_MASK = -2,    /* an endpoint is out of range / out of order  */
+  FA_ERR_INVALID_SEQLENS = -3, /* cu_seqlens prefix check failed on the GPU   */
+  FA_ERR_PLAN_MISMATCH = -4,   /* plan signature or geometry differs          */
+  FA_ERR_ALLOC = -5,           /* device or host allocation failed            */
+  FA_ERR_CUDA = -6,            /* a CUDA runtime / driver call failed         */
+  FA_ERR_DEVICE_TIMEOUT = -7,  /* a bounded in-kernel wait ran out            */
+  FA_ERR_UNSUPPORTED = -8      /* valid request outside what this build runs  */
+};
+
+enum { FA_LAYOUT_BSHD = 0, FA_LAYOUT_THD = 1 };
+enum { FA_DTYPE_BF16 = 0 };
+enum { FA_MOD_SOFTCAP = 1, FA_MOD_ALIBI = 2 };
+
+/* Physical tile of this build's consumer. */
+#define FA_TILE_Q 128
+#define FA_TILE_K 128
+/* uint32 words of packed predicate per tile row (128 columns / 32). */
+#define FA_PAYLOAD_WORDS 4
+
+typedef struct fa_plan fa_plan; /* opaque, immutable after build */
+
+/*
+ * Problem geometry ("Flex Attention Mask Plan Design" §3.1 Fixed Length,
+ * §3.2 Varlen).
+ *   layout FA_LAYOUT_BSHD: Q is [batch, seqlen_q, heads_q, head_dim] and K/V
+ *     are [batch, seqlen_k, heads_k, head_dim], contiguous; total_q/total_k
+ *     and cu_seqlens_* are ignored.
+ *   layout FA_LAYOUT_THD: Q is [total_q, heads_q, head_dim], K/V are
+ *     [total_k, heads_k, head_dim]; sample b owns Q rows
+ *     [cu_seqlens_q[b], cu_seqlens_q[b+1]) and K rows likewise.
+ *     cu_seqlens_q/k are device int32 [batch+1]; seqlen_q/k are the maximum
+ *     sample lengths (max_seqlen_q/k).  The planner validates the prefixes
+ *     on the GPU (start 0, end total, nondecreasing, within the maxima) and
+ *     the plan keeps its own copies, so the caller may change or free them
+ *     after the build returns.
+ *   heads_q must be a multiple of heads_k (GQA: Q head h reads K/V head
+ *   h / (heads_q / heads_k)).
+ */
+typedef struct {
+  int32_t layout;
+  int32_t batch;
+  int32_t seqlen_q;
+  int32_t seqlen_k;
+  int32_t total_q;
+  int32_t total_k;
+  const int32_t* cu_seqlens_q; /* device, THD only */
+  const int32_t* cu_seqlens_k; /* device, THD only */
+  int32_t heads_q;
+  int32_t heads_k;
+  int32_t head_dim;            /* 64 or 128 */
+  int32_t dtype;               /* FA_DTYPE_BF16 */
+} fa_geometry;
+
+/*
+ * Optional allocator for plan and workspace memory.  alloc returns device
+ * memory of at least `bytes` usable in stream order on `stream` (NULL on
+ * failure); free releases it in stream order.  Pass NULL to use the
+ * library's own stream-ordered pool (cudaMallocAsync-style).
+ */
+typedef struct {
+  void* (*alloc)(size_t bytes, void* stream, void* ctx);
+  void (*free)(void* ptr, size_t bytes, void* stream, void* ctx);
+  void* ctx;
+} fa_allocator;
+
+/*
+ * Build a plan from per-row interval endpoints ("Flex Attention Mask Plan
+ * Design" §2 Public Mask Representation, §4.2-§4.6, §4.8, §5).
+ *   mask_func: device int32 [Hmask, nfunc, total_q] (BSHD: total_q =
+ *     batch*seqlen_q, rows batch-major).  Row q's visible keys are
+ *     [0,F0) U [F1,F2) U ... with sample-local key positions and
+ *     0 <= F0 <= ... <= F(nfunc-1) <= k_len of the row's sample.
+ *   Hmask: 1 (one mask for every Q head) or heads_q.  nfunc: odd, >= 1.
+ * The build validates every endpoint and (THD) prefix on the GPU, reads an
+ * 8-value header back once (the only host/device synchronisation), then
+ * allocates exact-size outputs.  Malformed endpoints return
+ * FA_ERR_INVALID_MASK, malformed prefixes FA_ERR_INVALID_SEQLENS; no plan
+ * is produced.  The caller owns mask_func and may reuse it after return.
+ * On success *out receives a plan the caller must release with fa_plan_free.
+ */
+int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func,
+                            int32_t Hmask, int32_t nfunc, const fa_allocator* allocator,
+                            void* stream, fa_plan** out);
+
+/*
+ * Build a plan from a logical block-pair mask ("Decoupling Logical Masks
+ * from GPU Execution for Dynamic Block-Sparse Attention" §2: mask M with
+ * logical geometry B = (block_q, block_kv), effective set E(M); physical
+ * tiles T = 128 x 128 are chosen independently of B).
+ *   block_mask: device uint8 [Hmask, ceil(seqlen_q/block_q),
+ *     ceil(seqlen_k/block_kv)]; nonzero = active block pair.  Token pair
+ *     (q, k) is visible iff its block pair is active and q < seqlen_q,
+ *     k < seqlen_k.  Fixed-length (BSHD) geometry only; the same mask is
+ *     applied to every sample.
+ * Errors and ownership as for fa_plan_build_intervals.
+ */
+int fa_plan_build_blocks(const fa_geometry* geom, const uint8_t* block_mask, int32_t Hmask,
+                         int32_t block_q, int32_t block_kv, const fa_allocator* allocator,
+                         void* stream, fa_plan** out);
+
+/*
+ * Release a plan.  NULL is accepted.  Device memory is returned in stream
+ * order on `stream`: the caller must make sure no work that reads the plan
+ * is still pending on any other stream.
+ */
+int fa_plan_free(fa_plan* plan, void* stream);
+
+/* Score modifications applied after scaling (FlexAttention score_mod):
+ *   FA_MOD_SOFTCAP: s <- softcap * tanh(s / softcap)
+ *   FA_MOD_ALIBI:   s <- s + alibi_slopes[h] * (k - q)   (sample-local k, q)
+ * applied in that order.  alibi_slopes is a host array of heads_q floats,
+ * read during the call. */
+typedef struct {
+  int32_t flags;
+  float softcap;
+  const float* alibi_slopes;
+} fa_mods;
+
+/*
+ * Masked attention forward ("Flex Attention Mask Plan Design" §6.1):
+ * for every (sample, Q head, Q tile) task of the plan, partial tiles are
+ * computed with the packed predicate, full tiles without, empty tiles are
+ * skipped; rows without a visible key get O = 0 and LSE = -inf.
+ *   q, k, v: device bf16 in the geometry's layout; o: device bf16, same
+ *   layout as q; lse: device float32 [heads_q, total_q] (natural log), may
+ *   be NULL.  scale multiplies Q K^T before the mods.  mods may be NULL.
+ * Every base pointer must be 16-byte aligned.  The geometry must equal the
+ * one the plan was built for (FA_ERR_PLAN_MISMATCH otherwise).  The call
+ * is asynchronous on `stream`; one plan may be used concurrently on
+ * several streams.
+ */
+int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, void* o,
+           float* lse, const fa_geometry* geom, float scale, const fa_mods* mods,
+           void* stream);
+
+/* Plan statistics and layout sizes (Tessera-style mask statistics). */
+typedef struct {
+  int64_t header[8];      /* fwd Q rows, partial nnz, full nnz, 0, 0, 0, 0, error flags */
+  int32_t tile_q, tile_k;
+  int32_t mask_heads;     /* Hmask */
+  int32_t batch;
+  int32_t heads_q, heads_k, head_dim, layout;
+  int64_t num_tasks;      /* fwd Q rows * heads_q */
+  int64_t payload_bytes;  /* partial nnz * 128 * 4 * 4 */
+  int64_t plan_bytes;     /* device bytes owned by the plan */
+  int64_t visible_pairs;  /* visible (q,k) pairs summed over mask heads; -1 unless requested */
+  uint64_t signature;     /* consumer signature (§7); equal plans share it */
+  double build_us;        /* host wall time of the build call */
+} fa_plan_info;
+
+/*
+ * Fill `info`.  With count_visible != 0 the visible pairs are counted on
+ * the GPU (stream-synchronous); otherwise info->visible_pairs = -1.
+ */
+int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream,
+                     fa_plan_info* info);
+
+/*
+ * Debug snapshot ("Flex Attention Mask Plan Design" §8 debug_snapshot):
+ * copy the plan's arrays to caller-owned host buffers (each may be NULL to
+ * skip).  Sizes, with R = header[0], P = header[1], F = header[2],
+ * Hm = mask_heads, T = num_tasks:
+ *   cu_q_rows [batch+1], sequence_desc [batch*8]
+ *   (q_offset, k_offset, q_len, k_len, row begin, row count, K tiles, 0),
+ *   partial_offset / full_offset [Hm*R+1] (row-major over (mask head, row)),
+ *   partial_idx [P], full_idx [F] (sample-local K tile indices, ascending
+ *   per row), payload [P*128*4] (entry e, tile row r, word w: bit l keeps
+ *   column 32*w+l), work_desc [T*4] (m_block, head, batch, q_valid_rows) in
+ *   execution order.  Synchronous.
+ */
+typedef struct {
+  int32_t* cu_q_rows;
+  int32_t* sequence_desc;
+  int32_t* partial_offset;
+  int32_t* partial_idx;
+  int32_t* full_offset;
+  int32_t* full_idx;
+  uint32_t* payload;
+  int32_t* work_desc;
+} fa_plan_host_view;
+
+int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);
+
+/*
+ * Error bits written by the forward kernels on the current device (bit 0:
+ * a bounded in-kernel wait ran out and the kernel stopped early, so its
+ * output is incomplete).  Synchronises `stream`, returns the bits in
+ * *flags and clears them.
+ */
+int fa_device_error_flags(void* stream, uint32_t* flags);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* fa_last_error(void);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSM_FA_H */

@@ -89,13 +89,19 @@ def _pack_tiles(tiles: np.ndarray) -> np.ndarray:
     nw = -(-T_KV // 32)
     padded = np.zeros((n, T_Q, nw * 32), dtype=bool)
     padded[:, :, :T_KV] = tiles.transpose(1, 0, 2)
-    weights = (np.uint64(1) << np.arange(32, dtype=np.uint64))
-    words = (padded.reshape(n, T_Q, nw, 32).astype(np.uint64) * weights).sum(axis=3)
-    return words.astype(np.uint32)
+    # little bit order: column 32w+l -> byte 4w + l//8, bit l%8 -> bit l of the LE word w
+    packed = np.packbits(padded, axis=2, bitorder="little")
+    return np.ascontiguousarray(packed).view("<u4").reshape(n, T_Q, nw).astype(np.uint32)
 
 
-def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True) -> Plan:
-    """Build the plan for workload ``w`` by dense expansion (raises MaskError on bad input)."""
+def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
+               mask_heads=None) -> Plan:
+    """Build the plan for workload ``w`` by dense expansion (raises MaskError on bad input).
+
+    ``mask_heads`` restricts the build to those mask heads (the result then
+    covers only them, in the given order, and carries no schedule); it exists
+    so that large plans can be built one head per process and merged.
+    """
     bounds = w.sample_bounds()
     B = len(bounds)
     if w.layout == 1:
@@ -110,6 +116,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True) ->
     Hmask = w.Hmask
     if Hmask not in (1, w.Hq):
         raise M.MaskError("Hmask must be 1 or Hq")
+    heads = list(range(Hmask)) if mask_heads is None else list(mask_heads)
 
     q_rows = np.array([-(-ql // T_Q) for (_, ql, _, _) in bounds], dtype=np.int64)
     k_tiles = np.array([-(-kl // T_KV) for (_, _, _, kl) in bounds], dtype=np.int64)
@@ -120,11 +127,11 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True) ->
     row_qvalid = np.array([min(T_Q, bounds[b][1] - m * T_Q) for b, m in zip(row_batch, row_mblock)],
                           dtype=np.int64)
 
-    p_cnt = np.zeros((Hmask, rows), np.int64)
-    f_cnt = np.zeros((Hmask, rows), np.int64)
+    p_cnt = np.zeros((len(heads), rows), np.int64)
+    f_cnt = np.zeros((len(heads), rows), np.int64)
     p_lists, f_lists, payloads = [], [], []
     visible_pairs = 0
-    for hm in range(Hmask):
+    for slot, hm in enumerate(heads):
         for r in range(rows):
             b, m = int(row_batch[r]), int(row_mblock[r])
             q_off, q_len, k_off, k_len = bounds[b]
@@ -135,8 +142,8 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True) ->
             partial = visible & ~full
             pi = np.nonzero(partial)[0]
             fi = np.nonzero(full)[0]
-            p_cnt[hm, r] = pi.size
-            f_cnt[hm, r] = fi.size
+            p_cnt[slot, r] = pi.size
+            f_cnt[slot, r] = fi.size
             p_lists.append(pi)
             f_lists.append(fi)
             if with_payload and pi.size:
@@ -156,8 +163,11 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True) ->
     for b, (q_off, q_len, k_off, k_len) in enumerate(bounds):
         seq[b] = (q_off, k_off, q_len, k_len, cu_q_rows[b], q_rows[b], k_tiles[b], 0)
 
-    work = schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, w.Hq, w.Hk, Hmask)
-    return Plan(T_Q, T_KV, Hmask, w.Hq, w.Hk, rows, cu_q_rows, k_tiles, row_batch, row_mblock,
+    if mask_heads is None:
+        work = schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, w.Hq, w.Hk, Hmask)
+    else:
+        work = np.zeros((0, 4), np.int64)
+    return Plan(T_Q, T_KV, len(heads), w.Hq, w.Hk, rows, cu_q_rows, k_tiles, row_batch, row_mblock,
                 row_qvalid, p_cnt, f_cnt, _csr(p_cnt), _csr(f_cnt), partial_idx, full_idx,
                 payload, seq, work, visible_pairs)
 
@@ -210,3 +220,38 @@ def visible_from_plan(p: Plan, hm: int, b: int, q_len: int, k_len: int) -> np.nd
             dense = dense.reshape(T_Q, -1)[:, :T_KV]
             out[m * T_Q:(m + 1) * T_Q, j * T_KV:(j + 1) * T_KV] |= dense
     return out[:q_len, :k_len]
+
+
+def _one_head(args):
+    w, T_Q, T_KV, hm = args
+    return build_plan(w, T_Q, T_KV, True, mask_heads=[hm])
+
+
+def build_plan_by_heads(w, T_Q: int = 128, T_KV: int = 128, processes: int = 8) -> Plan:
+    """Same result as build_plan(w), one mask head per worker process (spawned).
+
+    ``w`` should be a mask-only workload (see Workload.mask_only) so that it
+    pickles cheaply.  Per-head plans are concatenated in head order, which is
+    exactly the row-major (mask head, row) layout of the CSR.
+    """
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(processes) as pool:
+        parts = pool.map(_one_head, [(w, T_Q, T_KV, hm) for hm in range(w.Hmask)])
+    first = parts[0]
+    p_cnt = np.concatenate([q.partial_count for q in parts])
+    f_cnt = np.concatenate([q.full_count for q in parts])
+
+    def _csr(cnt):
+        off = np.zeros(cnt.size + 1, np.int64)
+        off[1:] = np.cumsum(cnt.reshape(-1))
+        return off
+
+    work = schedule(first.row_batch, first.row_mblock, first.row_qvalid, p_cnt, f_cnt, w.Hq, w.Hk,
+                    w.Hmask)
+    return Plan(T_Q, T_KV, w.Hmask, w.Hq, w.Hk, first.rows, first.cu_q_rows, first.k_tiles,
+                first.row_batch, first.row_mblock, first.row_qvalid, p_cnt, f_cnt, _csr(p_cnt),
+                _csr(f_cnt), np.concatenate([q.partial_idx for q in parts]),
+                np.concatenate([q.full_idx for q in parts]),
+                np.concatenate([q.payload for q in parts]), first.sequence_desc, work,
+                sum(q.visible_pairs for q in parts))

@@ -1,0 +1,147 @@
+"""GPU forward vs the fp64 oracle through the C ABI: O max-abs <= 2e-2 and
+|LSE error| <= 1e-3.  Small problems are compared on every row; the full
+workloads on sampled rows (tile edges, sample tails and random rows)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_masked_gb300 as fa
+from block_sparse_masked_gb300 import runner
+from block_sparse_masked_gb300 import workloads as W
+
+import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    PT.ensure_built()
+
+
+def run(w):
+    dp = runner.to_device(w)
+    plan = runner.build_plan(dp)
+    runner.forward(dp, plan)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error_flags() == 0
+    return dp, plan
+
+
+def all_rows(w):
+    return {(b, h): list(range(ql)) for b, (_, ql, _, _) in enumerate(w.sample_bounds())
+            for h in range(w.Hq) if ql > 0}
+
+
+def test_tiny_causal_all_rows():
+    w = W.tiny_causal(0)
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+def _random_problem(seed, B, S, H, d, nfunc, Hk=None, Hmask=1, lens=None, softcap=0.0,
+                    alibi=False, Sk=None):
+    gen = torch.Generator().manual_seed(seed)
+    Hk = H if Hk is None else Hk
+    Sk = S if Sk is None else Sk
+    if lens is None:
+        q = torch.randn(B, S, H, d, generator=gen).bfloat16()
+        k = torch.randn(B, Sk, Hk, d, generator=gen).bfloat16()
+        v = torch.randn(B, Sk, Hk, d, generator=gen).bfloat16()
+        mf = W.random_intervals(seed, B, S, Sk, nfunc, Hmask)
+        w = W.Workload("rand", W.LAYOUT_BSHD, B, S, Sk, H, Hk, d, q, k, v, 1 / math.sqrt(d),
+                       "intervals", mask_func=mf)
+    else:
+        lens = np.array(lens)
+        tot = int(lens.sum())
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        q = torch.randn(tot, H, d, generator=gen).bfloat16()
+        k = torch.randn(tot, Hk, d, generator=gen).bfloat16()
+        v = torch.randn(tot, Hk, d, generator=gen).bfloat16()
+        mf = W.random_intervals(seed, len(lens), 0, 0, nfunc, Hmask, lens_q=lens, lens_k=lens)
+        mx = int(lens.max())
+        w = W.Workload("rand_varlen", W.LAYOUT_THD, len(lens), mx, mx, H, Hk, d, q, k, v,
+                       1 / math.sqrt(d), "intervals", mask_func=mf, cu_seqlens_q=cu,
+                       cu_seqlens_k=cu.copy())
+    w.softcap = softcap
+    if alibi:
+        w.alibi_slopes = W.alibi_slopes(H)
+    return w
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("case", [
+    dict(seed=1, B=2, S=300, H=2, nfunc=1),
+    dict(seed=2, B=1, S=513, H=2, nfunc=3),
+    dict(seed=3, B=1, S=400, H=4, Hk=2, nfunc=5, Hmask=4),       # GQA + per-head masks
+    dict(seed=4, B=1, S=260, H=2, nfunc=3, Sk=700),              # Sq != Sk
+    dict(seed=5, B=0, S=0, H=2, nfunc=3, lens=[70, 1, 129, 0, 300, 260]),
+    dict(seed=6, B=1, S=384, H=2, nfunc=3, softcap=5.0),
+    dict(seed=7, B=1, S=384, H=2, nfunc=3, alibi=True),
+    dict(seed=8, B=2, S=333, H=2, nfunc=1, softcap=50.0, alibi=True),
+])
+def test_random_small_all_rows(d, case):
+    w = _random_problem(d=d, **case)
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_mask_small_all_rows(d):
+    S, BQ, BKV = 700, 48, 80
+    gen = torch.Generator().manual_seed(9)
+    q, k, v = (torch.randn(1, S, 2, d, generator=gen).bfloat16() for _ in range(3))
+    bm = W.random_block_mask(9, 2, -(-S // BQ), -(-S // BKV), 0.25)
+    w = W.Workload("blk", W.LAYOUT_BSHD, 1, S, S, 2, 2, d, q, k, v, 1 / math.sqrt(d), "blocks",
+                   block_mask=bm, block_q=BQ, block_kv=BKV)
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+def test_rows_without_visible_keys():
+    w = _random_problem(10, B=1, S=300, H=2, d=64, nfunc=3)
+    w.mask_func[:] = 0               # nothing visible anywhere
+    w.mask_func[0, :, 130] = [0, 5, 7]  # except two keys of row 130
+    dp, plan = run(w)
+    lse = dp.lse.cpu()
+    assert torch.all(torch.isinf(lse[:, :130])) and torch.all(lse[:, :130] < 0)
+    assert torch.all(dp.o.float().cpu()[0, :130] == 0)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+def test_plan_reuse_with_new_values_and_mismatch():
+    w = _random_problem(11, B=1, S=300, H=2, d=64, nfunc=3)
+    dp, plan = run(w)
+    gen = torch.Generator().manual_seed(12)
+    w2 = W.Workload(**{**w.__dict__, "q": torch.randn(1, 300, 2, 64, generator=gen).bfloat16(),
+                       "v": torch.randn(1, 300, 2, 64, generator=gen).bfloat16()})
+    dp2 = runner.to_device(w2)
+    runner.forward(dp2, plan)
+    torch.cuda.synchronize()
+    PT.check_rows(w2, dp2.o, dp2.lse, all_rows(w2))
+    g_bad = fa.geometry(fa.FA_LAYOUT_BSHD, 1, 301, 300, 2, 2, 64)
+    with pytest.raises(fa.FaError) as ei:
+        fa.fa_fwd(plan, dp.q, dp.k, dp.v, dp.o, dp.lse, g_bad, 0.125)
+    assert ei.value.code == fa.FA_ERR_PLAN_MISMATCH
+    plan.free()
+
+
+@pytest.mark.parametrize("name,per_head,heads", [
+    ("sliding_sink", 256, None),
+    ("varlen_doc_causal", 256, None),
+    ("prefix_alibi_softcap", 128, None),
+    ("video_block_sparse", 512, [0, 5, 11, 17, 23]),
+])
+def test_full_workload_sampled_rows(name, per_head, heads):
+    w = W.make(name, 0)
+    dp, plan = run(w)
+    rows = PT.sample_rows(w, per_head, seed=1, heads=heads)
+    eo, el = PT.check_rows(w, dp.o, dp.lse, rows)
+    print(f"{name}: O max-abs {eo:.3e}, LSE max-abs {el:.3e}")
+    plan.free()
