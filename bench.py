@@ -275,6 +275,7 @@ def main():
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()  # L2 flush outside the per-step events
+        torch.cuda.synchronize()  # each step starts from a drained queue
         build_us.append(step(evs[i]))
     torch.cuda.synchronize()
     if world > 1:
