@@ -105,10 +105,12 @@ def lib():
         L.fa_plan_info_get.argtypes = [_vp, _i32, _vp, P(FaPlanInfo)]
         L.fa_plan_export.argtypes = [_vp, P(FaPlanHostView)]
         L.fa_device_error_flags.argtypes = [_vp, P(_u32)]
+        L.fa_plan_header_noalloc.argtypes = [P(FaGeometry), _vp, _i32, _i32, _vp, _vp]
         L.fa_last_error.restype = _c.c_char_p
         L.fa_version.restype = _c.c_char_p
         for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_free", "fa_fwd",
-                  "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags"):
+                  "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags",
+                  "fa_plan_header_noalloc"):
             getattr(L, f).restype = _c.c_int
         _LIB = L
     return _LIB
@@ -258,3 +260,10 @@ def fa_device_error_flags(stream=None) -> int:
     v = _u32(0)
     _check(lib().fa_device_error_flags(_stream_handle(stream), _c.byref(v)))
     return v.value
+
+
+def fa_plan_header_noalloc(geom: FaGeometry, mask_func, Hmask: int, nfunc: int, header_out,
+                           stream=None):
+    """Allocation-free plan sizing: writes the 8-value header into header_out (device int64[8])."""
+    _check(lib().fa_plan_header_noalloc(_c.byref(geom), _ptr(mask_func), Hmask, nfunc,
+                                        _ptr(header_out), _stream_handle(stream)))

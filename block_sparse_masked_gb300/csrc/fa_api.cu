@@ -318,6 +318,19 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
 }  // namespace
 
 namespace bsm {
+void clear_last_error() { t_err.clear(); }
+int report_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+int check_geometry_public(const fa_geometry* g) { return check_geometry(g); }
+Geometry geometry_public(const fa_geometry* g) { return to_geom(g); }
+
 uint64_t Signature::hash() const {
   uint64_t h = 1469598103934665603ull;
   for (int64_t v : {int64_t(arch), int64_t(direction), int64_t(kernel_family), int64_t(tile_q),

@@ -126,4 +126,10 @@ cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
 
+// ---- error reporting and argument checks shared with fa_plan_header_noalloc
+void clear_last_error();
+int report_error(int code, const char* fmt, ...);
+int check_geometry_public(const fa_geometry* g);
+Geometry geometry_public(const fa_geometry* g);
+
 }  // namespace bsm

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 
@@ -689,3 +690,111 @@ cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, c
 }
 
 }  // namespace bsm
+
+// ================================================= allocation-free sizing
+// Scratch of fa_plan_header_noalloc: the geometry, classification and scan
+// stages above write their workspace here instead of into memory obtained
+// from an allocator.  Every device on which the library is loaded holds
+// this array until the process exits.
+static constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace bsm {
+namespace {
+
+// Device address of g_noalloc_scratch for device `dev`, looked up once per
+// device (with that device current) and cached.  In host code the symbol
+// itself is only a host-side stand-in, so kernels must get this address.
+void* noalloc_scratch_address(int dev, cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[128] = {};
+  *err = cudaSuccess;
+  if (dev < 0 || dev >= 128) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace bsm
+
+extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* mask_func,
+                                      int32_t Hmask, int32_t nfunc, int64_t* header_out,
+                                      void* stream) {
+  using namespace bsm;
+  clear_last_error();
+  if (int e = check_geometry_public(geom)) return e;
+  if (nfunc < 1 || nfunc % 2 != 1) return report_error(FA_ERR_INVALID_ARG, "nfunc must be a positive odd integer");
+  if (Hmask != 1 && Hmask != geom->heads_q) return report_error(FA_ERR_INVALID_ARG, "Hmask must be 1 or heads_q");
+  if (!header_out || reinterpret_cast<uintptr_t>(header_out) % 8 != 0)
+    return report_error(FA_ERR_INVALID_ARG, "header_out must be a non-NULL, 8-byte aligned device pointer");
+  const Geometry g = geometry_public(geom);
+  if (!mask_func && g.total_q > 0) return report_error(FA_ERR_INVALID_ARG, "mask_func is NULL");
+  const int B = g.batch;
+  const long long nq_max = (static_cast<long long>(g.seqlen_q) + kTile - 1) / kTile;
+  const long long kt_ub = (static_cast<long long>(g.seqlen_k) + kTile - 1) / kTile;
+  const long long rows_ub = static_cast<long long>(B) * nq_max;
+  const long long words = kt_ub > 0 ? (kt_ub + 31) / 32 : 1;
+  const long long nflat = static_cast<long long>(Hmask) * rows_ub;
+  // same sub-arrays as the allocating build's first workspace
+  const size_t sizes[] = {4, 64, 4ull * (B + 1), 32ull * B, 4ull * rows_ub, 4ull * nflat * words,
+                          4ull * nflat * words, 4ull * nflat, 4ull * nflat, 4ull * (nflat + 1),
+                          4ull * (nflat + 1)};
+  size_t off[11], need = 0;
+  for (int i = 0; i < 11; ++i) {
+    off[i] = need;
+    need += round256(sizes[i]);
+  }
+  if (need > kNoAllocScratchBytes)
+    return report_error(FA_ERR_UNSUPPORTED,
+                        "this mask needs %zu bytes of planner scratch; the allocation-free entry point "
+                        "has %zu (use fa_plan_build_intervals)",
+                        need, kNoAllocScratchBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return report_error(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address(dev, &e));
+  if (!base) return report_error(FA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
+  PlanWorkspace ws{};
+  ws.err = reinterpret_cast<uint32_t*>(base + off[0]);
+  ws.header = reinterpret_cast<long long*>(header_out);  // the scan writes the header straight to the output
+  ws.cu_rows = reinterpret_cast<int32_t*>(base + off[2]);
+  ws.seq = reinterpret_cast<int32_t*>(base + off[3]);
+  ws.row_batch = reinterpret_cast<int32_t*>(base + off[4]);
+  ws.vis_bits = reinterpret_cast<uint32_t*>(base + off[5]);
+  ws.full_bits = reinterpret_cast<uint32_t*>(base + off[6]);
+  ws.p_cnt = reinterpret_cast<int32_t*>(base + off[7]);
+  ws.f_cnt = reinterpret_cast<int32_t*>(base + off[8]);
+  ws.p_off = reinterpret_cast<int32_t*>(base + off[9]);
+  ws.f_off = reinterpret_cast<int32_t*>(base + off[10]);
+  ws.rows_ub = static_cast<int>(rows_ub);
+  ws.kt_ub = static_cast<int>(kt_ub);
+  ws.words = static_cast<int>(words);
+  MaskArgs m{};
+  m.kind = MASK_INTERVALS;
+  m.mask_func = mask_func;
+  m.nfunc = nfunc;
+  m.Hmask = Hmask;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the error word must start at zero
+  e = cudaMemsetAsync(ws.err, 0, 4, st);
+  if (e == cudaSuccess) e = launch_geometry(g, geom->cu_seqlens_q, geom->cu_seqlens_k, ws, st);
+  if (e == cudaSuccess) e = launch_classify(g, m, ws, st);
+  if (e == cudaSuccess) e = launch_scan_header(g, Hmask, ws, st);
+  if (e != cudaSuccess) return report_error(FA_ERR_CUDA, "allocation-free planner stages: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+

@@ -228,6 +228,37 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);
  */
 int fa_device_error_flags(void* stream, uint32_t* flags);
 
+/*
+ * Allocation-free sizing of an interval plan.  The paper has no counterpart
+ * of this entry point; it exists for callers that cannot allocate device
+ * memory, neither themselves nor through this library: for example code
+ * running inside a memory manager that owns all device memory and must not
+ * re-enter cudaMalloc, or a loop with a strict latency budget where
+ * allocation calls (which may synchronise the device) are not allowed.
+ *
+ * It runs the geometry, classification and scan stages of
+ * fa_plan_build_intervals and writes the same 8-value header (fwd Q rows,
+ * partial nnz, full nnz, 0, 0, 0, 0, error flags) to `header_out`, a
+ * caller-owned device int64[8].  Nothing else is produced and nothing is
+ * read back: the call is asynchronous on `stream`, and a malformed mask or
+ * prefix shows up as a nonzero header_out[7] (bit 0: endpoints, bit 1:
+ * cu_seqlens) instead of an error code.  Arguments are those of
+ * fa_plan_build_intervals.
+ *
+ * The planner's scratch lives in one fixed 4 MiB array per device, held by
+ * every device that loads the library until the process exits.  No
+ * cudaMalloc, cudaFree or other allocating routine is called.  Masks whose
+ * scratch (about 8 bytes per (mask head, Q tile, 32 K tiles) plus small
+ * per-sample arrays) exceeds 4 MiB are rejected with FA_ERR_UNSUPPORTED.
+ * The first call on each device looks up the array's device address; make
+ * that first call before any stream capture.  All calls on a device share
+ * the array and it keeps the previous call's contents (the call clears what
+ * must start at zero), so calls whose GPU work overlaps (e.g. on unordered
+ * streams) race on it and give wrong results: order them.
+ */
+int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* mask_func, int32_t Hmask,
+                           int32_t nfunc, int64_t* header_out, void* stream);
+
 /* Message of the last error on the calling thread ("" if none). */
 const char* fa_last_error(void);
 
