@@ -5,27 +5,32 @@
 // packed predicate (§5: bit 1 keeps the score, bit 0 makes it -inf), then
 // the full K tiles without it; empty tiles are never visited.  A row without
 // any visible key ends with O = 0 and LSE = -inf.  The math is FlexAttention
-// Eq. 1, softmax(mod(Q K^T * scale)) V, computed with an online softmax so
-// the score matrix is never stored.
+// Eq. 1, softmax(mod(Q K^T * scale)) V, with an online softmax: the score
+// matrix is never stored.
 //
-// One CTA per task (the plan's work_desc gives the execution order), 192
-// threads, warp-specialised:
-//   warp 4     TMA producer: Q once, then K and V tiles through a ring of
-//              kStages shared-memory stages (mbarrier transaction counts).
-//   warp 5     TMEM allocator and MMA issuer (one thread): S = Q K^T into a
-//              double-buffered TMEM accumulator, O += P V into a TMEM
-//              accumulator, completion signalled with tcgen05.commit.
-//   warps 0-3  softmax warpgroup: thread r owns score row r (TMEM lane r),
-//              applies scale, score_mods and the predicate, keeps the running
-//              max / sum, writes P (bf16) to shared memory and rescales O in
-//              TMEM when the max moves; epilogue writes O (bf16) and LSE.
-// Every wait is bounded (global-timer limit); on a timeout the CTA sets an
-// error bit, drains what it has in flight, frees TMEM and exits.
+// Persistent CTAs (one per SM) walk the plan's work_desc with a static
+// stride.  320 threads, warp-specialised:
+//   warp 8     TMA producer: Q tiles into a 2-deep ring, K and V tiles into
+//              their own rings, issued in the order the MMAs consume them
+//              (K of tile g+1 before V of tile g).
+//   warp 9     TMEM allocator and MMA issuer (one thread): S(g) = Q K^T into
+//              one of three TMEM score buffers, then O += P(g-1) V with P read
+//              from TMEM (it overwrites its score buffer in bf16).
+//   warps 0-7  two softmax warpgroups; thread r of warpgroup w owns score row
+//              r, columns 64w..64w+63 (TMEM lane r).  Per tile they exchange
+//              the row max through shared memory, write P to TMEM, rescale
+//              their half of O when the max moves, and store their half of
+//              the output at the end of the task.
+// Every mbarrier wait is bounded (global-timer limit).  After a timeout the
+// CTA records an error bit and runs its loops to the end without waiting,
+// so that every thread still reaches every named barrier; then it drains
+// copies and MMAs in flight, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -45,22 +50,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct Cfg {
-  static constexpr int kChunks = D / 64;         // 64-column (128-byte) swizzle chunks
-  static constexpr int kTileBytes = 128 * D * 2; // Q, K or V tile, bf16
-  static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr int kPBytes = 128 * 128 * 2;
+  static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
+  static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile, bf16
+  static constexpr int kQStages = 2;
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + slack for 1 KB alignment
+  static constexpr int kOffK = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffSmall = kOffV + kVStages * kTileBytes;
+  static constexpr int kSmallBytes = 512 + 2 * 2 * 128 * 4 + 2 * 128 * 4;  // barriers, max and sum exchange
+  static constexpr int kSmem = kOffSmall + kSmallBytes + 1024;            // + slack for 1 KB alignment
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 128
-  static constexpr uint32_t kColO = 256;  // O accumulator
+  static constexpr uint32_t kColO = 384;  // S buffers at 0, 128, 256; O after them
+  static_assert(kColO + D <= kTmemCols, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
+
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr uint32_t kBarSoftmax = 1;  // named barrier id of the two softmax warpgroups
 
 struct FwdParams {
   const int32_t* work;
@@ -72,13 +81,43 @@ struct FwdParams {
   const uint32_t* payload;
   __nv_bfloat16* o;
   float* lse;
-  int Hq, Hk, Hmask, rows, total_q;
+  int Hq, Hk, Hmask, rows, total_q, ntasks;
   int flags;
   float scale;       // multiplies Q K^T
   float scale_log2;  // scale * log2(e)
   float softcap, inv_softcap;
   float slopes[kMaxHeads];
 };
+
+// Per-task view of the plan shared by every role.
+struct Task {
+  int m_block, h, b, qv, q_off, k_off, hk, p0, np, f0, n;
+};
+
+__device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
+  Task k;
+  const int* wd = p.work + 4LL * t;
+  k.m_block = wd[0];
+  k.h = wd[1];
+  k.b = wd[2];
+  k.qv = wd[3];
+  const int* sq = p.seq + 8 * k.b;
+  k.q_off = sq[0];
+  k.k_off = sq[1];
+  const int row_begin = sq[4];
+  const int hm = (p.Hmask == 1) ? 0 : k.h;
+  k.hk = k.h / (p.Hq / p.Hk);
+  const long long flat = static_cast<long long>(hm) * p.rows + row_begin + k.m_block;
+  k.p0 = p.p_off[flat];
+  k.np = p.p_off[flat + 1] - k.p0;
+  k.f0 = p.f_off[flat];
+  k.n = k.np + (p.f_off[flat + 1] - k.f0);
+  return k;
+}
+
+__device__ __forceinline__ int tile_index(const FwdParams& p, const Task& k, int j) {
+  return (j < k.np) ? __ldg(p.p_idx + k.p0 + j) : __ldg(p.f_idx + k.f0 + (j - k.np));
+}
 
 // cap * tanh(x / cap) for |x / cap| < 0.5: Maclaurin series of tanh through
 // y^13 (truncation error below 1e-6 relative at |y| = 0.5, far less below).
@@ -100,11 +139,11 @@ __device__ __forceinline__ float softcap_exp(float x, float cap, float inv_cap) 
 }
 
 template <int D, bool MODS>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -113,50 +152,51 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = base + C::kOffQ;
   const uint32_t sK = base + C::kOffK;
   const uint32_t sV = base + C::kOffV;
-  const uint32_t sP = base + C::kOffP;
-  const uint32_t bar0 = base + C::kOffBar;
   // barrier slots (8 bytes each)
-  const uint32_t b_q = bar0;
-  const uint32_t b_kfull = bar0 + 8;                // [S]
-  const uint32_t b_vfull = b_kfull + 8 * S;         // [S]
-  const uint32_t b_empty = b_vfull + 8 * S;         // [S]
-  const uint32_t b_sfull = b_empty + 8 * S;         // [2]
-  const uint32_t b_pfull = b_sfull + 16;            // [2]
-  const uint32_t b_odone = b_pfull + 16;
+  const uint32_t bar0 = base + C::kOffSmall;
+  const uint32_t b_qfull = bar0;                 // [2]
+  const uint32_t b_qempty = b_qfull + 16;        // [2]
+  const uint32_t b_kfull = b_qempty + 16;        // [KS]
+  const uint32_t b_kempty = b_kfull + 8 * KS;    // [KS]
+  const uint32_t b_vfull = b_kempty + 8 * KS;    // [VS]
+  const uint32_t b_vempty = b_vfull + 8 * VS;    // [VS]
+  const uint32_t b_sfull = b_vempty + 8 * VS;    // [3]
+  const uint32_t b_pfull = b_sfull + 24;         // [3]
+  const uint32_t b_pvdone = b_pfull + 24;        // [3]
+  const uint32_t b_odone = b_pvdone + 24;
   const uint32_t b_drain = b_odone + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBar + 8 * (3 * S + 8));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBar + 8 * (3 * S + 8) + 8);
+  uint8_t* small = gbase + C::kOffSmall;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + 400);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(small + 408);
+  float* xmax = reinterpret_cast<float*>(small + 512);                 // [2 parity][2 wg][128]
+  float* xsum = reinterpret_cast<float*>(small + 512 + 2 * 2 * 128 * 4);  // [2 wg][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* wd = p.work + 4LL * blockIdx.x;
-  const int m_block = wd[0], h = wd[1], b = wd[2], qv = wd[3];
-  const int* sq = p.seq + 8 * b;
-  const int q_off = sq[0], k_off = sq[1], row_begin = sq[4];
-  const int hm = (p.Hmask == 1) ? 0 : h;
-  const int hk = h / (p.Hq / p.Hk);
-  const long long flat = static_cast<long long>(hm) * p.rows + row_begin + m_block;
-  const int p0 = p.p_off[flat], np_ = p.p_off[flat + 1] - p0;
-  const int f0 = p.f_off[flat], nf = p.f_off[flat + 1] - f0;
-  const int n = np_ + nf;
-  const int q_row0 = q_off + m_block * kTile;
 
   if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(b_kfull + 8 * s, 1);
-      mbar_init(b_vfull + 8 * s, 1);
-      mbar_init(b_empty + 8 * s, 1);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(b_qfull + 8 * i, 1);
+      mbar_init(b_qempty + 8 * i, 1);
+    }
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(b_kfull + 8 * s, 1);
+      mbar_init(b_kempty + 8 * s, 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(b_vfull + 8 * s, 1);
+      mbar_init(b_vempty + 8 * s, 1);
+    }
+    for (int i = 0; i < 3; ++i) {
       mbar_init(b_sfull + 8 * i, 1);
-      mbar_init(b_pfull + 8 * i, 128);
+      mbar_init(b_pfull + 8 * i, kSoftmaxThreads);
+      mbar_init(b_pvdone + 8 * i, 1);
     }
     mbar_init(b_odone, 1);
     mbar_init(b_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -165,237 +205,277 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(b_q, C::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * 16384, &tmQ, b_q, h * D + c * 64, q_row0);
-      int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % S;
-        if (j >= S && !mbar_wait(b_empty + 8 * st, ((j / S) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs))
-          break;
-        const int kt = (j < np_) ? __ldg(p.p_idx + p0 + j) : __ldg(p.f_idx + f0 + (j - np_));
-        const int krow = k_off + kt * kTile;
-        mbar_arrive_expect_tx(b_kfull + 8 * st, C::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_2d(sK + st * C::kTileBytes + c * 16384, &tmK, b_kfull + 8 * st, hk * D + c * 64, krow);
-        mbar_arrive_expect_tx(b_vfull + 8 * st, C::kTileBytes);
+      int g = 0, tq = 0;
+      int q_issued = 0, k_issued = 0, v_issued = 0;  // loads actually started (for the abort drain)
+      bool pend = false;
+      int pv_g = 0, pv_row = 0, pv_hk = 0;
+      auto load_v = [&](int gv, int krow, int hk) {
+        const int vs = gv % VS;
+        if (gv >= VS) mbar_wait(b_vempty + 8 * vs, ((gv / VS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        if (*abort_flag) return;
+        v_issued = gv + 1;
+        mbar_arrive_expect_tx(b_vfull + 8 * vs, C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_2d(sV + st * C::kTileBytes + c * 16384, &tmV, b_vfull + 8 * st, hk * D + c * 64, krow);
-        issued = j + 1;
-      }
-      if (*abort_flag) {
-        // let copies already in flight land before the CTA exits
-        mbar_wait_drain(b_q, 0, kWaitTimeoutNs);
-        for (int j = (issued > S ? issued - S : 0); j < issued; ++j) {
-          mbar_wait_drain(b_kfull + 8 * (j % S), (j / S) & 1, kWaitTimeoutNs);
-          mbar_wait_drain(b_vfull + 8 * (j % S), (j / S) & 1, kWaitTimeoutNs);
+          tma_load_2d(sV + vs * C::kTileBytes + c * 16384, &tmV, b_vfull + 8 * vs, hk * D + c * 64, krow);
+      };
+      for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
+        const Task k = load_task(p, t);
+        if (k.n == 0) continue;
+        const int qb = tq & 1;
+        if (tq >= 2) mbar_wait(b_qempty + 8 * qb, ((tq >> 1) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        if (!*abort_flag) {
+          q_issued = tq + 1;
+          mbar_arrive_expect_tx(b_qfull + 8 * qb, C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sQ + qb * C::kTileBytes + c * 16384, &tmQ, b_qfull + 8 * qb, k.h * D + c * 64,
+                        k.q_off + k.m_block * kTile);
         }
+        for (int j = 0; j < k.n; ++j) {
+          const int gi = g + j;
+          const int krow = k.k_off + tile_index(p, k, j) * kTile;
+          const int ks = gi % KS;
+          if (gi >= KS) mbar_wait(b_kempty + 8 * ks, ((gi / KS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          if (!*abort_flag) {
+            k_issued = gi + 1;
+            mbar_arrive_expect_tx(b_kfull + 8 * ks, C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sK + ks * C::kTileBytes + c * 16384, &tmK, b_kfull + 8 * ks, k.hk * D + c * 64, krow);
+          }
+          if (pend) load_v(pv_g, pv_row, pv_hk);
+          pend = true;
+          pv_g = gi;
+          pv_row = krow;
+          pv_hk = k.hk;
+        }
+        g += k.n;
+        ++tq;
+      }
+      if (pend) load_v(pv_g, pv_row, pv_hk);
+      if (*abort_flag) {
+        // let the copies already started land before the CTA exits (the last
+        // load of each ring slot is the only one that can still be in flight)
+        for (int u = (q_issued > 2 ? q_issued - 2 : 0); u < q_issued; ++u)
+          mbar_wait_drain(b_qfull + 8 * (u & 1), (u >> 1) & 1, kWaitTimeoutNs);
+        for (int u = (k_issued > KS ? k_issued - KS : 0); u < k_issued; ++u)
+          mbar_wait_drain(b_kfull + 8 * (u % KS), (u / KS) & 1, kWaitTimeoutNs);
+        for (int u = (v_issued > VS ? v_issued - VS : 0); u < v_issued; ++u)
+          mbar_wait_drain(b_vfull + 8 * (u % VS), (u / VS) & 1, kWaitTimeoutNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
-      auto issue_s = [&](int buf, int st) {
-        const uint32_t dcol = tmem + C::kColS + 128u * buf;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16_ss(dcol, sdesc_sw128(sQ + off, 16, 1024),
-                       sdesc_sw128(sK + st * C::kTileBytes + off, 16, 1024), idS, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int buf, int st, bool acc) {
-        const uint32_t dcol = tmem + C::kColO;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_bf16_ss(dcol, sdesc_sw128(sP + buf * C::kPBytes + aoff, 16, 1024),
-                       sdesc_sw128(sV + st * C::kTileBytes + kk * 2048, 16384, 1024), idO,
-                       (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(b_q, 0, abort_flag, &g_fwd_err, kWaitTimeoutNs) &&
-                mbar_wait(b_kfull, 0, abort_flag, &g_fwd_err, kWaitTimeoutNs);
-      if (ok) {
+      int g = 0, tq = 0;
+      bool pend = false;
+      int pg = 0;
+      bool pacc = false;
+      auto issue_pv = [&](int gp, bool acc) {
+        const int sb = gp % 3, vs = gp % VS;
+        mbar_wait(b_pfull + 8 * sb, (gp / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        mbar_wait(b_vfull + 8 * vs, (gp / VS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        if (*abort_flag) return;
         tc_fence_after();
-        issue_s(0, 0);
-        umma_commit(b_sfull);
-        for (int j = 0; j < n; ++j) {
-          if (j + 1 < n) {
-            const int st1 = (j + 1) % S;
-            if (!mbar_wait(b_kfull + 8 * st1, ((j + 1) / S) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs)) break;
+        const uint32_t pcol = tmem + 128u * sb;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk,
+                       sdesc_sw128(sV + vs * C::kTileBytes + kk * 2048, 16384, 1024), idO,
+                       (acc || kk > 0) ? 1u : 0u);
+        umma_commit(b_vempty + 8 * vs);
+        umma_commit(b_pvdone + 8 * sb);
+        umma_commit(b_odone);
+      };
+      for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
+        const Task k = load_task(p, t);
+        if (k.n == 0) continue;
+        const int qb = tq & 1;
+        mbar_wait(b_qfull + 8 * qb, (tq >> 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        for (int j = 0; j < k.n; ++j) {
+          const int gi = g + j;
+          const int ks = gi % KS, sb = gi % 3;
+          mbar_wait(b_kfull + 8 * ks, (gi / KS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          if (gi >= 3) mbar_wait(b_pvdone + 8 * sb, ((gi / 3) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          if (!*abort_flag) {
             tc_fence_after();
-            issue_s((j + 1) & 1, st1);
-            umma_commit(b_sfull + 8 * ((j + 1) & 1));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              umma_bf16_ss(tmem + 128u * sb, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
+                           sdesc_sw128(sK + ks * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+            }
+            umma_commit(b_sfull + 8 * sb);
+            umma_commit(b_kempty + 8 * ks);
+            if (j == k.n - 1) umma_commit(b_qempty + 8 * qb);
           }
-          const int st = j % S;
-          if (!mbar_wait(b_pfull + 8 * (j & 1), (j >> 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs)) break;
-          if (!mbar_wait(b_vfull + 8 * st, (j / S) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs)) break;
-          tc_fence_after();
-          issue_pv(j & 1, st, j > 0);
-          umma_commit(b_empty + 8 * st);
-          umma_commit(b_odone);
+          if (pend) issue_pv(pg, pacc);
+          pend = true;
+          pg = gi;
+          pacc = j > 0;
         }
+        g += k.n;
+        ++tq;
       }
+      if (pend) issue_pv(pg, pacc);
       // every MMA issued above completes before TMEM is released
       umma_commit(b_drain);
       mbar_wait_drain(b_drain, 0, kWaitTimeoutNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x;  // score row, TMEM lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int q_local = m_block * kTile + r;
-    float m_run = -INFINITY, l_run = 0.0f;
-    float slope = 0.0f;
-    if (MODS && (p.flags & FA_MOD_ALIBI)) slope = p.slopes[h];
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int buf = j & 1;
-      const bool partial = j < np_;
-      uint4 pm = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
-      if (partial) pm = __ldg(reinterpret_cast<const uint4*>(p.payload) + static_cast<long long>(p0 + j) * kTile + r);
-      int kt = 0;
-      if (MODS) kt = partial ? __ldg(p.p_idx + p0 + j) : __ldg(p.f_idx + f0 + (j - np_));
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(b_sfull + 8 * buf, (j >> 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs))) {
-        ok = false;
-        break;
+    const int wg = warp >> 2;               // column half: 64*wg .. 64*wg+63
+    const int r = threadIdx.x & 127;         // score row, TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
+    int g = 0;
+    for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
+      const Task k = load_task(p, t);
+      const bool row_ok = r < k.qv;
+      const long long grow = static_cast<long long>(k.q_off) + k.m_block * kTile + r;
+      __nv_bfloat16* orow = p.o + (grow * p.Hq + k.h) * D + wg * (D / 2);
+      if (k.n == 0) {
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          if (wg == 0 && p.lse != nullptr) p.lse[static_cast<long long>(k.h) * p.total_q + grow] = -INFINITY;
+        }
+        continue;
       }
-      tc_fence_after();
-      float x[128];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + C::kColS + 128u * buf + 32u * c4, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c4 * 32 + i] = __uint_as_float(v[i]);
-      }
-      const uint32_t pw[4] = {pm.x, pm.y, pm.z, pm.w};
-      float mx = -INFINITY;
-      if (MODS) {
-        const float fd0 = static_cast<float>(kt * kTile - q_local);  // k - q at column 0
-        float amax = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          x[c] *= p.scale;
-          amax = fmaxf(amax, fabsf(x[c]));
-        }
-        if (p.flags & FA_MOD_SOFTCAP) {
-          // warp-uniform choice between the series (|s/cap| < 0.5 everywhere)
-          // and the exponential form of tanh
-          if (__any_sync(0xffffffffu, amax >= 0.5f * p.softcap)) {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = softcap_exp(x[c], p.softcap, p.inv_softcap);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = softcap_series(x[c], p.softcap, p.inv_softcap);
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float s = fmaf(slope, fd0 + static_cast<float>(c), x[c]);
-          if (partial && !((pw[c >> 5] >> (c & 31)) & 1u)) s = -INFINITY;
-          x[c] = s;
-          mx = fmaxf(mx, s);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float s = x[c] * p.scale_log2;
-          if (partial && !((pw[c >> 5] >> (c & 31)) & 1u)) s = -INFINITY;
-          x[c] = s;
-          mx = fmaxf(mx, s);
-        }
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      float alpha, rowsum = 0.0f;
-      uint32_t pk[64];
-      if (MODS) {
-        alpha = ex2_approx((m_run - m_use) * kLog2e);
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float e0 = ex2_approx((x[c] - m_use) * kLog2e);
-          const float e1 = ex2_approx((x[c + 1] - m_use) * kLog2e);
-          rowsum += e0 + e1;
-          pk[c >> 1] = pack_bf16x2(e0, e1);
-        }
-      } else {
-        alpha = ex2_approx(m_run - m_use);
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float e0 = ex2_approx(x[c] - m_use);
-          const float e1 = ex2_approx(x[c + 1] - m_use);
-          rowsum += e0 + e1;
-          pk[c >> 1] = pack_bf16x2(e0, e1);
-        }
-      }
-      l_run = l_run * alpha + rowsum;
-      m_run = m_new;
-      // P(j) -> shared memory, 128-byte swizzled K-major layout (two 64-key chunks)
-      {
-        const uint32_t prow = sP + buf * C::kPBytes + r * 128;
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int w0 = c * 32 + u * 4;  // packed word index (2 keys per word)
-            st_shared_v4(prow + c * 16384 + ((u ^ (r & 7)) << 4), pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
-          }
-      }
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(b_odone, (j - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs))) {
-          ok = false;
-          break;
-        }
+      float slope = 0.0f;
+      if (MODS && (p.flags & FA_MOD_ALIBI)) slope = p.slopes[k.h];
+      const int q_local = k.m_block * kTile + r;
+      float m_run = -INFINITY, l_half = 0.0f;
+      for (int j = 0; j < k.n; ++j) {
+        const int gi = g + j;
+        const int sb = gi % 3;
+        const bool partial = j < k.np;
+        uint2 pm = make_uint2(0xffffffffu, 0xffffffffu);
+        if (partial)
+          pm = __ldg(reinterpret_cast<const uint2*>(p.payload) + (static_cast<long long>(k.p0 + j) * kTile + r) * 2 + wg);
+        int kt = 0;
+        if (MODS) kt = tile_index(p, k, j);
+        mbar_wait(b_sfull + 8 * sb, (gi / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        float s[64];
+        tmem_ld64(lane_addr + 128u * sb + 64u * wg, s);
+        if (MODS) {
+          // natural units: scale, softcap, ALiBi, predicate
+          float amax = 0.0f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(lane_addr + C::kColO + 32u * c, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(lane_addr + C::kColO + 32u * c, v);
+          for (int c = 0; c < 64; ++c) {
+            s[c] *= p.scale;
+            amax = fmaxf(amax, fabsf(s[c]));
           }
-          tmem_st_wait();
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(b_pfull + 8 * buf);
-    }
-    // ------------------------------------------------------------ epilogue
-    const bool row_ok = r < qv;
-    const long long grow = static_cast<long long>(q_row0) + r;
-    __nv_bfloat16* orow = p.o + (grow * p.Hq + h) * D;
-    bool have = (n > 0) && ok && (l_run > 0.0f);
-    if (n > 0 && ok) {
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(b_odone, (n - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs))) {
-        ok = false;
-        have = false;
-      }
-    }
-    if (n > 0 && ok) {
-      tc_fence_after();
-      const float inv_l = have ? 1.0f / l_run : 0.0f;
+          if (p.flags & FA_MOD_SOFTCAP) {
+            if (__any_sync(0xffffffffu, amax >= 0.5f * p.softcap)) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+              for (int c = 0; c < 64; ++c) s[c] = softcap_exp(s[c], p.softcap, p.inv_softcap);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) s[c] = softcap_series(s[c], p.softcap, p.inv_softcap);
+            }
+          }
+          const float fd0 = static_cast<float>(kt * kTile + wg * 64 - q_local);  // k - q at column 0
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = fmaf(slope, fd0 + static_cast<float>(c), s[c]);
+        }
+        if (partial) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const uint32_t w = (c < 32) ? pm.x : pm.y;
+            if (!((w >> (c & 31)) & 1u)) s[c] = -INFINITY;
+          }
+        }
+        // row max of this half (four independent chains), then of the row
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          m0 = max3f(m0, s[c], s[c + 1]);
+          m1 = max3f(m1, s[c + 2], s[c + 3]);
+          m2 = max3f(m2, s[c + 4], s[c + 5]);
+          m3 = max3f(m3, s[c + 6], s[c + 7]);
+        }
+        const float mhalf = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        float* xm = xmax + (gi & 1) * 256;
+        xm[wg * 128 + r] = mhalf;
+        tc_fence_before();
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        tc_fence_after();
+        const float mrow = fmaxf(mhalf, xm[(wg ^ 1) * 128 + r]);
+        // running max in the exponent's units (scaled log2 units without mods)
+        const float m_tile = MODS ? mrow : mrow * p.scale_log2;
+        const float m_new = fmaxf(m_run, m_tile);
+        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+        const float alpha = MODS ? ex2_approx((m_run - m_use) * kLog2e) : ex2_approx(m_run - m_use);
+        m_run = m_new;
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial sums
+        uint32_t pk[32];
+        const uint64_t negm = f2_pack(-m_use, -m_use);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          uint64_t x = f2_pack(s[c], s[c + 1]);
+          x = MODS ? f2_mul(f2_add(x, negm), l2e2) : f2_fma(x, sc2, negm);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          const uint64_t e = f2_pack(e0, e1);
+          switch ((c >> 1) & 3) {
+            case 0: acc0 = f2_add(acc0, e); break;
+            case 1: acc1 = f2_add(acc1, e); break;
+            case 2: acc2 = f2_add(acc2, e); break;
+            default: acc3 = f2_add(acc3, e); break;
+          }
+          pk[c >> 1] = pack_bf16x2(e0, e1);
+        }
+        float a0, a1;
+        f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
+        l_half = l_half * alpha + (a0 + a1);
+        // P (bf16 pairs) over this half's 32 columns of the score buffer
+        tmem_st32(lane_addr + 128u * sb + 32u * wg, pk);
+        if (j > 0) {
+          mbar_wait(b_odone, (gi - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              uint32_t v[32];
+              const uint32_t oa = lane_addr + C::kColO + wg * (D / 2) + 32u * c;
+              tmem_ld32(oa, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(oa, v);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_pfull + 8 * sb);
+      }
+      g += k.n;
+      // ---------------------------------------------------------- epilogue
+      mbar_wait(b_odone, (g - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+      tc_fence_after();
+      xsum[wg * 128 + r] = l_half;
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      const float l = l_half + xsum[(wg ^ 1) * 128 + r];
+      const bool have = l > 0.0f;
+      const float inv_l = have ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_addr + C::kColO + 32u * c, v);
+        tmem_ld32(lane_addr + C::kColO + wg * (D / 2) + 32u * c, v);
         if (row_ok) {
           uint32_t pkd[16];
 #pragma unroll
@@ -406,20 +486,19 @@ __global__ void __launch_bounds__(192, 1)
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
         }
       }
-    } else if (row_ok) {
-      uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-    }
-    if (row_ok && p.lse != nullptr) {
-      float lse = -INFINITY;
-      if (have) lse = MODS ? (m_run + __logf(l_run)) : (m_run + __log2f(l_run)) * kLn2;
-      p.lse[static_cast<long long>(h) * p.total_q + grow] = lse;
+      if (wg == 0 && row_ok && p.lse != nullptr) {
+        float lse = -INFINITY;
+        if (have) lse = MODS ? (m_run + __logf(l)) : (m_run + __log2f(l)) * kLn2;
+        p.lse[static_cast<long long>(k.h) * p.total_q + grow] = lse;
+      }
+      // the sum exchange slots are rewritten at the next task's epilogue only
+      // after at least one more softmax barrier, so no extra barrier is needed
+      tc_fence_before();
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -467,6 +546,7 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
     return cudaErrorInvalidValue;
   }
   FwdParams p{};
+  p.ntasks = static_cast<int>(pl->tasks);
   p.work = pl->work_desc;
   p.seq = pl->seq_desc;
   p.p_off = pl->p_off;
@@ -489,16 +569,18 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   if (a.flags & FA_MOD_ALIBI)
     for (int h = 0; h < g.heads_q; ++h) p.slopes[h] = a.slopes[h];
   auto kern = k_fwd<D, MODS>;
-  static thread_local int configured_dev = -1;  // attribute is per device
-  int dev = 0;
+  int dev = 0, sms = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
-  (void)configured_dev;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
   if (e != cudaSuccess) {
-    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    *why = "device attribute / cudaFuncSetAttribute failed";
     return e;
   }
-  kern<<<static_cast<unsigned>(pl->tasks), 192, Cfg<D>::kSmem, st>>>(mq, mk, mv, p);
+  // persistent: one CTA per SM (shared memory keeps it to one), tasks by static stride
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(pl->tasks, sms));
+  kern<<<grid, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "forward kernel launch failed";
   return e;

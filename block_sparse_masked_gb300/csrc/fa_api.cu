@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <chrono>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -406,6 +407,8 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev != plan->device) return fail(FA_ERR_PLAN_MISMATCH, "plan was built on device %d", plan->device);
+  if (!(scale > 0.0f) || !std::isfinite(scale))
+    return fail(FA_ERR_INVALID_ARG, "scale must be positive and finite");
   if (plan->tasks == 0) return FA_OK;  // nothing to compute (e.g. no Q rows)
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   for (const void* ptr : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)})

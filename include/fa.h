@@ -162,7 +162,8 @@ typedef struct {
  * skipped; rows without a visible key get O = 0 and LSE = -inf.
  *   q, k, v: device bf16 in the geometry's layout; o: device bf16, same
  *   layout as q; lse: device float32 [heads_q, total_q] (natural log), may
- *   be NULL.  scale multiplies Q K^T before the mods.  mods may be NULL.
+ *   be NULL.  scale (> 0, finite) multiplies Q K^T before the mods.  mods
+ *   may be NULL.
  * Every base pointer must be 16-byte aligned.  The geometry must equal the
  * one the plan was built for (FA_ERR_PLAN_MISMATCH otherwise).  The call
  * is asynchronous on `stream`; one plan may be used concurrently on
