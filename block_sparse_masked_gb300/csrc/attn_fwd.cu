@@ -9,22 +9,22 @@
 // matrix is never stored.
 //
 // Persistent CTAs (one per SM) walk the plan's work_desc with a static
-// stride.  320 threads, warp-specialised:
-//   warp 8     TMA producer: Q tiles into a 2-deep ring, K and V tiles into
-//              their own rings, issued in the order the MMAs consume them
-//              (K of tile g+1 before V of tile g).
-//   warp 9     TMEM allocator and MMA issuer (one thread): S(g) = Q K^T into
-//              one of three TMEM score buffers, then O += P(g-1) V with P read
-//              from TMEM (it overwrites its score buffer in bf16).
-//   warps 0-7  two softmax warpgroups; thread r of warpgroup w owns score row
-//              r, columns 64w..64w+63 (TMEM lane r).  Per tile they exchange
-//              the row max through shared memory, write P to TMEM, rescale
-//              their half of O when the max moves, and store their half of
-//              the output at the end of the task.
-// Every mbarrier wait is bounded (global-timer limit).  After a timeout the
-// CTA records an error bit and runs its loops to the end without waiting,
-// so that every thread still reaches every named barrier; then it drains
-// copies and MMAs in flight, frees TMEM and exits.
+// stride.  576 threads, warp-specialised:
+//   warp 16     TMA producer: Q tiles into a 2-deep ring; K and V tiles into
+//               one ring, issued in the order the MMAs consume them (K of
+//               tile g+1 before V of tile g).
+//   warp 17     TMEM allocator and MMA issuer (one thread): S(g) = Q K^T into
+//               one of three TMEM score buffers, then O += P(g-1) V with P
+//               read from TMEM (it overwrites its score buffer in bf16).
+//   warps 0-15  four softmax warpgroups; thread r of warpgroup w owns score
+//               row r, columns 32w..32w+31 (TMEM lane r).  Per tile they
+//               exchange the row max through shared memory, write P to TMEM,
+//               rescale their quarter of O when the reference max moves, and
+//               store their quarter of the output at the end of the task.
+// Every wait is an mbarrier wait with a global-timer limit (the softmax
+// warps synchronise through an mbarrier too, not a named barrier).  After a
+// timeout the CTA records an error bit, stops waiting, drains copies and
+// MMAs in flight, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,29 +47,34 @@ namespace {
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold, log2 units
 
 template <int D>
 struct Cfg {
   static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
   static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile, bf16
   static constexpr int kQStages = 2;
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
-  static constexpr int kVStages = (D == 128) ? 2 : 4;
+  static constexpr int kSlots = (D == 128) ? 4 : 8;  // one ring of K and V tiles
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQStages * kTileBytes;
-  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffSmall = kOffV + kVStages * kTileBytes;
-  static constexpr int kSmallBytes = 512 + 2 * 2 * 128 * 4 + 2 * 128 * 4;  // barriers, max and sum exchange
-  static constexpr int kSmem = kOffSmall + kSmallBytes + 1024;            // + slack for 1 KB alignment
+  static constexpr int kOffKV = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffSmall = kOffKV + kSlots * kTileBytes;
+  static constexpr int kSmallBytes = 512 + 256 + 128 + 2 * 4 * 128 * 4;  // barriers, task ring, task broadcast, exchange
+  static constexpr int kNeed = kOffSmall + kSmallBytes;
+  // dynamic shared memory normally starts 1 KB-aligned; what is left up to the
+  // per-block limit is slack for a misaligned start (checked at run time)
+  static constexpr int kSmem = (kNeed + 1024 <= 232448) ? kNeed + 1024 : 232448;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 384;  // S buffers at 0, 128, 256; O after them
   static_assert(kColO + D <= kTmemCols, "TMEM budget");
-  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kNeed <= 232448, "shared memory budget");
 };
 
-constexpr int kThreads = 320;
-constexpr int kSoftmaxThreads = 256;
-constexpr uint32_t kBarSoftmax = 1;  // named barrier id of the two softmax warpgroups
+constexpr int kWG = 4;                     // softmax warpgroups, 32 score columns each
+constexpr int kCols = 128 / kWG;
+constexpr int kSoftmaxThreads = 128 * kWG;
+constexpr int kWarpProducer = 4 * kWG, kWarpMma = 4 * kWG + 1;
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr uint32_t kBarSoftmax = 1;  // named barrier of the softmax warps
 
 struct FwdParams {
   const int32_t* work;
@@ -89,10 +94,12 @@ struct FwdParams {
   float slopes[kMaxHeads];
 };
 
-// Per-task view of the plan shared by every role.
+// Per-task view of the plan shared by every role (decoded once by the
+// producer and handed to the other roles through a shared-memory ring).
 struct Task {
-  int m_block, h, b, qv, q_off, k_off, hk, p0, np, f0, n;
+  int m_block, h, b, qv, q_off, k_off, hk, p0, np, f0, n, pad;
 };
+constexpr int kTaskRing = 4;
 
 __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
   Task k;
@@ -141,35 +148,43 @@ __device__ __forceinline__ float softcap_exp(float x, float cap, float inv_cap) 
 template <int D, bool MODS>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
+          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+          const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
-  constexpr int KS = C::kKStages, VS = C::kVStages;
+  constexpr int NS = C::kSlots;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
 
   const uint32_t sQ = base + C::kOffQ;
-  const uint32_t sK = base + C::kOffK;
-  const uint32_t sV = base + C::kOffV;
+  const uint32_t sKV = base + C::kOffKV;
   // barrier slots (8 bytes each)
   const uint32_t bar0 = base + C::kOffSmall;
   const uint32_t b_qfull = bar0;                 // [2]
   const uint32_t b_qempty = b_qfull + 16;        // [2]
-  const uint32_t b_kfull = b_qempty + 16;        // [KS]
-  const uint32_t b_kempty = b_kfull + 8 * KS;    // [KS]
-  const uint32_t b_vfull = b_kempty + 8 * KS;    // [VS]
-  const uint32_t b_vempty = b_vfull + 8 * VS;    // [VS]
-  const uint32_t b_sfull = b_vempty + 8 * VS;    // [3]
+  const uint32_t b_full = b_qempty + 16;         // [NS] K/V ring
+  const uint32_t b_empty = b_full + 8 * NS;      // [NS]
+  const uint32_t b_sfull = b_empty + 8 * NS;     // [3]
   const uint32_t b_pfull = b_sfull + 24;         // [3]
-  const uint32_t b_pvdone = b_pfull + 24;        // [3]
-  const uint32_t b_odone = b_pvdone + 24;
-  const uint32_t b_drain = b_odone + 8;
+  const uint32_t b_pvdone = b_pfull + 24;        // [3] PV(g) done: P buffer g%3 free, O updated
+  const uint32_t b_drain = b_pvdone + 24;
+  const uint32_t b_tfull = b_drain + 8;          // [kTaskRing] task ring
+  const uint32_t b_tempty = b_tfull + 8 * kTaskRing;
+
   uint8_t* small = gbase + C::kOffSmall;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + 400);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(small + 408);
-  float* xmax = reinterpret_cast<float*>(small + 512);                 // [2 parity][2 wg][128]
-  float* xsum = reinterpret_cast<float*>(small + 512 + 2 * 2 * 128 * 4);  // [2 wg][128]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + 480);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(small + 488);
+  Task* tring = reinterpret_cast<Task*>(small + 512);    // [kTaskRing]
+  Task* tdec = reinterpret_cast<Task*>(small + 768);     // [2] task as seen by the softmax warps
+  float* xmax = reinterpret_cast<float*>(small + 896);  // [2 parity][kWG][128]; also the per-task sum exchange
+  static_assert(16 + 16 + 16 * C::kSlots + 3 * 24 + 8 + 16 * kTaskRing <= 480, "barrier slots");
+  static_assert(sizeof(Task) * kTaskRing <= 256, "task ring");
+  if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
+    // dynamic shared memory not aligned as expected: report and stop (uniform exit)
+    if (threadIdx.x == 0) atomicOr(&g_fwd_err, DEVERR_SMEM_ALIGN);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -178,25 +193,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_qfull + 8 * i, 1);
       mbar_init(b_qempty + 8 * i, 1);
     }
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(b_kfull + 8 * s, 1);
-      mbar_init(b_kempty + 8 * s, 1);
-    }
-    for (int s = 0; s < VS; ++s) {
-      mbar_init(b_vfull + 8 * s, 1);
-      mbar_init(b_vempty + 8 * s, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(b_full + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 1);
     }
     for (int i = 0; i < 3; ++i) {
       mbar_init(b_sfull + 8 * i, 1);
       mbar_init(b_pfull + 8 * i, kSoftmaxThreads);
       mbar_init(b_pvdone + 8 * i, 1);
     }
-    mbar_init(b_odone, 1);
     mbar_init(b_drain, 1);
+    for (int i = 0; i < kTaskRing; ++i) {
+      mbar_init(b_tfull + 8 * i, 1);
+      mbar_init(b_tempty + 8 * i, 2);  // the MMA issuer and softmax thread 0
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -205,28 +219,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
+    // K and V tiles share one ring, filled in the order the MMA issuer
+    // consumes them: K(0), then K(g) followed by V(g-1) for every later tile
+    // (across task boundaries), and V of the last tile at the end.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int g = 0, tq = 0;
-      int q_issued = 0, k_issued = 0, v_issued = 0;  // loads actually started (for the abort drain)
+      int tq = 0, c = 0;               // tasks with tiles, ring loads
+      int q_issued = 0, c_issued = 0;  // loads actually started (for the abort drain)
       bool pend = false;
-      int pv_g = 0, pv_row = 0, pv_hk = 0;
-      auto load_v = [&](int gv, int krow, int hk) {
-        const int vs = gv % VS;
-        if (gv >= VS) mbar_wait(b_vempty + 8 * vs, ((gv / VS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
-        if (*abort_flag) return;
-        v_issued = gv + 1;
-        mbar_arrive_expect_tx(b_vfull + 8 * vs, C::kTileBytes);
+      int pv_row = 0, pv_hk = 0;
+      auto load_tile = [&](const CUtensorMap* map, int row, int hk) {
+        const int slot = c % NS;
+        if (c >= NS) mbar_wait(b_empty + 8 * slot, ((c / NS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        if (!*abort_flag) {
+          c_issued = c + 1;
+          mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_2d(sV + vs * C::kTileBytes + c * 16384, &tmV, b_vfull + 8 * vs, hk * D + c * 64, krow);
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384, map, b_full + 8 * slot, hk * D + ch * 64, row);
+        }
+        ++c;
+      };
+      int ti = 0;  // task ring position
+      auto publish = [&](const Task& k) {
+        const int slot = ti % kTaskRing;
+        if (ti >= kTaskRing)
+          mbar_wait(b_tempty + 8 * slot, ((ti / kTaskRing) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        tring[slot] = k;
+        mbar_arrive(b_tfull + 8 * slot);  // release: the task is visible to the waiters
+        ++ti;
       };
       for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
         const Task k = load_task(p, t);
+        publish(k);
         if (k.n == 0) continue;
         const int qb = tq & 1;
         if (tq >= 2) mbar_wait(b_qempty + 8 * qb, ((tq >> 1) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
@@ -234,89 +263,95 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_issued = tq + 1;
           mbar_arrive_expect_tx(b_qfull + 8 * qb, C::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sQ + qb * C::kTileBytes + c * 16384, &tmQ, b_qfull + 8 * qb, k.h * D + c * 64,
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_2d(sQ + qb * C::kTileBytes + ch * 16384, &tmQ, b_qfull + 8 * qb, k.h * D + ch * 64,
                         k.q_off + k.m_block * kTile);
         }
         for (int j = 0; j < k.n; ++j) {
-          const int gi = g + j;
           const int krow = k.k_off + tile_index(p, k, j) * kTile;
-          const int ks = gi % KS;
-          if (gi >= KS) mbar_wait(b_kempty + 8 * ks, ((gi / KS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
-          if (!*abort_flag) {
-            k_issued = gi + 1;
-            mbar_arrive_expect_tx(b_kfull + 8 * ks, C::kTileBytes);
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d(sK + ks * C::kTileBytes + c * 16384, &tmK, b_kfull + 8 * ks, k.hk * D + c * 64, krow);
+          // at a task boundary the previous task's last V goes first, so that
+          // its last PV can run before the new task's first S
+          if (j == 0 && pend) {
+            load_tile(&tmV, pv_row, pv_hk);
+            pend = false;
           }
-          if (pend) load_v(pv_g, pv_row, pv_hk);
+          load_tile(&tmK, krow, k.hk);
+          if (pend) load_tile(&tmV, pv_row, pv_hk);
           pend = true;
-          pv_g = gi;
           pv_row = krow;
           pv_hk = k.hk;
         }
-        g += k.n;
         ++tq;
       }
-      if (pend) load_v(pv_g, pv_row, pv_hk);
+      if (pend) load_tile(&tmV, pv_row, pv_hk);
+      {
+        Task end{};
+        end.n = -1;  // end of this CTA's tasks
+        publish(end);
+      }
       if (*abort_flag) {
-        // let the copies already started land before the CTA exits (the last
-        // load of each ring slot is the only one that can still be in flight)
+        // let the copies already started land before the CTA exits (only the
+        // last load of each slot can still be in flight)
         for (int u = (q_issued > 2 ? q_issued - 2 : 0); u < q_issued; ++u)
           mbar_wait_drain(b_qfull + 8 * (u & 1), (u >> 1) & 1, kWaitTimeoutNs);
-        for (int u = (k_issued > KS ? k_issued - KS : 0); u < k_issued; ++u)
-          mbar_wait_drain(b_kfull + 8 * (u % KS), (u / KS) & 1, kWaitTimeoutNs);
-        for (int u = (v_issued > VS ? v_issued - VS : 0); u < v_issued; ++u)
-          mbar_wait_drain(b_vfull + 8 * (u % VS), (u / VS) & 1, kWaitTimeoutNs);
+        for (int u = (c_issued > NS ? c_issued - NS : 0); u < c_issued; ++u)
+          mbar_wait_drain(b_full + 8 * (u % NS), (u / NS) & 1, kWaitTimeoutNs);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
-      int g = 0, tq = 0;
+      int g = 0, tq = 0, c = 0;  // tiles, tasks with tiles, ring slots consumed
       bool pend = false;
       int pg = 0;
       bool pacc = false;
       auto issue_pv = [&](int gp, bool acc) {
-        const int sb = gp % 3, vs = gp % VS;
+        const int sb = gp % 3, slot = c % NS;
         mbar_wait(b_pfull + 8 * sb, (gp / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
-        mbar_wait(b_vfull + 8 * vs, (gp / VS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        mbar_wait(b_full + 8 * slot, (c / NS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        ++c;
         if (*abort_flag) return;
         tc_fence_after();
         const uint32_t pcol = tmem + 128u * sb;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk,
-                       sdesc_sw128(sV + vs * C::kTileBytes + kk * 2048, 16384, 1024), idO,
+                       sdesc_sw128(sKV + slot * C::kTileBytes + kk * 2048, 16384, 1024), idO,
                        (acc || kk > 0) ? 1u : 0u);
-        umma_commit(b_vempty + 8 * vs);
+        umma_commit(b_empty + 8 * slot);
         umma_commit(b_pvdone + 8 * sb);
-        umma_commit(b_odone);
       };
-      for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
-        const Task k = load_task(p, t);
+      for (int ti = 0;; ++ti) {
+        const int tslot = ti % kTaskRing;
+        mbar_wait(b_tfull + 8 * tslot, (ti / kTaskRing) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        const Task k = tring[tslot];
+        mbar_arrive(b_tempty + 8 * tslot);
+        if (k.n < 0 || *abort_flag) break;
         if (k.n == 0) continue;
-        const int qb = tq & 1;
+        const int qb = tq & 1;  // (its buffer is handed back by the softmax epilogue)
         mbar_wait(b_qfull + 8 * qb, (tq >> 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         for (int j = 0; j < k.n; ++j) {
           const int gi = g + j;
-          const int ks = gi % KS, sb = gi % 3;
-          mbar_wait(b_kfull + 8 * ks, (gi / KS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          if (j == 0 && pend) {  // previous task's last PV first (same order as the producer)
+            issue_pv(pg, pacc);
+            pend = false;
+          }
+          const int sb = gi % 3, slot = c % NS;
+          mbar_wait(b_full + 8 * slot, (c / NS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
           if (gi >= 3) mbar_wait(b_pvdone + 8 * sb, ((gi / 3) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          ++c;
           if (!*abort_flag) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
               umma_bf16_ss(tmem + 128u * sb, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
-                           sdesc_sw128(sK + ks * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+                           sdesc_sw128(sKV + slot * C::kTileBytes + off, 16, 1024), idS, kk > 0);
             }
             umma_commit(b_sfull + 8 * sb);
-            umma_commit(b_kempty + 8 * ks);
-            if (j == k.n - 1) umma_commit(b_qempty + 8 * qb);
+            umma_commit(b_empty + 8 * slot);
           }
           if (pend) issue_pv(pg, pacc);
           pend = true;
@@ -333,98 +368,127 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int wg = warp >> 2;               // column half: 64*wg .. 64*wg+63
+    const int wg = warp >> 2;                // score columns kCols*wg .. kCols*wg + kCols-1
     const int r = threadIdx.x & 127;         // score row, TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    constexpr int OC = D / kWG;              // output columns of this warpgroup
     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
-    int g = 0;
-    for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
-      const Task k = load_task(p, t);
+    // Thread 0 takes each task from the ring (and turns a timeout into the
+    // end marker) and broadcasts it through shared memory, so that every
+    // softmax warp runs the same loops and reaches the same named barriers.
+    auto group_sync = [&]() { named_bar_sync(kBarSoftmax, kSoftmaxThreads); };
+    int g = 0, tq = 0;
+    bool store_pending = false;  // thread 0: an output tile is being stored from Q buffer pend_qb
+    int pend_qb = 0;
+    for (int ti = 0;; ++ti) {
+      if (threadIdx.x == 0) {
+        const int tslot = ti % kTaskRing;
+        mbar_wait(b_tfull + 8 * tslot, (ti / kTaskRing) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        Task kk = tring[tslot];
+        mbar_arrive(b_tempty + 8 * tslot);
+        if (*abort_flag) kk.n = -1;
+        tdec[ti & 1] = kk;
+      }
+      group_sync();
+      const Task k = tdec[ti & 1];
+      if (k.n < 0) break;
       const bool row_ok = r < k.qv;
       const long long grow = static_cast<long long>(k.q_off) + k.m_block * kTile + r;
-      __nv_bfloat16* orow = p.o + (grow * p.Hq + k.h) * D + wg * (D / 2);
+      __nv_bfloat16* orow = p.o + (grow * p.Hq + k.h) * D + wg * OC;
       if (k.n == 0) {
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-          for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < OC / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           if (wg == 0 && p.lse != nullptr) p.lse[static_cast<long long>(k.h) * p.total_q + grow] = -INFINITY;
         }
         continue;
       }
+      const int qb = tq & 1;
       float slope = 0.0f;
       if (MODS && (p.flags & FA_MOD_ALIBI)) slope = p.slopes[k.h];
       const int q_local = k.m_block * kTile + r;
-      float m_run = -INFINITY, l_half = 0.0f;
+      float m_run = -INFINITY, l_part = 0.0f;
       for (int j = 0; j < k.n; ++j) {
         const int gi = g + j;
         const int sb = gi % 3;
         const bool partial = j < k.np;
-        uint2 pm = make_uint2(0xffffffffu, 0xffffffffu);
-        if (partial)
-          pm = __ldg(reinterpret_cast<const uint2*>(p.payload) + (static_cast<long long>(k.p0 + j) * kTile + r) * 2 + wg);
+        uint32_t pw = 0xffffffffu;  // predicate bits of this warpgroup's 32 columns
+        if (partial) pw = __ldg(p.payload + (static_cast<long long>(k.p0 + j) * kTile + r) * 4 + wg);
         int kt = 0;
         if (MODS) kt = tile_index(p, k, j);
         mbar_wait(b_sfull + 8 * sb, (gi / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         tc_fence_after();
-        float s[64];
-        tmem_ld64(lane_addr + 128u * sb + 64u * wg, s);
+        float s[kCols];
+        tmem_ld32f(lane_addr + 128u * sb + kCols * wg, s);
         if (MODS) {
-          // natural units: scale, softcap, ALiBi, predicate
+          // natural units: scale, softcap, ALiBi
           float amax = 0.0f;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < kCols; ++c) {
             s[c] *= p.scale;
             amax = fmaxf(amax, fabsf(s[c]));
           }
           if (p.flags & FA_MOD_SOFTCAP) {
             if (__any_sync(0xffffffffu, amax >= 0.5f * p.softcap)) {
 #pragma unroll
-              for (int c = 0; c < 64; ++c) s[c] = softcap_exp(s[c], p.softcap, p.inv_softcap);
+              for (int c = 0; c < kCols; ++c) s[c] = softcap_exp(s[c], p.softcap, p.inv_softcap);
             } else {
 #pragma unroll
-              for (int c = 0; c < 64; ++c) s[c] = softcap_series(s[c], p.softcap, p.inv_softcap);
+              for (int c = 0; c < kCols; ++c) s[c] = softcap_series(s[c], p.softcap, p.inv_softcap);
             }
           }
-          const float fd0 = static_cast<float>(kt * kTile + wg * 64 - q_local);  // k - q at column 0
+          const float fd0 = static_cast<float>(kt * kTile + wg * kCols - q_local);  // k - q at column 0
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = fmaf(slope, fd0 + static_cast<float>(c), s[c]);
+          for (int c = 0; c < kCols; ++c) s[c] = fmaf(slope, fd0 + static_cast<float>(c), s[c]);
         }
         if (partial) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const uint32_t w = (c < 32) ? pm.x : pm.y;
-            if (!((w >> (c & 31)) & 1u)) s[c] = -INFINITY;
-          }
+          for (int c = 0; c < kCols; ++c)
+            if (!((pw >> c) & 1u)) s[c] = -INFINITY;
         }
-        // row max of this half (four independent chains), then of the row
+        // row max of this quarter (four independent chains), then of the row
         float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
+        for (int c = 0; c < kCols; c += 8) {
           m0 = max3f(m0, s[c], s[c + 1]);
           m1 = max3f(m1, s[c + 2], s[c + 3]);
           m2 = max3f(m2, s[c + 4], s[c + 5]);
           m3 = max3f(m3, s[c + 6], s[c + 7]);
         }
-        const float mhalf = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-        float* xm = xmax + (gi & 1) * 256;
-        xm[wg * 128 + r] = mhalf;
+        float* xm = xmax + (gi & 1) * (kWG * 128);
+        xm[wg * 128 + r] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
         tc_fence_before();
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        group_sync();
         tc_fence_after();
-        const float mrow = fmaxf(mhalf, xm[(wg ^ 1) * 128 + r]);
-        // running max in the exponent's units (scaled log2 units without mods)
+        if (j == 0 && threadIdx.x == 0 && store_pending) {
+          // the previous task's output tile has left shared memory by now:
+          // hand its Q buffer back to the producer
+          bulk_wait_read_all();
+          mbar_arrive(b_qempty + 8 * pend_qb);
+          store_pending = false;
+        }
+        const float mrow = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
+        // Running max in the exponent's units (scaled log2 units without mods).
+        // The reference max only moves when the tile max exceeds it by more
+        // than kRescaleLog2 (a factor 256): exp values stay <= 256, and O
+        // and l are rescaled (after PV(g-1) completes) only when it moves.
         const float m_tile = MODS ? mrow : mrow * p.scale_log2;
-        const float m_new = fmaxf(m_run, m_tile);
-        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-        const float alpha = MODS ? ex2_approx((m_run - m_use) * kLog2e) : ex2_approx(m_run - m_use);
-        m_run = m_new;
+        const float th = MODS ? kRescaleLog2 * kLn2 : kRescaleLog2;
+        float alpha = 1.0f;
+        if (j == 0) {
+          m_run = m_tile;
+        } else if (m_tile > m_run + th) {
+          alpha = MODS ? ex2_approx((m_run - m_tile) * kLog2e) : ex2_approx(m_run - m_tile);
+          m_run = m_tile;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
         uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial sums
-        uint32_t pk[32];
+        uint32_t pk[kCols / 2];
         const uint64_t negm = f2_pack(-m_use, -m_use);
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < kCols; c += 2) {
           uint64_t x = f2_pack(s[c], s[c + 1]);
           x = MODS ? f2_mul(f2_add(x, negm), l2e2) : f2_fma(x, sc2, negm);
           float x0, x1;
@@ -441,22 +505,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float a0, a1;
         f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
-        l_half = l_half * alpha + (a0 + a1);
-        // P (bf16 pairs) over this half's 32 columns of the score buffer
-        tmem_st32(lane_addr + 128u * sb + 32u * wg, pk);
-        if (j > 0) {
-          mbar_wait(b_odone, (gi - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        l_part = l_part * alpha + (a0 + a1);
+        // P (bf16 pairs) of this quarter's keys into the score buffer's first 64 columns
+        tmem_st16(lane_addr + 128u * sb + (kCols / 2) * wg, pk);
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          // O holds PV(g-1): wait for it before rescaling
+          mbar_wait(b_pvdone + 8 * ((gi - 1) % 3), ((gi - 1) / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-              uint32_t v[32];
-              const uint32_t oa = lane_addr + C::kColO + wg * (D / 2) + 32u * c;
-              tmem_ld32(oa, v);
+          for (int c = 0; c < OC / 16; ++c) {
+            uint32_t v[16];
+            const uint32_t oa = lane_addr + C::kColO + wg * OC + 16u * c;
+            tmem_ld16(oa, v);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(oa, v);
-            }
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st16(oa, v);
           }
         }
         tmem_st_wait();
@@ -465,25 +528,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       g += k.n;
       // ---------------------------------------------------------- epilogue
-      mbar_wait(b_odone, (g - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+      mbar_wait(b_pvdone + 8 * ((g - 1) % 3), ((g - 1) / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
       tc_fence_after();
-      xsum[wg * 128 + r] = l_half;
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-      const float l = l_half + xsum[(wg ^ 1) * 128 + r];
+      // sum exchange through the max-exchange buffer of the next tile's parity
+      // (its last readers passed the previous tile's barrier); a second
+      // barrier keeps the next task's max exchange from overwriting it early
+      float* xs = xmax + (g & 1) * (kWG * 128);
+      xs[wg * 128 + r] = l_part;
+      group_sync();
+      const float l = (xs[r] + xs[128 + r]) + (xs[256 + r] + xs[384 + r]);
       const bool have = l > 0.0f;
       const float inv_l = have ? 1.0f / l : 0.0f;
+      // A full 128-row tile is staged in its task's Q buffer (no S MMA reads it
+      // any more: the last PV has completed) and written by one TMA store; a
+      // tail tile is stored row by row so that no other task's rows are touched.
+      const bool tma_out = (k.qv == kTile);
+      const uint32_t stage = sQ + qb * C::kTileBytes;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + C::kColO + wg * (D / 2) + 32u * c, v);
-        if (row_ok) {
-          uint32_t pkd[16];
+      for (int c = 0; c < OC / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(lane_addr + C::kColO + wg * OC + 16u * c, v);
+        uint32_t pkd[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int i = 0; i < 8; ++i)
+          pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
+        if (tma_out) {
+          const int col = wg * OC + 16 * c;         // first output column of these 16
+          const int chunk = col >> 6, unit = (col & 63) >> 3;
+          const uint32_t rowa = stage + chunk * 16384 + r * 128;
+          st_shared_v4(rowa + (((unit) ^ (r & 7)) << 4), pkd[0], pkd[1], pkd[2], pkd[3]);
+          st_shared_v4(rowa + (((unit + 1) ^ (r & 7)) << 4), pkd[4], pkd[5], pkd[6], pkd[7]);
+        } else if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+          dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+          dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+        }
+      }
+      if (tma_out) fence_proxy_async_smem();
+      group_sync();  // staging complete; also keeps the sum exchange slots alive until read
+      if (threadIdx.x == 0) {
+        if (tma_out) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_store_2d(&tmO, stage + c * 16384, k.h * D + c * 64, k.q_off + k.m_block * kTile);
+          bulk_commit_group();
+          store_pending = true;
+          pend_qb = qb;
+        } else {
+          mbar_arrive(b_qempty + 8 * qb);
         }
       }
       if (wg == 0 && row_ok && p.lse != nullptr) {
@@ -491,14 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (have) lse = MODS ? (m_run + __logf(l)) : (m_run + __log2f(l)) * kLn2;
         p.lse[static_cast<long long>(k.h) * p.total_q + grow] = lse;
       }
-      // the sum exchange slots are rewritten at the next task's epilogue only
-      // after at least one more softmax barrier, so no extra barrier is needed
+      ++tq;
       tc_fence_before();
     }
+    if (threadIdx.x == 0 && store_pending) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -539,9 +631,9 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   const Geometry& g = pl->geom;
   const int64_t rows_q = (g.layout == FA_LAYOUT_BSHD) ? int64_t(g.batch) * g.seqlen_q : g.total_q;
   const int64_t rows_k = (g.layout == FA_LAYOUT_BSHD) ? int64_t(g.batch) * g.seqlen_k : g.total_k;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, a.q, rows_q, g.heads_q, D) || !make_map(&mk, a.k, rows_k, g.heads_k, D) ||
-      !make_map(&mv, a.v, rows_k, g.heads_k, D)) {
+      !make_map(&mv, a.v, rows_k, g.heads_k, D) || !make_map(&mo, a.o, rows_q, g.heads_q, D)) {
     *why = "cuTensorMapEncodeTiled failed (pointer alignment or driver entry point)";
     return cudaErrorInvalidValue;
   }
@@ -580,7 +672,7 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   }
   // persistent: one CTA per SM (shared memory keeps it to one), tasks by static stride
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(pl->tasks, sms));
-  kern<<<grid, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, mo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "forward kernel launch failed";
   return e;
