@@ -8,8 +8,10 @@
 // Eq. 1, softmax(mod(Q K^T * scale)) V, with an online softmax: the score
 // matrix is never stored.
 //
-// Persistent CTAs (one per SM) walk the plan's work_desc with a static
-// stride.  576 threads, warp-specialised:
+// Persistent CTAs (one per SM) take tasks in work_desc order from a
+// call-local atomic counter ("Flex Attention Mask Plan Design" §4.8: the
+// queue counter is per-call workspace, so one plan can serve concurrent
+// calls).  576 threads, warp-specialised:
 //   warp 16     TMA producer: Q tiles into a 2-deep ring; K and V tiles into
 //               one ring, issued in the order the MMAs consume them (K of
 //               tile g+1 before V of tile g).
@@ -87,6 +89,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int Hq, Hk, Hmask, rows, total_q, ntasks;
+  int* counter;      // task queue head (zeroed before the launch)
   int flags;
   float scale;       // multiplies Q K^T
   float scale_log2;  // scale * log2(e)
@@ -99,7 +102,7 @@ struct FwdParams {
 struct Task {
   int m_block, h, b, qv, q_off, k_off, hk, p0, np, f0, n, pad;
 };
-constexpr int kTaskRing = 4;
+constexpr int kTaskRing = 2;  // tasks a CTA may hold ahead of its softmax warps
 
 __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
   Task k;
@@ -253,7 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(b_tfull + 8 * slot);  // release: the task is visible to the waiters
         ++ti;
       };
-      for (int t = blockIdx.x; t < p.ntasks; t += gridDim.x) {
+      for (;;) {
+        const int t = atomicAdd(p.counter, 1);
+        if (t >= p.ntasks) break;
         const Task k = load_task(p, t);
         publish(k);
         if (k.n == 0) continue;
@@ -639,6 +644,7 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   }
   FwdParams p{};
   p.ntasks = static_cast<int>(pl->tasks);
+  p.counter = a.counter;
   p.work = pl->work_desc;
   p.seq = pl->seq_desc;
   p.p_off = pl->p_off;

@@ -432,7 +432,14 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
   }
   const char* why = "";
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (g.head_dim == 64) ? bsm::launch_fwd_d64(a, st, &why) : bsm::launch_fwd_d128(a, st, &why);
+  // per-call task queue counter (stream-ordered workspace, released after the launch)
+  Alloc al{plan->custom_alloc ? &plan->alloc : nullptr, plan->device, st};
+  int* counter = static_cast<int*>(al.get(sizeof(int)));
+  if (!counter) return fail(FA_ERR_ALLOC, "task counter allocation failed");
+  a.counter = counter;
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int), st);
+  if (!e) e = (g.head_dim == 64) ? bsm::launch_fwd_d64(a, st, &why) : bsm::launch_fwd_d128(a, st, &why);
+  al.put(counter, sizeof(int));
   if (e) return fail(FA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   return FA_OK;
 }

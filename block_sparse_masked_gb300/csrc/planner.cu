@@ -434,12 +434,11 @@ __device__ __forceinline__ bool visible_at(const PayloadParams& p, int hm, int q
   }
 }
 
-// One CTA (4 warps) per partial entry; warp wi packs rows 32*wi .. 32*wi+31.
-// For each row the 32 lanes test 32 consecutive columns and a ballot forms
-// one uint32 word; lane i keeps the 4 words of row i and the warp stores
-// 32 rows x 16 bytes contiguously.
-template <int KIND>
-__global__ void __launch_bounds__(128) k_payload(PayloadParams p) {
+// Interval masks: one CTA (4 warps) per partial entry; warp wi packs rows
+// 32*wi .. 32*wi+31.  For each row the 32 lanes test 32 consecutive columns
+// and a ballot forms one uint32 word; lane i keeps the 4 words of row i and
+// the warp stores 32 rows x 16 bytes contiguously.
+__global__ void __launch_bounds__(128) k_payload_intervals(PayloadParams p) {
   const long long e = blockIdx.x;
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   const int flat = p.entry_row[e];
@@ -456,13 +455,67 @@ __global__ void __launch_bounds__(128) k_payload(PayloadParams p) {
 #pragma unroll
     for (int wd = 0; wd < kPayloadWords; ++wd) {
       const int col = j * kTile + wd * 32 + lane;
-      const bool v = (q_local < q_len) && (col < k_len) && visible_at<KIND>(p, hm, q_off, q_local, col);
+      const bool v = (q_local < q_len) && (col < k_len) &&
+                     visible_at<MASK_INTERVALS>(p, hm, q_off, q_local, col);
       const uint32_t word = __ballot_sync(kFull, v);
       if (lane == i) mine[wd] = word;
     }
   }
   uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + wi * 32 + lane;
   *dst = make_uint4(mine[0], mine[1], mine[2], mine[3]);
+}
+
+// Block masks: one warp per partial entry.  The rows of a tile that fall in
+// the same logical block row have identical predicate words, so the warp
+// walks the tile's row segments (one per logical block row, clipped to the
+// sample) and forms each segment's 4 words with 4 ballots over the columns;
+// lane l then stores rows l, l+32, l+64, l+96 (16 bytes each, coalesced).
+__global__ void __launch_bounds__(128) k_payload_blocks(PayloadParams p) {
+  const long long e = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (e >= p.P) return;
+  const int flat = p.entry_row[e];
+  const int hm = flat / p.rows, row = flat % p.rows;
+  const int j = p.p_idx[e];
+  const int b = p.row_batch[row];
+  const int32_t* s = p.seq + 8 * b;
+  const int q_len = s[2], k_len = s[3], row_begin = s[4];
+  const int q0 = (row - row_begin) * kTile;
+  const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
+  int cb[kPayloadWords];
+  bool cin[kPayloadWords];
+#pragma unroll
+  for (int wd = 0; wd < kPayloadWords; ++wd) {
+    const int col = j * kTile + wd * 32 + lane;
+    cin[wd] = col < k_len;
+    cb[wd] = cin[wd] ? col / p.block_kv : 0;
+  }
+  uint32_t mine[4][kPayloadWords];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int wd = 0; wd < kPayloadWords; ++wd) mine[i][wd] = 0;
+  const int r_end = min(kTile, q_len - q0);  // rows past the sample stay 0
+  for (int r = 0; r < r_end;) {
+    const int rb = (q0 + r) / p.block_q;
+    const int seg_end = min(r_end, (rb + 1) * p.block_q - q0);
+    const uint8_t* Mr = M + static_cast<long long>(rb) * p.nbk;
+    uint32_t words[kPayloadWords];
+#pragma unroll
+    for (int wd = 0; wd < kPayloadWords; ++wd)
+      words[wd] = __ballot_sync(kFull, cin[wd] && __ldg(Mr + cb[wd]) != 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int R = lane + 32 * i;
+      if (R >= r && R < seg_end)
+#pragma unroll
+        for (int wd = 0; wd < kPayloadWords; ++wd) mine[i][wd] = words[wd];
+    }
+    r = seg_end;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + lane;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
 }
 
 // ------------------------------------------------------------ schedule
@@ -660,9 +713,9 @@ cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanW
   pp.nbq = m.nbq;
   pp.nbk = m.nbk;
   if (m.kind == MASK_INTERVALS)
-    k_payload<MASK_INTERVALS><<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
+    k_payload_intervals<<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
   else
-    k_payload<MASK_BLOCKS><<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
+    k_payload_blocks<<<static_cast<unsigned>((plan->P + 3) / 4), 128, 0, st>>>(pp);
   return cudaGetLastError();
 }
 

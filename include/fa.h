@@ -167,7 +167,9 @@ typedef struct {
  * Every base pointer must be 16-byte aligned.  The geometry must equal the
  * one the plan was built for (FA_ERR_PLAN_MISMATCH otherwise).  The call
  * is asynchronous on `stream`; one plan may be used concurrently on
- * several streams.
+ * several streams.  Each call takes a 4-byte task-queue counter from the
+ * plan's allocator (or the library pool) in stream order and returns it
+ * after the launch.
  */
 int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, void* o,
            float* lse, const fa_geometry* geom, float scale, const fa_mods* mods,
