@@ -142,6 +142,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Work of every rank in one step over the (max-over-ranks) step time."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def visible_flops(info: dict, Hq: int, d: int) -> float:
     vp = info["visible_pairs"]
     heads = Hq if info["mask_heads"] == 1 else 1
@@ -285,13 +301,9 @@ def main():
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = tot_ms / args.steps
-    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, world, ms_per_step)
     fwd_mean = statistics.mean(fwd_ms)
     fwd_tflops = flops_step / (fwd_mean * 1e-3) / 1e12
 
@@ -323,12 +335,8 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / ksteps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ksteps, world)
+    e2e_val = whole_job_tflops(flops_step, world, e2e_ms)
     assert fa.fa_device_error_flags() == 0, "device error flags set"
 
     peaks, peak_src = load_peaks()

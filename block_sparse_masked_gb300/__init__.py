@@ -106,11 +106,12 @@ def lib():
         L.fa_plan_export.argtypes = [_vp, P(FaPlanHostView)]
         L.fa_device_error_flags.argtypes = [_vp, P(_u32)]
         L.fa_plan_header_noalloc.argtypes = [P(FaGeometry), _vp, _i32, _i32, _vp, _vp]
+        L.fa_selftest_wait_timeout.argtypes = [_u64, _vp]
         L.fa_last_error.restype = _c.c_char_p
         L.fa_version.restype = _c.c_char_p
         for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_free", "fa_fwd",
                   "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags",
-                  "fa_plan_header_noalloc"):
+                  "fa_plan_header_noalloc", "fa_selftest_wait_timeout"):
             getattr(L, f).restype = _c.c_int
         _LIB = L
     return _LIB
@@ -254,6 +255,11 @@ def fa_plan_export(plan: Plan) -> dict:
     _check(lib().fa_plan_export(plan.handle, _c.byref(view)))
     arrs["header"] = np.array(info["header"], np.int64)
     return arrs
+
+
+def fa_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None):
+    """Launch the never-completing bounded wait (see fa.h); read the result with fa_device_error_flags."""
+    _check(lib().fa_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)))
 
 
 def fa_device_error_flags(stream=None) -> int:

@@ -684,7 +684,26 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   return e;
 }
 
+// Nothing ever arrives on this barrier: every thread's bounded wait gives up
+// after timeout_ns, the first one records DEVERR_TIMEOUT, and the kernel ends.
+__global__ void k_wait_selftest(uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(smem_u32(&bar), 0, &abort_flag, &g_fwd_err, timeout_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st) {
+  k_wait_selftest<<<1, 64, 0, st>>>(timeout_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why) {
   return (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) ? launch_impl<64, true>(a, st, why)

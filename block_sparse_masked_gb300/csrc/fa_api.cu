@@ -519,6 +519,15 @@ int fa_device_error_flags(void* stream, uint32_t* flags) {
   return FA_OK;
 }
 
+int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+  t_err.clear();
+  if (timeout_ns < 1000 || timeout_ns > 100000000ull)
+    return fail(FA_ERR_INVALID_ARG, "timeout_ns must be in [1 us, 100 ms]");
+  cudaError_t e = bsm::launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream));
+  if (e) return cuda_fail(e, "self-test launch");
+  return FA_OK;
+}
+
 const char* fa_last_error(void) { return t_err.c_str(); }
 
 const char* fa_version(void) { return "block_sparse_masked_gb300 0.1 (sm_103a)"; }

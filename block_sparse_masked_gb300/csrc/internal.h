@@ -126,6 +126,7 @@ struct FwdLaunch {
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
 
 // ---- error reporting and argument checks shared with fa_plan_header_noalloc
 void clear_last_error();

@@ -437,7 +437,12 @@ __device__ __forceinline__ bool visible_at(const PayloadParams& p, int hm, int q
 // Interval masks: one CTA (4 warps) per partial entry; warp wi packs rows
 // 32*wi .. 32*wi+31.  For each row the 32 lanes test 32 consecutive columns
 // and a ballot forms one uint32 word; lane i keeps the 4 words of row i and
-// the warp stores 32 rows x 16 bytes contiguously.
+// the warp stores 32 rows x 16 bytes contiguously.  With at most kMaxFuncFast
+// endpoints per row, lane i loads row i's endpoints once and the warp
+// broadcasts them with shuffles; otherwise every lane reads them per row.
+constexpr int kMaxFuncFast = 9;
+
+template <bool FAST>
 __global__ void __launch_bounds__(128) k_payload_intervals(PayloadParams p) {
   const long long e = blockIdx.x;
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
@@ -448,16 +453,44 @@ __global__ void __launch_bounds__(128) k_payload_intervals(PayloadParams p) {
   const int32_t* s = p.seq + 8 * b;
   const int q_off = s[0], q_len = s[2], k_len = s[3], row_begin = s[4];
   const int q0 = (row - row_begin) * kTile;
+  const int c0 = j * kTile;
+  const int32_t* Fbase = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off;
+  const long long fs = p.total_q;
+  int myF[kMaxFuncFast];
+  if (FAST) {
+    const int q_mine = q0 + wi * 32 + lane;
+#pragma unroll
+    for (int f = 0; f < kMaxFuncFast; ++f)
+      myF[f] = (f < p.nfunc && q_mine < q_len) ? __ldg(Fbase + f * fs + q_mine) : 0;
+  }
   uint32_t mine[kPayloadWords] = {0, 0, 0, 0};
   for (int i = 0; i < 32; ++i) {
-    const int r = wi * 32 + i;
-    const int q_local = q0 + r;
+    const int q_local = q0 + wi * 32 + i;
+    if (q_local >= q_len) break;  // uniform: rows past the sample stay 0
+    bool in[kPayloadWords];
+    if (FAST) {
+      int F[kMaxFuncFast];
+#pragma unroll
+      for (int f = 0; f < kMaxFuncFast; ++f) F[f] = __shfl_sync(kFull, myF[f], i);
+#pragma unroll
+      for (int wd = 0; wd < kPayloadWords; ++wd) {
+        const int col = c0 + wd * 32 + lane;
+        bool v = col < F[0];
+#pragma unroll
+        for (int f = 1; f + 1 < kMaxFuncFast; f += 2)
+          if (f + 1 < p.nfunc) v |= (col >= F[f]) && (col < F[f + 1]);
+        in[wd] = v && (col < k_len);
+      }
+    } else {
+#pragma unroll
+      for (int wd = 0; wd < kPayloadWords; ++wd) {
+        const int col = c0 + wd * 32 + lane;
+        in[wd] = (col < k_len) && visible_at<MASK_INTERVALS>(p, hm, q_off, q_local, col);
+      }
+    }
 #pragma unroll
     for (int wd = 0; wd < kPayloadWords; ++wd) {
-      const int col = j * kTile + wd * 32 + lane;
-      const bool v = (q_local < q_len) && (col < k_len) &&
-                     visible_at<MASK_INTERVALS>(p, hm, q_off, q_local, col);
-      const uint32_t word = __ballot_sync(kFull, v);
+      const uint32_t word = __ballot_sync(kFull, in[wd]);
       if (lane == i) mine[wd] = word;
     }
   }
@@ -712,8 +745,10 @@ cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanW
   pp.block_kv = m.block_kv;
   pp.nbq = m.nbq;
   pp.nbk = m.nbk;
-  if (m.kind == MASK_INTERVALS)
-    k_payload_intervals<<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
+  if (m.kind == MASK_INTERVALS && m.nfunc <= kMaxFuncFast)
+    k_payload_intervals<true><<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
+  else if (m.kind == MASK_INTERVALS)
+    k_payload_intervals<false><<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
   else
     k_payload_blocks<<<static_cast<unsigned>((plan->P + 3) / 4), 128, 0, st>>>(pp);
   return cudaGetLastError();

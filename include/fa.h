@@ -226,10 +226,20 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);
 /*
  * Error bits written by the forward kernels on the current device (bit 0:
  * a bounded in-kernel wait ran out and the kernel stopped early, so its
- * output is incomplete).  Synchronises `stream`, returns the bits in
+ * output is incomplete; bit 1: dynamic shared memory was not aligned as
+ * the kernel requires, so it did no work).  Synchronises `stream`, returns the bits in
  * *flags and clears them.
  */
 int fa_device_error_flags(void* stream, uint32_t* flags);
+
+/*
+ * Diagnostic of the bounded in-kernel waits: launches one small kernel on
+ * `stream` whose mbarrier wait can never complete.  Each wait gives up after
+ * timeout_ns (1 us .. 100 ms), bit 0 of the device error flags is set and
+ * the kernel ends normally, so the CUDA context stays usable; read the bit
+ * with fa_device_error_flags.  Nothing faults, traps or hangs.
+ */
+int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 
 /*
  * Allocation-free sizing of an interval plan.  The paper has no counterpart
