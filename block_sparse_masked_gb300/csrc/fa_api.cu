@@ -189,12 +189,15 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   ws.kt_ub = kt_ub;
   ws.words = words;
   const long long nflat_ub = static_cast<long long>(Hmask) * rows_ub;
+  const int NS = B * g.heads_k;  // schedule sections
+  const int C = kt_ub;           // largest task cost
   Carver c1;
   const size_t o_err = c1.take(4), o_hdr = c1.take(64), o_cur = c1.take(4ull * (B + 1)),
                o_seq = c1.take(32ull * B), o_rb = c1.take(4ull * rows_ub),
                o_vis = c1.take(4ull * nflat_ub * words), o_full = c1.take(4ull * nflat_ub * words),
                o_pc = c1.take(4ull * nflat_ub), o_fc = c1.take(4ull * nflat_ub),
-               o_po = c1.take(4ull * (nflat_ub + 1)), o_fo = c1.take(4ull * (nflat_ub + 1));
+               o_po = c1.take(4ull * (nflat_ub + 1)), o_fo = c1.take(4ull * (nflat_ub + 1)),
+               o_hist = c1.take(4ull * NS * (C + 1)), o_cursor = c1.take(4ull * NS * (C + 1));
   Alloc al{allocator, dev, st};
   uint8_t* w1 = static_cast<uint8_t*>(al.get(c1.off));
   if (!w1) return fail(FA_ERR_ALLOC, "workspace allocation of %zu bytes failed", c1.off);
@@ -209,14 +212,16 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   ws.f_cnt = reinterpret_cast<int32_t*>(w1 + o_fc);
   ws.p_off = reinterpret_cast<int32_t*>(w1 + o_po);
   ws.f_off = reinterpret_cast<int32_t*>(w1 + o_fo);
+  ws.hist = reinterpret_cast<int32_t*>(w1 + o_hist);
+  ws.cursors = reinterpret_cast<int32_t*>(w1 + o_cursor);
 
   auto bail = [&](int code) {
     al.put(w1, c1.off);
     return code;
   };
 
-  cudaError_t e = cudaMemsetAsync(ws.err, 0, 4, st);
-  if (!e) e = bsm::launch_geometry(g, gi->cu_seqlens_q, gi->cu_seqlens_k, ws, st);
+  // the geometry kernel zeroes the error word before anything sets it
+  cudaError_t e = bsm::launch_geometry(g, gi->cu_seqlens_q, gi->cu_seqlens_k, ws, st);
   if (!e) e = bsm::launch_classify(g, margs, ws, st);
   if (!e) e = bsm::launch_scan_header(g, Hmask, ws, st);
   long long* hh = pinned_header();
@@ -258,7 +263,8 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
                q_pi = c2.take(4ull * plan->P), q_fi = c2.take(4ull * plan->F),
                q_pay = c2.take(16ull * bsm::kTile * plan->P), q_work = c2.take(16ull * plan->tasks),
                q_cq = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
-               q_ck = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0);
+               q_ck = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
+               q_er = c2.take(4ull * plan->P);
   uint8_t* pm = static_cast<uint8_t*>(al.get(c2.off));
   if (!pm) {
     delete plan;
@@ -278,37 +284,16 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
     plan->cu_seqlens_q = reinterpret_cast<int32_t*>(pm + q_cq);
     plan->cu_seqlens_k = reinterpret_cast<int32_t*>(pm + q_ck);
   }
+  plan->entry_row = reinterpret_cast<int32_t*>(pm + q_er);
 
-  // second workspace: entry -> row map and the schedule's counting buffers
-  const int NS = B * g.heads_k;
-  const int C = kt_ub;
-  Carver c3;
-  const size_t r_er = c3.take(4ull * plan->P), r_h = c3.take(4ull * NS * (C + 1)),
-               r_c = c3.take(4ull * NS * (C + 1));
-  uint8_t* w2 = static_cast<uint8_t*>(al.get(c3.off));
-  auto bail2 = [&](int code) {
-    al.put(w2, c3.off);
+  // exact-size copies, CSR lists, payloads (two launches), schedule (one launch)
+  e = bsm::launch_materialize(g, margs, ws, plan, gi->cu_seqlens_q, gi->cu_seqlens_k, st);
+  if (!e) e = bsm::launch_schedule(g, plan, ws.hist, ws.cursors, NS, C, st);
+  if (e) {
     free_plan_mem(plan, st);
     delete plan;
-    return bail(code);
-  };
-  if (!w2) return bail2(fail(FA_ERR_ALLOC, "workspace allocation of %zu bytes failed", c3.off));
-
-  e = cudaMemcpyAsync(plan->cu_q_rows, ws.cu_rows, 4ull * (B + 1), cudaMemcpyDeviceToDevice, st);
-  if (!e) e = cudaMemcpyAsync(plan->seq_desc, ws.seq, 32ull * B, cudaMemcpyDeviceToDevice, st);
-  if (!e) e = cudaMemcpyAsync(plan->p_off, ws.p_off, 4ull * (nflat + 1), cudaMemcpyDeviceToDevice, st);
-  if (!e) e = cudaMemcpyAsync(plan->f_off, ws.f_off, 4ull * (nflat + 1), cudaMemcpyDeviceToDevice, st);
-  if (!e && g.layout == FA_LAYOUT_THD) {
-    e = cudaMemcpyAsync(plan->cu_seqlens_q, gi->cu_seqlens_q, 4ull * (B + 1), cudaMemcpyDeviceToDevice, st);
-    if (!e)
-      e = cudaMemcpyAsync(plan->cu_seqlens_k, gi->cu_seqlens_k, 4ull * (B + 1), cudaMemcpyDeviceToDevice, st);
+    return bail(cuda_fail(e, "planner (materialize/payload/schedule)"));
   }
-  if (!e) e = bsm::launch_materialize(g, margs, ws, plan, reinterpret_cast<int32_t*>(w2 + r_er), st);
-  if (!e)
-    e = bsm::launch_schedule(g, ws, plan, reinterpret_cast<int32_t*>(w2 + r_h),
-                             reinterpret_cast<int32_t*>(w2 + r_c), NS, C, st);
-  if (e) return bail2(cuda_fail(e, "planner (materialize/payload/schedule)"));
-  al.put(w2, c3.off);
   al.put(w1, c1.off);
   plan->build_us =
       std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();

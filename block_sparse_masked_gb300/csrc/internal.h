@@ -66,6 +66,7 @@ struct fa_plan {
   int32_t* work_desc = nullptr;     // [tasks*4]
   int32_t* cu_seqlens_q = nullptr;  // clones (THD)
   int32_t* cu_seqlens_k = nullptr;
+  int32_t* entry_row = nullptr;     // [P] planner scratch kept with the plan: flat row of each entry
 };
 
 namespace bsm {
@@ -83,6 +84,8 @@ struct PlanWorkspace {
   int32_t* f_cnt;
   int32_t* p_off;         // [Hmask*rows_ub+1]
   int32_t* f_off;
+  int32_t* hist;          // schedule counting buffers [num_sections*(max_cost+1)]
+  int32_t* cursors;
   int rows_ub, kt_ub, words;
 };
 
@@ -101,12 +104,14 @@ cudaError_t launch_classify(const Geometry& g, const MaskArgs& m, const PlanWork
                             cudaStream_t st);
 cudaError_t launch_scan_header(const Geometry& g, int Hmask, const PlanWorkspace& ws,
                                cudaStream_t st);
-// After the header: CSR lists, the entry->row map, payloads and the schedule.
+// After the header: exact-size copies into the plan, CSR lists, the
+// entry->row map, payloads (one launch each for CSR+copies and payload) and
+// the schedule (one launch).
 cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
-                               fa_plan* plan, int32_t* entry_row, cudaStream_t st);
-cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, fa_plan* plan,
-                            int32_t* hist, int32_t* cursors, int num_sections, int max_cost,
-                            cudaStream_t st);
+                               fa_plan* plan, const int32_t* cu_q_src, const int32_t* cu_k_src,
+                               cudaStream_t st);
+cudaError_t launch_schedule(const Geometry& g, fa_plan* plan, int32_t* hist, int32_t* cursors,
+                            int num_sections, int max_cost, cudaStream_t st);
 cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, cudaStream_t st);
 
 // ---- forward (attn_fwd*.cu) ---------------------------------------------

@@ -76,6 +76,8 @@ struct GeoParams {
 };
 
 __global__ void __launch_bounds__(1024) k_geometry(GeoParams g) {
+  if (threadIdx.x == 0) *g.err = 0;  // the build's error word starts here
+  __syncthreads();
   long long carry = 0;
   for (int base = 0; base < g.B; base += 1024) {
     const int b = base + threadIdx.x;
@@ -351,18 +353,30 @@ __global__ void __launch_bounds__(1024) k_scan_header(ScanParams p) {
 struct MatParams {
   const uint32_t* vis_bits;
   const uint32_t* full_bits;
-  const int32_t* p_off;  // exact [Hmask*rows+1]
+  const int32_t* p_off;  // workspace offsets, exact [Hmask*rows+1] layout
   const int32_t* f_off;
   int32_t* p_idx;
   int32_t* f_idx;
   int32_t* entry_row;  // [P]: flat (hm*rows + row) of each partial entry
   int rows, rows_ub, words;
+  // exact-size copies into the plan, done by the same launch
+  const int32_t* src[6];
+  int32_t* dst[6];
+  long long count[6];
 };
 
 // One warp per (row, mask head): lane w handles bitset word w; ranks come
 // from a warp scan of popcounts, so indices come out ascending.
 __global__ void __launch_bounds__(32) k_materialize(MatParams p) {
+  {
+    const long long tid = (static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x) * 32 + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * gridDim.y * 32;
+#pragma unroll
+    for (int a = 0; a < 6; ++a)
+      for (long long i = tid; i < p.count[a]; i += nthreads) p.dst[a][i] = p.src[a][i];
+  }
   const int row = blockIdx.x, hm = blockIdx.y, lane = threadIdx.x;
+  if (row >= p.rows) return;
   const long long flat = static_cast<long long>(hm) * p.rows + row;
   const long long ws_row = static_cast<long long>(hm) * p.rows_ub + row;
   int pbase = p.p_off[flat], fbase = p.f_off[flat];
@@ -572,40 +586,44 @@ __device__ __forceinline__ int task_bucket(const SchedParams& p, int cost) {
   return cost > 0 ? (p.C - min(cost, p.C)) : p.C;
 }
 
-// Section s = (sample b, K/V head hk); its tasks in tie order are
-// (h in the head group, m_block).
-__global__ void __launch_bounds__(256) k_sched_hist(SchedParams p) {
-  const int sct = blockIdx.x;
-  const int group = p.Hq / p.Hk;
-  const int b = sct / p.Hk, hk = sct % p.Hk;
-  const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5];
-  const int n = group * nrows;
-  for (int t = threadIdx.x; t < n; t += blockDim.x) {
-    const int h = hk * group + t / nrows, m = t % nrows;
-    const int c = task_cost(p, h, begin + m);
-    atomicAdd(&p.hist[static_cast<long long>(sct) * (p.C + 1) + task_bucket(p, c)], 1);
-  }
-}
-
-// One CTA: positive-cost tasks of section s start after all positive tasks of
-// sections < s, ordered by bucket; zero-cost tasks follow every positive task,
-// sections in order.
-__global__ void __launch_bounds__(1024) k_sched_offsets(SchedParams p) {
-  __shared__ long long s_tot_pos;
+// One CTA builds the whole schedule with bounded counting:
+//  1. histogram of (section, cost bucket) over every task;
+//  2. offsets: positive-cost tasks of section s start after every positive
+//     task of sections < s, ordered by bucket (cost descending); zero-cost
+//     tasks follow every positive task, sections in order;
+//  3. scatter: one warp per section walks its tasks in tie order (head in the
+//     section's group, then m_block), 32 at a time; lanes with the same
+//     bucket take consecutive slots in lane order, so the sort is stable.
+// Section s = (sample b, K/V head hk).
+__global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   const int C = p.C;
+  const int group = p.Hq / p.Hk;
+  const long long nb = static_cast<long long>(p.NS) * (C + 1);
+  for (long long i = threadIdx.x; i < nb; i += blockDim.x) p.hist[i] = 0;
+  __syncthreads();
+  for (int sct = 0; sct < p.NS; ++sct) {
+    const int b = sct / p.Hk, hk = sct % p.Hk;
+    const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5];
+    const int n = group * nrows;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      const int h = hk * group + t / nrows, m = t % nrows;
+      atomicAdd(&p.hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, h, begin + m))], 1);
+    }
+  }
+  __syncthreads();
+  __shared__ long long s_tot_pos;
   long long carry_pos = 0;
-  // pass 1: positive totals -> section starts; stash in cursors[s*(C+1)+C] temporarily
   for (int base = 0; base < p.NS; base += 1024) {
-    const int s = base + threadIdx.x;
+    const int sct = base + threadIdx.x;
     long long pos = 0;
-    if (s < p.NS)
-      for (int c = 0; c < C; ++c) pos += p.hist[static_cast<long long>(s) * (C + 1) + c];
+    if (sct < p.NS)
+      for (int c = 0; c < C; ++c) pos += p.hist[static_cast<long long>(sct) * (C + 1) + c];
     long long tot;
     const long long start = carry_pos + block_excl_scan(pos, &tot);
-    if (s < p.NS) {
+    if (sct < p.NS) {
       long long run = start;
       for (int c = 0; c < C; ++c) {
-        const long long i = static_cast<long long>(s) * (C + 1) + c;
+        const long long i = static_cast<long long>(sct) * (C + 1) + c;
         p.cursors[i] = static_cast<int32_t>(run);
         run += p.hist[i];
       }
@@ -616,45 +634,40 @@ __global__ void __launch_bounds__(1024) k_sched_offsets(SchedParams p) {
   __syncthreads();
   long long carry_zero = s_tot_pos;
   for (int base = 0; base < p.NS; base += 1024) {
-    const int s = base + threadIdx.x;
-    const long long z = (s < p.NS) ? p.hist[static_cast<long long>(s) * (C + 1) + C] : 0;
+    const int sct = base + threadIdx.x;
+    const long long z = (sct < p.NS) ? p.hist[static_cast<long long>(sct) * (C + 1) + C] : 0;
     long long tot;
     const long long start = carry_zero + block_excl_scan(z, &tot);
-    if (s < p.NS) p.cursors[static_cast<long long>(s) * (C + 1) + C] = static_cast<int32_t>(start);
+    if (sct < p.NS) p.cursors[static_cast<long long>(sct) * (C + 1) + C] = static_cast<int32_t>(start);
     carry_zero += tot;
   }
-}
-
-// One warp per section walks its tasks in tie order, 32 at a time; lanes with
-// the same bucket take consecutive slots in lane order (stable).
-__global__ void __launch_bounds__(128) k_sched_scatter(SchedParams p) {
-  const int sct = blockIdx.x * 4 + (threadIdx.x >> 5);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  if (sct >= p.NS) return;
-  const int group = p.Hq / p.Hk;
-  const int b = sct / p.Hk, hk = sct % p.Hk;
-  const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5], q_len = p.seq[8 * b + 2];
-  const int n = group * nrows;
-  int32_t* cur = p.cursors + static_cast<long long>(sct) * (p.C + 1);
-  for (int t0 = 0; t0 < n; t0 += 32) {
-    const int t = t0 + lane;
-    const bool act = t < n;
-    const unsigned amask = __ballot_sync(kFull, act);
-    if (act) {
-      const int h = hk * group + t / nrows, m = t % nrows;
-      const int bucket = task_bucket(p, task_cost(p, h, begin + m));
-      const unsigned same = __match_any_sync(amask, bucket);
-      const int rank = __popc(same & ((1u << lane) - 1));
-      const int pos = cur[bucket] + rank;
-      int32_t* wd = p.work + 4LL * pos;
-      wd[0] = m;
-      wd[1] = h;
-      wd[2] = b;
-      wd[3] = min(kTile, q_len - m * kTile);
-      __syncwarp(amask);
-      if (rank == 0) cur[bucket] += __popc(same);
+  for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
+    const int b = sct / p.Hk, hk = sct % p.Hk;
+    const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5], q_len = p.seq[8 * b + 2];
+    const int n = group * nrows;
+    int32_t* cur = p.cursors + static_cast<long long>(sct) * (C + 1);
+    for (int t0 = 0; t0 < n; t0 += 32) {
+      const int t = t0 + lane;
+      const bool act = t < n;
+      const unsigned amask = __ballot_sync(kFull, act);
+      if (act) {
+        const int h = hk * group + t / nrows, m = t % nrows;
+        const int bucket = task_bucket(p, task_cost(p, h, begin + m));
+        const unsigned same = __match_any_sync(amask, bucket);
+        const int rank = __popc(same & ((1u << lane) - 1));
+        const int pos = cur[bucket] + rank;
+        int32_t* wd = p.work + 4LL * pos;
+        wd[0] = m;
+        wd[1] = h;
+        wd[2] = b;
+        wd[3] = min(kTile, q_len - m * kTile);
+        __syncwarp(amask);
+        if (rank == 0) cur[bucket] += __popc(same);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
 }
 
@@ -721,16 +734,37 @@ cudaError_t launch_scan_header(const Geometry& g, int Hmask, const PlanWorkspace
 }
 
 cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
-                               fa_plan* plan, int32_t* entry_row, cudaStream_t st) {
+                               fa_plan* plan, const int32_t* cu_q_src, const int32_t* cu_k_src,
+                               cudaStream_t st) {
   const int rows = static_cast<int>(plan->rows);
-  if (rows == 0) return cudaSuccess;
-  MatParams mp{ws.vis_bits, ws.full_bits, plan->p_off, plan->f_off, plan->p_idx, plan->f_idx,
-               entry_row, rows, ws.rows_ub, ws.words};
-  k_materialize<<<dim3(rows, m.Hmask), 32, 0, st>>>(mp);
+  const long long nflat = static_cast<long long>(m.Hmask) * rows;
+  MatParams mp{};
+  mp.vis_bits = ws.vis_bits;
+  mp.full_bits = ws.full_bits;
+  mp.p_off = ws.p_off;
+  mp.f_off = ws.f_off;
+  mp.p_idx = plan->p_idx;
+  mp.f_idx = plan->f_idx;
+  mp.entry_row = plan->entry_row;
+  mp.rows = rows;
+  mp.rows_ub = ws.rows_ub;
+  mp.words = ws.words;
+  const int32_t* src[6] = {ws.cu_rows, ws.seq, ws.p_off, ws.f_off, cu_q_src, cu_k_src};
+  int32_t* dst[6] = {plan->cu_q_rows, plan->seq_desc, plan->p_off, plan->f_off, plan->cu_seqlens_q,
+                     plan->cu_seqlens_k};
+  const long long cnt[6] = {g.batch + 1LL, 8LL * g.batch, nflat + 1, nflat + 1,
+                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0,
+                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0};
+  for (int a = 0; a < 6; ++a) {
+    mp.src[a] = src[a];
+    mp.dst[a] = dst[a];
+    mp.count[a] = cnt[a];
+  }
+  k_materialize<<<dim3(rows > 0 ? rows : 1, rows > 0 ? m.Hmask : 1), 32, 0, st>>>(mp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || plan->P == 0) return e;
   PayloadParams pp{};
-  pp.entry_row = entry_row;
+  pp.entry_row = plan->entry_row;
   pp.p_idx = plan->p_idx;
   pp.row_batch = ws.row_batch;
   pp.seq = ws.seq;
@@ -754,18 +788,13 @@ cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanW
   return cudaGetLastError();
 }
 
-cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, fa_plan* plan,
-                            int32_t* hist, int32_t* cursors, int num_sections, int max_cost,
-                            cudaStream_t st) {
+cudaError_t launch_schedule(const Geometry& g, fa_plan* plan, int32_t* hist, int32_t* cursors,
+                            int num_sections, int max_cost, cudaStream_t st) {
   if (plan->tasks == 0) return cudaSuccess;
   SchedParams p{plan->seq_desc, plan->p_off, plan->f_off, hist, cursors, plan->work_desc,
                 g.batch, g.heads_q, g.heads_k, plan->Hmask, static_cast<int>(plan->rows),
                 max_cost, num_sections};
-  cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(int32_t) * num_sections * (max_cost + 1), st);
-  if (e != cudaSuccess) return e;
-  k_sched_hist<<<num_sections, 256, 0, st>>>(p);
-  k_sched_offsets<<<1, 1024, 0, st>>>(p);
-  k_sched_scatter<<<(num_sections + 3) / 4, 128, 0, st>>>(p);
+  k_schedule<<<1, 1024, 0, st>>>(p);
   return cudaGetLastError();
 }
 
