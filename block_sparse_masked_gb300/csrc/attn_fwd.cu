@@ -142,6 +142,19 @@ __device__ __forceinline__ float softcap_series(float x, float cap, float inv_ca
   s = fmaf(s, y2, -1.0f / 3.0f);
   return cap * fmaf(s * y2, y, y);
 }
+// Two columns of softcap_series at once in packed fp32.
+__device__ __forceinline__ void softcap_series2(float& x0, float& x1, float cap, float inv_cap) {
+  const uint64_t y = f2_mul(f2_pack(x0, x1), f2_pack(inv_cap, inv_cap));
+  const uint64_t y2 = f2_mul(y, y);
+  uint64_t s = f2_pack(21844.0f / 6081075.0f, 21844.0f / 6081075.0f);
+  s = f2_fma(s, y2, f2_pack(-1382.0f / 155925.0f, -1382.0f / 155925.0f));
+  s = f2_fma(s, y2, f2_pack(62.0f / 2835.0f, 62.0f / 2835.0f));
+  s = f2_fma(s, y2, f2_pack(-17.0f / 315.0f, -17.0f / 315.0f));
+  s = f2_fma(s, y2, f2_pack(2.0f / 15.0f, 2.0f / 15.0f));
+  s = f2_fma(s, y2, f2_pack(-1.0f / 3.0f, -1.0f / 3.0f));
+  const uint64_t t = f2_fma(f2_mul(s, y2), y, y);
+  f2_unpack(f2_mul(t, f2_pack(cap, cap)), x0, x1);
+}
 // cap * tanh(x / cap) for any x, from tanh(y) = 1 - 2 / (exp(2y) + 1).
 __device__ __forceinline__ float softcap_exp(float x, float cap, float inv_cap) {
   const float e = ex2_approx(2.0f * kLog2e * (x * inv_cap));
@@ -428,12 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[kCols];
         tmem_ld32f(lane_addr + 128u * sb + kCols * wg, s);
         if (MODS) {
-          // natural units: scale, softcap, ALiBi
+          // natural units: scale, softcap, ALiBi (pairs of columns in packed fp32)
+          const uint64_t sc = f2_pack(p.scale, p.scale);
           float amax = 0.0f;
 #pragma unroll
-          for (int c = 0; c < kCols; ++c) {
-            s[c] *= p.scale;
-            amax = fmaxf(amax, fabsf(s[c]));
+          for (int c = 0; c < kCols; c += 2) {
+            f2_unpack(f2_mul(f2_pack(s[c], s[c + 1]), sc), s[c], s[c + 1]);
+            amax = max3f(amax, fabsf(s[c]), fabsf(s[c + 1]));
           }
           if (p.flags & FA_MOD_SOFTCAP) {
             if (__any_sync(0xffffffffu, amax >= 0.5f * p.softcap)) {
@@ -441,12 +455,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < kCols; ++c) s[c] = softcap_exp(s[c], p.softcap, p.inv_softcap);
             } else {
 #pragma unroll
-              for (int c = 0; c < kCols; ++c) s[c] = softcap_series(s[c], p.softcap, p.inv_softcap);
+              for (int c = 0; c < kCols; c += 2) softcap_series2(s[c], s[c + 1], p.softcap, p.inv_softcap);
             }
           }
-          const float fd0 = static_cast<float>(kt * kTile + wg * kCols - q_local);  // k - q at column 0
+          if (p.flags & FA_MOD_ALIBI) {
+            const float fd0 = static_cast<float>(kt * kTile + wg * kCols - q_local);  // k - q at column 0
+            const uint64_t sl = f2_pack(slope, slope);
 #pragma unroll
-          for (int c = 0; c < kCols; ++c) s[c] = fmaf(slope, fd0 + static_cast<float>(c), s[c]);
+            for (int c = 0; c < kCols; c += 2) {
+              const uint64_t kq = f2_pack(fd0 + static_cast<float>(c), fd0 + static_cast<float>(c + 1));
+              f2_unpack(f2_fma(sl, kq, f2_pack(s[c], s[c + 1])), s[c], s[c + 1]);
+            }
+          }
         }
         if (partial) {
 #pragma unroll
