@@ -76,7 +76,7 @@ class FaPlanInfo(_c.Structure):
 class FaPlanHostView(_c.Structure):
     _fields_ = [("cu_q_rows", _vp), ("sequence_desc", _vp), ("partial_offset", _vp),
                 ("partial_idx", _vp), ("full_offset", _vp), ("full_idx", _vp), ("payload", _vp),
-                ("work_desc", _vp)]
+                ("work_desc", _vp), ("halves", _vp)]
 
 
 class FaError(RuntimeError):
@@ -250,6 +250,7 @@ def fa_plan_export(plan: Plan) -> dict:
         "full_idx": np.zeros(F, np.int32),
         "payload": np.zeros((P, FA_TILE_Q, FA_PAYLOAD_WORDS), np.uint32),
         "work_desc": np.zeros((T, 4), np.int32),
+        "halves": np.zeros(P, np.uint8),
     }
     view = FaPlanHostView(*[a.ctypes.data if a.size else None for a in arrs.values()])
     _check(lib().fa_plan_export(plan.handle, _c.byref(view)))

@@ -86,6 +86,7 @@ struct FwdParams {
   const int32_t* p_idx;
   const int32_t* f_idx;
   const uint32_t* payload;
+  const uint8_t* halves;  // [P] bit s: key columns 64s..64s+63 of the entry hold a visible element
   __nv_bfloat16* o;
   float* lse;
   int Hq, Hk, Hmask, rows, total_q, ntasks;
@@ -128,6 +129,12 @@ __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
 __device__ __forceinline__ int tile_index(const FwdParams& p, const Task& k, int j) {
   return (j < k.np) ? __ldg(p.p_idx + k.p0 + j) : __ldg(p.f_idx + k.f0 + (j - k.np));
 }
+// Key halves of tile j that hold a visible element (bit s: keys 64s..64s+63);
+// full tiles use both.  A tile with one empty half loads, multiplies and
+// exponentiates only the other half.
+__device__ __forceinline__ int tile_halves(const FwdParams& p, const Task& k, int j) {
+  return (j < k.np) ? static_cast<int>(__ldg(p.halves + k.p0 + j)) : 3;
+}
 
 // cap * tanh(x / cap) for |x / cap| < 0.5: Maclaurin series of tanh through
 // y^13 (truncation error below 1e-6 relative at |y| = 0.5, far less below).
@@ -161,10 +168,13 @@ __device__ __forceinline__ float softcap_exp(float x, float cap, float inv_cap) 
   return cap * (1.0f - __fdividef(2.0f, e + 1.0f));
 }
 
-template <int D, bool MODS>
+// HALVES: the plan may hold partial tiles with an empty 64-key half (block
+// masks); those load, multiply and exponentiate only the live half.
+template <int D, bool MODS, bool HALVES>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+          const __grid_constant__ CUtensorMap tmKh, const __grid_constant__ CUtensorMap tmVh,
           const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   constexpr int NS = C::kSlots;
@@ -189,12 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_tempty = b_tfull + 8 * kTaskRing;
 
   uint8_t* small = gbase + C::kOffSmall;
+  int* slot_hm = reinterpret_cast<int*>(small + 400);  // [NS] key halves of the K tile in each ring slot
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + 480);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(small + 488);
   Task* tring = reinterpret_cast<Task*>(small + 512);    // [kTaskRing]
   Task* tdec = reinterpret_cast<Task*>(small + 768);     // [2] task as seen by the softmax warps
   float* xmax = reinterpret_cast<float*>(small + 896);  // [2 parity][kWG][128]; also the per-task sum exchange
-  static_assert(16 + 16 + 16 * C::kSlots + 3 * 24 + 8 + 16 * kTaskRing <= 480, "barrier slots");
+  static_assert(16 + 16 + 16 * C::kSlots + 3 * 24 + 8 + 16 * kTaskRing <= 400, "barrier slots");
+  static_assert(C::kSlots * 4 <= 80, "slot tags");
   static_assert(sizeof(Task) * kTaskRing <= 256, "task ring");
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
     // dynamic shared memory not aligned as expected: report and stop (uniform exit)
@@ -247,16 +259,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tq = 0, c = 0;               // tasks with tiles, ring loads
       int q_issued = 0, c_issued = 0;  // loads actually started (for the abort drain)
       bool pend = false;
-      int pv_row = 0, pv_hk = 0;
-      auto load_tile = [&](const CUtensorMap* map, int row, int hk) {
+      int pv_row = 0, pv_hk = 0, pv_hm = 3;
+      // hm = key halves to load: 3 = the whole 128-row tile, 1 or 2 = only
+      // rows 0-63 or 64-127 (placed where the full tile would put them)
+      auto load_tile = [&](const CUtensorMap* map, const CUtensorMap* hmap, int row, int hk, int hm) {
         const int slot = c % NS;
         if (c >= NS) mbar_wait(b_empty + 8 * slot, ((c / NS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         if (!*abort_flag) {
           c_issued = c + 1;
-          mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes);
+          if (HALVES) slot_hm[slot] = hm;  // published to the MMA issuer by the arrive below
+          if (hm == 3) {
+            mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes);
 #pragma unroll
-          for (int ch = 0; ch < C::kChunks; ++ch)
-            tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384, map, b_full + 8 * slot, hk * D + ch * 64, row);
+            for (int ch = 0; ch < C::kChunks; ++ch)
+              tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384, map, b_full + 8 * slot, hk * D + ch * 64, row);
+          } else {
+            const int sh = hm >> 1;
+            mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes / 2);
+#pragma unroll
+            for (int ch = 0; ch < C::kChunks; ++ch)
+              tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384 + sh * 8192, hmap, b_full + 8 * slot,
+                          hk * D + ch * 64, row + 64 * sh);
+          }
         }
         ++c;
       };
@@ -287,21 +311,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < k.n; ++j) {
           const int krow = k.k_off + tile_index(p, k, j) * kTile;
+          const int hm = HALVES ? tile_halves(p, k, j) : 3;
           // at a task boundary the previous task's last V goes first, so that
           // its last PV can run before the new task's first S
           if (j == 0 && pend) {
-            load_tile(&tmV, pv_row, pv_hk);
+            load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
             pend = false;
           }
-          load_tile(&tmK, krow, k.hk);
-          if (pend) load_tile(&tmV, pv_row, pv_hk);
+          load_tile(&tmK, &tmKh, krow, k.hk, hm);
+          if (pend) load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
           pend = true;
           pv_row = krow;
           pv_hk = k.hk;
+          pv_hm = hm;
         }
         ++tq;
       }
-      if (pend) load_tile(&tmV, pv_row, pv_hk);
+      if (pend) load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
       {
         Task end{};
         end.n = -1;  // end of this CTA's tasks
@@ -320,12 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0);
+      constexpr uint32_t idS64 = idesc_bf16_f32(128, 64, 0);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
       int g = 0, tq = 0, c = 0;  // tiles, tasks with tiles, ring slots consumed
       bool pend = false;
-      int pg = 0;
+      int pg = 0, phm = 3;
       bool pacc = false;
-      auto issue_pv = [&](int gp, bool acc) {
+      auto issue_pv = [&](int gp, bool acc, int hm) {
         const int sb = gp % 3, slot = c % NS;
         mbar_wait(b_pfull + 8 * sb, (gp / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         mbar_wait(b_full + 8 * slot, (c / NS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
@@ -333,11 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag) return;
         tc_fence_after();
         const uint32_t pcol = tmem + 128u * sb;
+        const int kk0 = (hm & 1) ? 0 : 4, kk1 = (hm & 2) ? 8 : 4;  // 16-key steps of the live halves
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk,
-                       sdesc_sw128(sKV + slot * C::kTileBytes + kk * 2048, 16384, 1024), idO,
-                       (acc || kk > 0) ? 1u : 0u);
+          if (kk >= kk0 && kk < kk1)
+            umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk,
+                         sdesc_sw128(sKV + slot * C::kTileBytes + kk * 2048, 16384, 1024), idO,
+                         (acc || kk > kk0) ? 1u : 0u);
         umma_commit(b_empty + 8 * slot);
         umma_commit(b_pvdone + 8 * sb);
       };
@@ -353,33 +382,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < k.n; ++j) {
           const int gi = g + j;
           if (j == 0 && pend) {  // previous task's last PV first (same order as the producer)
-            issue_pv(pg, pacc);
+            issue_pv(pg, pacc, phm);
             pend = false;
           }
           const int sb = gi % 3, slot = c % NS;
           mbar_wait(b_full + 8 * slot, (c / NS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+          const int hm = HALVES ? slot_hm[slot] : 3;  // written by the producer before its arrive
           if (gi >= 3) mbar_wait(b_pvdone + 8 * sb, ((gi / 3) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
           ++c;
           if (!*abort_flag) {
             tc_fence_after();
+            if (hm == 3) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              umma_bf16_ss(tmem + 128u * sb, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
-                           sdesc_sw128(sKV + slot * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                umma_bf16_ss(tmem + 128u * sb, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
+                             sdesc_sw128(sKV + slot * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+              }
+            } else {
+              // one live half: N = 64 keys, written to the score columns of that half
+              const int sh = hm >> 1;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                umma_bf16_ss(tmem + 128u * sb + 64u * sh, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
+                             sdesc_sw128(sKV + slot * C::kTileBytes + off + sh * 8192, 16, 1024), idS64, kk > 0);
+              }
             }
             umma_commit(b_sfull + 8 * sb);
             umma_commit(b_empty + 8 * slot);
           }
-          if (pend) issue_pv(pg, pacc);
+          if (pend) issue_pv(pg, pacc, phm);
           pend = true;
           pg = gi;
           pacc = j > 0;
+          phm = hm;
         }
         g += k.n;
         ++tq;
       }
-      if (pend) issue_pv(pg, pacc);
+      if (pend) issue_pv(pg, pacc, phm);
       // every MMA issued above completes before TMEM is released
       umma_commit(b_drain);
       mbar_wait_drain(b_drain, 0, kWaitTimeoutNs);
@@ -436,11 +478,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (partial) pw = __ldg(p.payload + (static_cast<long long>(k.p0 + j) * kTile + r) * 4 + wg);
         int kt = 0;
         if (MODS) kt = tile_index(p, k, j);
+        // a warp whose 32 rows see none of this warpgroup's 32 columns has
+        // nothing to exponentiate: its P is 0 (the score half may not even
+        // have been computed when the whole key half is empty)
+        const bool dead = HALVES && partial && __all_sync(0xffffffffu, pw == 0u);
         mbar_wait(b_sfull + 8 * sb, (gi / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         tc_fence_after();
         float s[kCols];
-        tmem_ld32f(lane_addr + 128u * sb + kCols * wg, s);
-        if (MODS) {
+        if (!dead) tmem_ld32f(lane_addr + 128u * sb + kCols * wg, s);
+        else {
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) s[c] = -INFINITY;
+        }
+        if (MODS && !dead) {
           // natural units: scale, softcap, ALiBi (pairs of columns in packed fp32)
           const uint64_t sc = f2_pack(p.scale, p.scale);
           float amax = 0.0f;
@@ -468,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (partial) {
+        if (partial && !dead) {
 #pragma unroll
           for (int c = 0; c < kCols; ++c)
             if (!((pw >> c) & 1u)) s[c] = -INFINITY;
@@ -512,21 +562,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial sums
         uint32_t pk[kCols / 2];
         const uint64_t negm = f2_pack(-m_use, -m_use);
+        if (dead) {
 #pragma unroll
-        for (int c = 0; c < kCols; c += 2) {
-          uint64_t x = f2_pack(s[c], s[c + 1]);
-          x = MODS ? f2_mul(f2_add(x, negm), l2e2) : f2_fma(x, sc2, negm);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          const uint64_t e = f2_pack(e0, e1);
-          switch ((c >> 1) & 3) {
-            case 0: acc0 = f2_add(acc0, e); break;
-            case 1: acc1 = f2_add(acc1, e); break;
-            case 2: acc2 = f2_add(acc2, e); break;
-            default: acc3 = f2_add(acc3, e); break;
+          for (int c = 0; c < kCols / 2; ++c) pk[c] = 0u;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kCols; c += 2) {
+            uint64_t x = f2_pack(s[c], s[c + 1]);
+            x = MODS ? f2_mul(f2_add(x, negm), l2e2) : f2_fma(x, sc2, negm);
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            const uint64_t e = f2_pack(e0, e1);
+            switch ((c >> 1) & 3) {
+              case 0: acc0 = f2_add(acc0, e); break;
+              case 1: acc1 = f2_add(acc1, e); break;
+              case 2: acc2 = f2_add(acc2, e); break;
+              default: acc3 = f2_add(acc3, e); break;
+            }
+            pk[c >> 1] = pack_bf16x2(e0, e1);
           }
-          pk[c >> 1] = pack_bf16x2(e0, e1);
         }
         float a0, a1;
         f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
@@ -636,13 +691,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view [rows, heads*D] of a bf16 tensor, box 64 x 128, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t heads, int D) {
+// 2-D view [rows, heads*D] of a bf16 tensor, box 64 columns x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t heads, int D, uint32_t box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * D), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * D * 2)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -650,15 +705,16 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t heads, int 
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool MODS>
+template <int D, bool MODS, bool HALVES>
 cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   const fa_plan* pl = a.plan;
   const Geometry& g = pl->geom;
   const int64_t rows_q = (g.layout == FA_LAYOUT_BSHD) ? int64_t(g.batch) * g.seqlen_q : g.total_q;
   const int64_t rows_k = (g.layout == FA_LAYOUT_BSHD) ? int64_t(g.batch) * g.seqlen_k : g.total_k;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mkh, mvh;
   if (!make_map(&mq, a.q, rows_q, g.heads_q, D) || !make_map(&mk, a.k, rows_k, g.heads_k, D) ||
-      !make_map(&mv, a.v, rows_k, g.heads_k, D) || !make_map(&mo, a.o, rows_q, g.heads_q, D)) {
+      !make_map(&mv, a.v, rows_k, g.heads_k, D) || !make_map(&mo, a.o, rows_q, g.heads_q, D) ||
+      !make_map(&mkh, a.k, rows_k, g.heads_k, D, 64) || !make_map(&mvh, a.v, rows_k, g.heads_k, D, 64)) {
     *why = "cuTensorMapEncodeTiled failed (pointer alignment or driver entry point)";
     return cudaErrorInvalidValue;
   }
@@ -672,6 +728,7 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   p.p_idx = pl->p_idx;
   p.f_idx = pl->f_idx;
   p.payload = pl->payload;
+  p.halves = pl->halves;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
   p.Hq = g.heads_q;
@@ -686,7 +743,7 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   p.inv_softcap = (a.softcap > 0.0f) ? 1.0f / a.softcap : 0.0f;
   if (a.flags & FA_MOD_ALIBI)
     for (int h = 0; h < g.heads_q; ++h) p.slopes[h] = a.slopes[h];
-  auto kern = k_fwd<D, MODS>;
+  auto kern = k_fwd<D, MODS, HALVES>;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -698,7 +755,7 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   }
   // persistent: one CTA per SM (shared memory keeps it to one), tasks by static stride
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(pl->tasks, sms));
-  kern<<<grid, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, mo, p);
+  kern<<<grid, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, mo, mkh, mvh, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "forward kernel launch failed";
   return e;
@@ -725,13 +782,19 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_d(const FwdLaunch& a, cudaStream_t st, const char** why) {
+  const bool mods = (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) != 0;
+  const bool halves = a.plan->mask_kind == MASK_BLOCKS;
+  if (mods) return halves ? launch_impl<D, true, true>(a, st, why) : launch_impl<D, true, false>(a, st, why);
+  return halves ? launch_impl<D, false, true>(a, st, why) : launch_impl<D, false, false>(a, st, why);
+}
+
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why) {
-  return (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) ? launch_impl<64, true>(a, st, why)
-                                                     : launch_impl<64, false>(a, st, why);
+  return launch_d<64>(a, st, why);
 }
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why) {
-  return (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) ? launch_impl<128, true>(a, st, why)
-                                                     : launch_impl<128, false>(a, st, why);
+  return launch_d<128>(a, st, why);
 }
 
 uint32_t* fwd_error_word() {

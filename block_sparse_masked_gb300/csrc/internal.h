@@ -67,6 +67,7 @@ struct fa_plan {
   int32_t* cu_seqlens_q = nullptr;  // clones (THD)
   int32_t* cu_seqlens_k = nullptr;
   int32_t* entry_row = nullptr;     // [P] planner scratch kept with the plan: flat row of each entry
+  uint8_t* halves = nullptr;        // [P] bit s: key columns 64s..64s+63 of the entry hold a visible element
 };
 
 namespace bsm {

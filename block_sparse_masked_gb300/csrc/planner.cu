@@ -423,6 +423,7 @@ struct PayloadParams {
   const int32_t* row_batch;
   const int32_t* seq;
   uint32_t* payload;
+  uint8_t* halves;  // [P] bit s: column half s of the entry has a visible element
   int rows, P;
   // intervals
   const int32_t* mask_func;
@@ -510,6 +511,13 @@ __global__ void __launch_bounds__(128) k_payload_intervals(PayloadParams p) {
   }
   uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + wi * 32 + lane;
   *dst = make_uint4(mine[0], mine[1], mine[2], mine[3]);
+  // which 64-column halves hold a visible element (OR over the 128 rows)
+  __shared__ uint32_t s_half[4];
+  const uint32_t hb = ((mine[0] | mine[1]) ? 1u : 0u) | ((mine[2] | mine[3]) ? 2u : 0u);
+  const uint32_t hw = __reduce_or_sync(kFull, hb);
+  if (lane == 0) s_half[wi] = hw;
+  __syncthreads();
+  if (threadIdx.x == 0) p.halves[e] = static_cast<uint8_t>(s_half[0] | s_half[1] | s_half[2] | s_half[3]);
 }
 
 // Block masks: one warp per partial entry.  The rows of a tile that fall in
@@ -561,8 +569,14 @@ __global__ void __launch_bounds__(128) k_payload_blocks(PayloadParams p) {
     r = seg_end;
   }
   uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + lane;
+  uint32_t hb = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
+  for (int i = 0; i < 4; ++i) {
+    dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
+    hb |= ((mine[i][0] | mine[i][1]) ? 1u : 0u) | ((mine[i][2] | mine[i][3]) ? 2u : 0u);
+  }
+  hb = __reduce_or_sync(kFull, hb);
+  if (lane == 0) p.halves[e] = static_cast<uint8_t>(hb);
 }
 
 // ------------------------------------------------------------ schedule
@@ -769,6 +783,7 @@ cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanW
   pp.row_batch = ws.row_batch;
   pp.seq = ws.seq;
   pp.payload = plan->payload;
+  pp.halves = plan->halves;
   pp.rows = rows;
   pp.P = static_cast<int>(plan->P);
   pp.mask_func = m.mask_func;

@@ -208,7 +208,8 @@ int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream,
  *   partial_idx [P], full_idx [F] (sample-local K tile indices, ascending
  *   per row), payload [P*128*4] (entry e, tile row r, word w: bit l keeps
  *   column 32*w+l), work_desc [T*4] (m_block, head, batch, q_valid_rows) in
- *   execution order.  Synchronous.
+ *   execution order, halves [P] (bit s: some element of key columns
+ *   64s..64s+63 of the partial tile is visible).  Synchronous.
  */
 typedef struct {
   int32_t* cu_q_rows;
@@ -219,6 +220,7 @@ typedef struct {
   int32_t* full_idx;
   uint32_t* payload;
   int32_t* work_desc;
+  uint8_t* halves;
 } fa_plan_host_view;
 
 int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);

@@ -15,7 +15,9 @@ Follows "Flex Attention Mask Plan Design":
 * §5 packed predicate payload, one per partial entry.  Layout of this
   library's consumer (one TMEM lane = one score row): payload[e, r, w] is a
   uint32 whose bit l is 1 iff element (row r, column 32*w + l) of the tile is
-  visible; padding and out-of-sample elements are 0.
+  visible; padding and out-of-sample elements are 0.  With it goes
+  halves[e]: bit s is 1 iff some element in columns [s*T_KV/2, (s+1)*T_KV/2)
+  of the tile is visible (the consumer skips an empty half).
 * §4.8 schedule: ``sequence_desc[B, 8]`` = (q_offset, k_offset, q_len, k_len,
   Q-plan-row begin, Q-plan-row count, K tile count, 0) and
   ``work_desc[tasks, 4]`` = (m_block, head, batch, q_valid_rows), one task per
@@ -57,6 +59,7 @@ class Plan:
     partial_idx: np.ndarray        # int64 [P]
     full_idx: np.ndarray           # int64 [F]
     payload: np.ndarray            # uint32 [P, T_Q, ceil(T_KV/32)]
+    halves: np.ndarray             # uint8 [P]: bit s = some element of column half s is visible
     sequence_desc: np.ndarray      # int64 [B, 8]
     work_desc: np.ndarray          # int64 [tasks, 4]
     visible_pairs: int             # |visible (q, k)| summed over mask heads and samples
@@ -129,7 +132,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
 
     p_cnt = np.zeros((len(heads), rows), np.int64)
     f_cnt = np.zeros((len(heads), rows), np.int64)
-    p_lists, f_lists, payloads = [], [], []
+    p_lists, f_lists, payloads, halves = [], [], [], []
     visible_pairs = 0
     for slot, hm in enumerate(heads):
         for r in range(rows):
@@ -148,6 +151,11 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
             f_lists.append(fi)
             if with_payload and pi.size:
                 payloads.append(_pack_tiles(tiles[:, pi, :]))
+            if pi.size:
+                hcut = T_KV // 2
+                lo = tiles[:, pi, :hcut].any(axis=(0, 2))
+                hi = tiles[:, pi, hcut:].any(axis=(0, 2))
+                halves.append((lo.astype(np.uint8) | (hi.astype(np.uint8) << 1)))
 
     def _csr(cnt):
         off = np.zeros(cnt.size + 1, np.int64)
@@ -158,6 +166,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
     full_idx = np.concatenate(f_lists).astype(np.int64) if f_lists else np.zeros(0, np.int64)
     nw = -(-T_KV // 32)
     payload = (np.concatenate(payloads) if payloads else np.zeros((0, T_Q, nw), np.uint32))
+    halves_arr = np.concatenate(halves) if halves else np.zeros(0, np.uint8)
 
     seq = np.zeros((B, 8), np.int64)
     for b, (q_off, q_len, k_off, k_len) in enumerate(bounds):
@@ -169,7 +178,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
         work = np.zeros((0, 4), np.int64)
     return Plan(T_Q, T_KV, len(heads), w.Hq, w.Hk, rows, cu_q_rows, k_tiles, row_batch, row_mblock,
                 row_qvalid, p_cnt, f_cnt, _csr(p_cnt), _csr(f_cnt), partial_idx, full_idx,
-                payload, seq, work, visible_pairs)
+                payload, halves_arr, seq, work, visible_pairs)
 
 
 def schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, Hq, Hk, Hmask) -> np.ndarray:
@@ -253,5 +262,6 @@ def build_plan_by_heads(w, T_Q: int = 128, T_KV: int = 128, processes: int = 8) 
                 first.row_batch, first.row_mblock, first.row_qvalid, p_cnt, f_cnt, _csr(p_cnt),
                 _csr(f_cnt), np.concatenate([q.partial_idx for q in parts]),
                 np.concatenate([q.full_idx for q in parts]),
-                np.concatenate([q.payload for q in parts]), first.sequence_desc, work,
+                np.concatenate([q.payload for q in parts]),
+                np.concatenate([q.halves for q in parts]), first.sequence_desc, work,
                 sum(q.visible_pairs for q in parts))

@@ -32,6 +32,7 @@ def compare_plan(gpu: dict, ref: OP.Plan):
     assert np.array_equal(gpu["partial_idx"], ref.partial_idx)
     assert np.array_equal(gpu["full_idx"], ref.full_idx)
     assert np.array_equal(gpu["payload"], ref.payload)
+    assert np.array_equal(gpu["halves"], ref.halves)
     assert np.array_equal(gpu["work_desc"], ref.work_desc)
 
 

@@ -146,6 +146,15 @@ def test_each_tile_exactly_one_class_and_tail_never_full():
         assert lst == sorted(lst)
 
 
+def test_halves_match_payload_columns():
+    w = _tiny_interval_workload(seed=13, B=0, S=0, nfunc=5, varlen_lens=[300, 129, 257])
+    p = P.build_plan(w, 128, 128)
+    for e in range(p.partial_idx.size):
+        words = p.payload[e]
+        want = int(np.any(words[:, :2] != 0)) | (int(np.any(words[:, 2:] != 0)) << 1)
+        assert p.halves[e] == want and want != 0
+
+
 def test_payload_bit_layout_single_element():
     """One visible element at (row 5, col 70) of a tile lands in word 2, bit 6."""
     import torch
@@ -164,6 +173,7 @@ def test_payload_bit_layout_single_element():
     want = np.zeros((128, 4), np.uint32)
     want[5, 2] = 1 << 6
     assert np.array_equal(p.payload[0], want)
+    assert p.halves.tolist() == [2]  # column 70 is in the upper half
 
 
 def test_malformed_inputs_raise():
