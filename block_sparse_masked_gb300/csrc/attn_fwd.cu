@@ -251,18 +251,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // K and V tiles share one ring, filled in the order the MMA issuer
     // consumes them: K(0), then K(g) followed by V(g-1) for every later tile
-    // (across task boundaries), and V of the last tile at the end.
-    if (lane == 0) {
+    // (across task boundaries; at a boundary the previous task's last V goes
+    // first), and V of the last tile at the end.  The whole warp walks the
+    // loop: lanes fetch tile indices 32 at a time, lane 0 issues the copies.
+    const bool leader = lane == 0;
+    if (leader) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int tq = 0, c = 0;               // tasks with tiles, ring loads
-      int q_issued = 0, c_issued = 0;  // loads actually started (for the abort drain)
-      bool pend = false;
-      int pv_row = 0, pv_hk = 0, pv_hm = 3;
-      // hm = key halves to load: 3 = the whole 128-row tile, 1 or 2 = only
-      // rows 0-63 or 64-127 (placed where the full tile would put them)
-      auto load_tile = [&](const CUtensorMap* map, const CUtensorMap* hmap, int row, int hk, int hm) {
+    }
+    int tq = 0, c = 0;               // tasks with tiles, ring loads
+    int q_issued = 0, c_issued = 0;  // loads actually started (for the abort drain)
+    bool pend = false;
+    int pv_row = 0, pv_hk = 0, pv_hm = 3;
+    // hm = key halves to load: 3 = the whole 128-row tile, 1 or 2 = only
+    // rows 0-63 or 64-127 (placed where the full tile would put them)
+    auto load_tile = [&](const CUtensorMap* map, const CUtensorMap* hmap, int row, int hk, int hm) {
+      if (leader) {
         const int slot = c % NS;
         if (c >= NS) mbar_wait(b_empty + 8 * slot, ((c / NS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         if (!*abort_flag) {
@@ -282,24 +287,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                           hk * D + ch * 64, row + 64 * sh);
           }
         }
-        ++c;
-      };
-      int ti = 0;  // task ring position
-      auto publish = [&](const Task& k) {
+      }
+      __syncwarp();
+      ++c;
+    };
+    int ti = 0;  // task ring position
+    auto publish = [&](const Task& k) {
+      if (leader) {
         const int slot = ti % kTaskRing;
         if (ti >= kTaskRing)
           mbar_wait(b_tempty + 8 * slot, ((ti / kTaskRing) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         tring[slot] = k;
         mbar_arrive(b_tfull + 8 * slot);  // release: the task is visible to the waiters
-        ++ti;
-      };
-      for (;;) {
-        const int t = atomicAdd(p.counter, 1);
-        if (t >= p.ntasks) break;
-        const Task k = load_task(p, t);
-        publish(k);
-        if (k.n == 0) continue;
-        const int qb = tq & 1;
+      }
+      __syncwarp();
+      ++ti;
+    };
+    for (;;) {
+      int t = 0;
+      if (leader) t = atomicAdd(p.counter, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t >= p.ntasks) break;
+      const Task k = load_task(p, t);
+      publish(k);
+      if (k.n == 0) continue;
+      const int qb = tq & 1;
+      if (leader) {
         if (tq >= 2) mbar_wait(b_qempty + 8 * qb, ((tq >> 1) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         if (!*abort_flag) {
           q_issued = tq + 1;
@@ -309,11 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sQ + qb * C::kTileBytes + ch * 16384, &tmQ, b_qfull + 8 * qb, k.h * D + ch * 64,
                         k.q_off + k.m_block * kTile);
         }
-        for (int j = 0; j < k.n; ++j) {
-          const int krow = k.k_off + tile_index(p, k, j) * kTile;
-          const int hm = HALVES ? tile_halves(p, k, j) : 3;
-          // at a task boundary the previous task's last V goes first, so that
-          // its last PV can run before the new task's first S
+      }
+      __syncwarp();
+      for (int j0 = 0; j0 < k.n; j0 += 32) {
+        int my_kt = 0, my_hm = 3;
+        if (j0 + lane < k.n) {
+          my_kt = tile_index(p, k, j0 + lane);
+          if (HALVES) my_hm = tile_halves(p, k, j0 + lane);
+        }
+        const int cnt = min(32, k.n - j0);
+        for (int jj = 0; jj < cnt; ++jj) {
+          const int j = j0 + jj;
+          const int krow = k.k_off + __shfl_sync(0xffffffffu, my_kt, jj) * kTile;
+          const int hm = __shfl_sync(0xffffffffu, my_hm, jj);
           if (j == 0 && pend) {
             load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
             pend = false;
@@ -325,22 +346,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           pv_hk = k.hk;
           pv_hm = hm;
         }
-        ++tq;
       }
-      if (pend) load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
-      {
-        Task end{};
-        end.n = -1;  // end of this CTA's tasks
-        publish(end);
-      }
-      if (*abort_flag) {
-        // let the copies already started land before the CTA exits (only the
-        // last load of each slot can still be in flight)
-        for (int u = (q_issued > 2 ? q_issued - 2 : 0); u < q_issued; ++u)
-          mbar_wait_drain(b_qfull + 8 * (u & 1), (u >> 1) & 1, kWaitTimeoutNs);
-        for (int u = (c_issued > NS ? c_issued - NS : 0); u < c_issued; ++u)
-          mbar_wait_drain(b_full + 8 * (u % NS), (u / NS) & 1, kWaitTimeoutNs);
-      }
+      ++tq;
+    }
+    if (pend) load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
+    {
+      Task end{};
+      end.n = -1;  // end of this CTA's tasks
+      publish(end);
+    }
+    if (leader && *abort_flag) {
+      // let the copies already started land before the CTA exits (only the
+      // last load of each slot can still be in flight)
+      for (int u = (q_issued > 2 ? q_issued - 2 : 0); u < q_issued; ++u)
+        mbar_wait_drain(b_qfull + 8 * (u & 1), (u >> 1) & 1, kWaitTimeoutNs);
+      for (int u = (c_issued > NS ? c_issued - NS : 0); u < c_issued; ++u)
+        mbar_wait_drain(b_full + 8 * (u % NS), (u / NS) & 1, kWaitTimeoutNs);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -470,14 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODS && (p.flags & FA_MOD_ALIBI)) slope = p.slopes[k.h];
       const int q_local = k.m_block * kTile + r;
       float m_run = -INFINITY, l_part = 0.0f;
+      // predicate word of this warpgroup's 32 columns, fetched one tile ahead
+      const uint32_t* pay = p.payload + static_cast<long long>(k.p0) * kTile * 4 + r * 4 + wg;
+      uint32_t pw_next = (k.np > 0) ? __ldg(pay) : 0xffffffffu;
+      int kt_next = MODS ? tile_index(p, k, 0) : 0;
       for (int j = 0; j < k.n; ++j) {
         const int gi = g + j;
         const int sb = gi % 3;
         const bool partial = j < k.np;
-        uint32_t pw = 0xffffffffu;  // predicate bits of this warpgroup's 32 columns
-        if (partial) pw = __ldg(p.payload + (static_cast<long long>(k.p0 + j) * kTile + r) * 4 + wg);
-        int kt = 0;
-        if (MODS) kt = tile_index(p, k, j);
+        const uint32_t pw = partial ? pw_next : 0xffffffffu;
+        if (j + 1 < k.np) pw_next = __ldg(pay + static_cast<long long>(j + 1) * kTile * 4);
+        const int kt = kt_next;  // key tile (for ALiBi positions), also fetched one tile ahead
+        if (MODS && j + 1 < k.n) kt_next = tile_index(p, k, j + 1);
         // a warp whose 32 rows see none of this warpgroup's 32 columns has
         // nothing to exponentiate: its P is 0 (the score half may not even
         // have been computed when the whole key half is empty)
