@@ -369,6 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0);
       constexpr uint32_t idS64 = idesc_bf16_f32(128, 64, 0);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, 1);
+      // shared-memory descriptors of Q buffer 0 and ring slot 0 (K-major for
+      // Q K^T, MN-major for P V), built once: a step inside the buffers adds
+      // its byte offset / 16 to the start-address field, which stays below
+      // 2^14 because shared memory is below 256 KB
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sKV, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sKV, 16384, 1024);
       int g = 0, tq = 0, c = 0;  // tiles, tasks with tiles, ring slots consumed
       bool pend = false;
       int pg = 0, phm = 3;
@@ -382,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t pcol = tmem + 128u * sb;
         const int kk0 = (hm & 1) ? 0 : 4, kk1 = (hm & 2) ? 8 : 4;  // 16-key steps of the live halves
+        const uint64_t dV = dV0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (kk >= kk0 && kk < kk1)
-            umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk,
-                         sdesc_sw128(sKV + slot * C::kTileBytes + kk * 2048, 16384, 1024), idO,
+            umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk, dV + static_cast<uint64_t>((kk * 2048) >> 4), idO,
                          (acc || kk > kk0) ? 1u : 0u);
         umma_commit(b_empty + 8 * slot);
         umma_commit(b_pvdone + 8 * sb);
@@ -413,21 +420,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++c;
           if (!*abort_flag) {
             tc_fence_after();
+            const uint64_t dQ = dQ0 + static_cast<uint64_t>((qb * C::kTileBytes) >> 4);
+            const uint64_t dK = dK0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
             if (hm == 3) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_bf16_ss(tmem + 128u * sb, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
-                             sdesc_sw128(sKV + slot * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+                const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                umma_bf16_ss(tmem + 128u * sb, dQ + off16, dK + off16, idS, kk > 0);
               }
             } else {
               // one live half: N = 64 keys, written to the score columns of that half
               const int sh = hm >> 1;
+              const uint64_t dKh = dK + static_cast<uint64_t>((sh * 8192) >> 4);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_bf16_ss(tmem + 128u * sb + 64u * sh, sdesc_sw128(sQ + qb * C::kTileBytes + off, 16, 1024),
-                             sdesc_sw128(sKV + slot * C::kTileBytes + off + sh * 8192, 16, 1024), idS64, kk > 0);
+                const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                umma_bf16_ss(tmem + 128u * sb + 64u * sh, dQ + off16, dKh + off16, idS64, kk > 0);
               }
             }
             umma_commit(b_sfull + 8 * sb);
