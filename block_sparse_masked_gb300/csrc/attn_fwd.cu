@@ -405,14 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(b_tempty + 8 * tslot);
         if (k.n < 0 || *abort_flag) break;
         if (k.n == 0) continue;
+        // the previous task's last PV first (the producer loads its V before
+        // this task's K tiles), and before waiting for this task's Q tile:
+        // that task's epilogue waits for it
+        if (pend) {
+          issue_pv(pg, pacc, phm);
+          pend = false;
+        }
         const int qb = tq & 1;  // (its buffer is handed back by the softmax epilogue)
         mbar_wait(b_qfull + 8 * qb, (tq >> 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         for (int j = 0; j < k.n; ++j) {
           const int gi = g + j;
-          if (j == 0 && pend) {  // previous task's last PV first (same order as the producer)
-            issue_pv(pg, pacc, phm);
-            pend = false;
-          }
           const int sb = gi % 3, slot = c % NS;
           mbar_wait(b_full + 8 * slot, (c / NS) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
           const int hm = HALVES ? slot_hm[slot] : 3;  // written by the producer before its arrive
