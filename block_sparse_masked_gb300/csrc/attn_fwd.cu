@@ -60,7 +60,7 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQStages * kTileBytes;
   static constexpr int kOffSmall = kOffKV + kSlots * kTileBytes;
-  static constexpr int kSmallBytes = 512 + 256 + 128 + 2 * 4 * 128 * 4;  // barriers, task ring, task broadcast, exchange
+  static constexpr int kSmallBytes = 512 + 256 + 128 + 2 * 2 * 128 * 4;  // barriers, task ring, task broadcast, exchange
   static constexpr int kNeed = kOffSmall + kSmallBytes;
   // dynamic shared memory normally starts 1 KB-aligned; what is left up to the
   // per-block limit is slack for a misaligned start (checked at run time)
@@ -71,7 +71,7 @@ struct Cfg {
   static_assert(kNeed <= 232448, "shared memory budget");
 };
 
-constexpr int kWG = 4;                     // softmax warpgroups, 32 score columns each
+constexpr int kWG = 2;                     // softmax warpgroups, 64 score columns each
 constexpr int kCols = 128 / kWG;
 constexpr int kSoftmaxThreads = 128 * kWG;
 constexpr int kWarpProducer = 4 * kWG, kWarpMma = 4 * kWG + 1;
@@ -502,26 +502,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODS && (p.flags & FA_MOD_ALIBI)) slope = p.slopes[k.h];
       const int q_local = k.m_block * kTile + r;
       float m_run = -INFINITY, l_part = 0.0f;
-      // predicate word of this warpgroup's 32 columns, fetched one tile ahead
-      const uint32_t* pay = p.payload + static_cast<long long>(k.p0) * kTile * 4 + r * 4 + wg;
-      uint32_t pw_next = (k.np > 0) ? __ldg(pay) : 0xffffffffu;
+      // predicate words of this warpgroup's 64 columns, fetched one tile ahead
+      const uint2* pay = reinterpret_cast<const uint2*>(p.payload + static_cast<long long>(k.p0) * kTile * 4 + r * 4) + wg;
+      uint2 pw_next = (k.np > 0) ? __ldg(pay) : make_uint2(~0u, ~0u);
       int kt_next = MODS ? tile_index(p, k, 0) : 0;
       for (int j = 0; j < k.n; ++j) {
         const int gi = g + j;
         const int sb = gi % 3;
         const bool partial = j < k.np;
-        const uint32_t pw = partial ? pw_next : 0xffffffffu;
-        if (j + 1 < k.np) pw_next = __ldg(pay + static_cast<long long>(j + 1) * kTile * 4);
+        const uint2 pw = partial ? pw_next : make_uint2(~0u, ~0u);
+        if (j + 1 < k.np) pw_next = __ldg(pay + static_cast<long long>(j + 1) * kTile * 2);
         const int kt = kt_next;  // key tile (for ALiBi positions), also fetched one tile ahead
         if (MODS && j + 1 < k.n) kt_next = tile_index(p, k, j + 1);
-        // a warp whose 32 rows see none of this warpgroup's 32 columns has
-        // nothing to exponentiate: its P is 0 (the score half may not even
-        // have been computed when the whole key half is empty)
-        const bool dead = HALVES && partial && __all_sync(0xffffffffu, pw == 0u);
+        // a warp whose 32 rows see none of this warpgroup's 64 columns (one
+        // key half) has nothing to exponentiate: its P is 0 (that score half
+        // is not even computed when the whole key half is empty)
+        const bool dead = HALVES && partial && __all_sync(0xffffffffu, (pw.x | pw.y) == 0u);
         mbar_wait(b_sfull + 8 * sb, (gi / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         tc_fence_after();
         float s[kCols];
-        if (!dead) tmem_ld32f(lane_addr + 128u * sb + kCols * wg, s);
+        if (!dead) tmem_ld64(lane_addr + 128u * sb + kCols * wg, s);
         else {
 #pragma unroll
           for (int c = 0; c < kCols; ++c) s[c] = -INFINITY;
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (partial && !dead) {
 #pragma unroll
           for (int c = 0; c < kCols; ++c)
-            if (!((pw >> c) & 1u)) s[c] = -INFINITY;
+            if (!((((c < 32) ? pw.x : pw.y) >> (c & 31)) & 1u)) s[c] = -INFINITY;
         }
         // row max of this quarter (four independent chains), then of the row
         float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(b_qempty + 8 * pend_qb);
           store_pending = false;
         }
-        const float mrow = fmaxf(fmaxf(xm[r], xm[128 + r]), fmaxf(xm[256 + r], xm[384 + r]));
+        const float mrow = fmaxf(xm[r], xm[128 + r]);
         // Running max in the exponent's units (scaled log2 units without mods).
         // The reference max only moves when the tile max exceeds it by more
         // than kRescaleLog2 (a factor 256): exp values stay <= 256, and O
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
         l_part = l_part * alpha + (a0 + a1);
         // P (bf16 pairs) of this quarter's keys into the score buffer's first 64 columns
-        tmem_st16(lane_addr + 128u * sb + (kCols / 2) * wg, pk);
+        tmem_st32(lane_addr + 128u * sb + (kCols / 2) * wg, pk);
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
           // O holds PV(g-1): wait for it before rescaling
           mbar_wait(b_pvdone + 8 * ((gi - 1) % 3), ((gi - 1) / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* xs = xmax + (g & 1) * (kWG * 128);
       xs[wg * 128 + r] = l_part;
       group_sync();
-      const float l = (xs[r] + xs[128 + r]) + (xs[256 + r] + xs[384 + r]);
+      const float l = xs[r] + xs[128 + r];
       const bool have = l > 0.0f;
       const float inv_l = have ? 1.0f / l : 0.0f;
       // A full 128-row tile is staged in its task's Q buffer (no S MMA reads it
