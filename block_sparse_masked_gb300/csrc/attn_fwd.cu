@@ -56,7 +56,7 @@ struct Cfg {
   static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
   static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile, bf16
   static constexpr int kQStages = 2;
-  static constexpr int kSlots = (D == 128) ? 4 : 8;  // one ring of K and V tiles
+  static constexpr int kSlots = (D == 128) ? 5 : 12;  // one ring of K and V tiles
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kQStages * kTileBytes;
   static constexpr int kOffSmall = kOffKV + kSlots * kTileBytes;
