@@ -94,7 +94,8 @@ struct FwdParams {
   int flags;
   float scale;       // multiplies Q K^T
   float scale_log2;  // scale * log2(e)
-  float softcap, inv_softcap;
+  float y_scale;     // scale / softcap: argument of tanh per unit of Q K^T
+  float cap_log2;    // softcap * log2(e)
   float slopes[kMaxHeads];
 };
 
@@ -136,22 +137,9 @@ __device__ __forceinline__ int tile_halves(const FwdParams& p, const Task& k, in
   return (j < k.np) ? static_cast<int>(__ldg(p.halves + k.p0 + j)) : 3;
 }
 
-// cap * tanh(x / cap) for |x / cap| < 0.5: Maclaurin series of tanh through
-// y^13 (truncation error below 1e-6 relative at |y| = 0.5, far less below).
-__device__ __forceinline__ float softcap_series(float x, float cap, float inv_cap) {
-  const float y = x * inv_cap;
-  const float y2 = y * y;
-  float s = 21844.0f / 6081075.0f;
-  s = fmaf(s, y2, -1382.0f / 155925.0f);
-  s = fmaf(s, y2, 62.0f / 2835.0f);
-  s = fmaf(s, y2, -17.0f / 315.0f);
-  s = fmaf(s, y2, 2.0f / 15.0f);
-  s = fmaf(s, y2, -1.0f / 3.0f);
-  return cap * fmaf(s * y2, y, y);
-}
-// Two columns of softcap_series at once in packed fp32.
-__device__ __forceinline__ void softcap_series2(float& x0, float& x1, float cap, float inv_cap) {
-  const uint64_t y = f2_mul(f2_pack(x0, x1), f2_pack(inv_cap, inv_cap));
+// tanh(y) for |y| < 0.5 on a pair of columns in packed fp32: Maclaurin
+// series through y^13 (truncation error below 1e-6 relative at |y| = 0.5).
+__device__ __forceinline__ uint64_t tanh_series13(uint64_t y) {
   const uint64_t y2 = f2_mul(y, y);
   uint64_t s = f2_pack(21844.0f / 6081075.0f, 21844.0f / 6081075.0f);
   s = f2_fma(s, y2, f2_pack(-1382.0f / 155925.0f, -1382.0f / 155925.0f));
@@ -159,13 +147,19 @@ __device__ __forceinline__ void softcap_series2(float& x0, float& x1, float cap,
   s = f2_fma(s, y2, f2_pack(-17.0f / 315.0f, -17.0f / 315.0f));
   s = f2_fma(s, y2, f2_pack(2.0f / 15.0f, 2.0f / 15.0f));
   s = f2_fma(s, y2, f2_pack(-1.0f / 3.0f, -1.0f / 3.0f));
-  const uint64_t t = f2_fma(f2_mul(s, y2), y, y);
-  f2_unpack(f2_mul(t, f2_pack(cap, cap)), x0, x1);
+  return f2_fma(f2_mul(s, y2), y, y);
 }
-// cap * tanh(x / cap) for any x, from tanh(y) = 1 - 2 / (exp(2y) + 1).
-__device__ __forceinline__ float softcap_exp(float x, float cap, float inv_cap) {
-  const float e = ex2_approx(2.0f * kLog2e * (x * inv_cap));
-  return cap * (1.0f - __fdividef(2.0f, e + 1.0f));
+// tanh(y) for |y| < 0.125, pair of columns: the same series through y^5
+// (the first omitted term, 17 y^7 / 315, is below 3e-7 of y there).
+__device__ __forceinline__ uint64_t tanh_series5(uint64_t y) {
+  const uint64_t y2 = f2_mul(y, y);
+  const uint64_t q = f2_fma(y2, f2_pack(2.0f / 15.0f, 2.0f / 15.0f), f2_pack(-1.0f / 3.0f, -1.0f / 3.0f));
+  return f2_fma(f2_mul(y, y2), q, y);
+}
+// tanh(y) for any y, from tanh(y) = 1 - 2 / (exp(2y) + 1).
+__device__ __forceinline__ float tanh_exp(float y) {
+  const float e = ex2_approx(2.0f * kLog2e * y);
+  return 1.0f - __fdividef(2.0f, e + 1.0f);
 }
 
 // HALVES: the plan may hold partial tiles with an empty 64-key half (block
@@ -465,7 +459,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     constexpr int OC = D / kWG;              // output columns of this warpgroup
     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-    const uint64_t l2e2 = f2_pack(kLog2e, kLog2e);
     // Thread 0 takes each task from the ring (and turns a timeout into the
     // end marker) and broadcasts it through shared memory, so that every
     // softmax warp runs the same loops and reaches the same named barriers.
@@ -498,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int qb = tq & 1;
-      float slope = 0.0f;
-      if (MODS && (p.flags & FA_MOD_ALIBI)) slope = p.slopes[k.h];
+      float slope2 = 0.0f;  // ALiBi slope in log2 units
+      if (MODS && (p.flags & FA_MOD_ALIBI)) slope2 = p.slopes[k.h] * kLog2e;
       const int q_local = k.m_block * kTile + r;
       float m_run = -INFINITY, l_part = 0.0f;
       // predicate words of this warpgroup's 64 columns, fetched one tile ahead
@@ -527,26 +520,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kCols; ++c) s[c] = -INFINITY;
         }
         if (MODS && !dead) {
-          // natural units: scale, softcap, ALiBi (pairs of columns in packed fp32)
-          const uint64_t sc = f2_pack(p.scale, p.scale);
-          float amax = 0.0f;
-#pragma unroll
-          for (int c = 0; c < kCols; c += 2) {
-            f2_unpack(f2_mul(f2_pack(s[c], s[c + 1]), sc), s[c], s[c + 1]);
-            amax = max3f(amax, fabsf(s[c]), fabsf(s[c + 1]));
-          }
+          // scores in log2 units, log2(e) * (softcap(scale * s) + slope * (k - q)),
+          // pairs of columns in packed fp32; the tanh series is chosen per warp
+          // from the largest |y| = |scale * s / softcap| it holds
           if (p.flags & FA_MOD_SOFTCAP) {
-            if (__any_sync(0xffffffffu, amax >= 0.5f * p.softcap)) {
+            float amax = 0.0f;
 #pragma unroll
-              for (int c = 0; c < kCols; ++c) s[c] = softcap_exp(s[c], p.softcap, p.inv_softcap);
+            for (int c = 0; c < kCols; c += 2) amax = max3f(amax, fabsf(s[c]), fabsf(s[c + 1]));
+            const float ya = amax * p.y_scale;
+            const uint64_t ys = f2_pack(p.y_scale, p.y_scale), cl = f2_pack(p.cap_log2, p.cap_log2);
+            if (__any_sync(0xffffffffu, ya >= 0.5f)) {
+#pragma unroll
+              for (int c = 0; c < kCols; ++c) s[c] = p.cap_log2 * tanh_exp(s[c] * p.y_scale);
+            } else if (__any_sync(0xffffffffu, ya >= 0.125f)) {
+#pragma unroll
+              for (int c = 0; c < kCols; c += 2)
+                f2_unpack(f2_mul(tanh_series13(f2_mul(f2_pack(s[c], s[c + 1]), ys)), cl), s[c], s[c + 1]);
             } else {
 #pragma unroll
-              for (int c = 0; c < kCols; c += 2) softcap_series2(s[c], s[c + 1], p.softcap, p.inv_softcap);
+              for (int c = 0; c < kCols; c += 2)
+                f2_unpack(f2_mul(tanh_series5(f2_mul(f2_pack(s[c], s[c + 1]), ys)), cl), s[c], s[c + 1]);
             }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kCols; c += 2) f2_unpack(f2_mul(f2_pack(s[c], s[c + 1]), sc2), s[c], s[c + 1]);
           }
           if (p.flags & FA_MOD_ALIBI) {
             const float fd0 = static_cast<float>(kt * kTile + wg * kCols - q_local);  // k - q at column 0
-            const uint64_t sl = f2_pack(slope, slope);
+            const uint64_t sl = f2_pack(slope2, slope2);
 #pragma unroll
             for (int c = 0; c < kCols; c += 2) {
               const uint64_t kq = f2_pack(fd0 + static_cast<float>(c), fd0 + static_cast<float>(c + 1));
@@ -581,17 +582,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_pending = false;
         }
         const float mrow = fmaxf(xm[r], xm[128 + r]);
-        // Running max in the exponent's units (scaled log2 units without mods).
-        // The reference max only moves when the tile max exceeds it by more
-        // than kRescaleLog2 (a factor 256): exp values stay <= 256, and O
-        // and l are rescaled (after PV(g-1) completes) only when it moves.
+        // Running max in log2 units of the exponent (with mods the scores are
+        // already in them; without, the scale is applied to the max and inside
+        // the exponential).  The reference max only moves when the tile max
+        // exceeds it by more than kRescaleLog2 (a factor 256): exp values stay
+        // <= 256, and O and l are rescaled (after PV(g-1) completes) only when
+        // it moves.
         const float m_tile = MODS ? mrow : mrow * p.scale_log2;
-        const float th = MODS ? kRescaleLog2 * kLn2 : kRescaleLog2;
         float alpha = 1.0f;
         if (j == 0) {
           m_run = m_tile;
-        } else if (m_tile > m_run + th) {
-          alpha = MODS ? ex2_approx((m_run - m_tile) * kLog2e) : ex2_approx(m_run - m_tile);
+        } else if (m_tile > m_run + kRescaleLog2) {
+          alpha = ex2_approx(m_run - m_tile);
           m_run = m_tile;
         }
         const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
@@ -605,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCols; c += 2) {
             uint64_t x = f2_pack(s[c], s[c + 1]);
-            x = MODS ? f2_mul(f2_add(x, negm), l2e2) : f2_fma(x, sc2, negm);
+            x = MODS ? f2_add(x, negm) : f2_fma(x, sc2, negm);
             float x0, x1;
             f2_unpack(x, x0, x1);
             const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
@@ -696,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (wg == 0 && row_ok && p.lse != nullptr) {
         float lse = -INFINITY;
-        if (have) lse = MODS ? (m_run + __logf(l)) : (m_run + __log2f(l)) * kLn2;
+        if (have) lse = (m_run + __log2f(l)) * kLn2;
         p.lse[static_cast<long long>(k.h) * p.total_q + grow] = lse;
       }
       ++tq;
@@ -775,8 +777,8 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   p.flags = a.flags;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
-  p.softcap = a.softcap;
-  p.inv_softcap = (a.softcap > 0.0f) ? 1.0f / a.softcap : 0.0f;
+  p.y_scale = (a.softcap > 0.0f) ? a.scale / a.softcap : 0.0f;
+  p.cap_log2 = a.softcap * kLog2e;
   if (a.flags & FA_MOD_ALIBI)
     for (int h = 0; h < g.heads_q; ++h) p.slopes[h] = a.slopes[h];
   auto kern = k_fwd<D, MODS, HALVES>;
