@@ -82,6 +82,12 @@ def _random_problem(seed, B, S, H, d, nfunc, Hk=None, Hmask=1, lens=None, softca
     dict(seed=6, B=1, S=384, H=2, nfunc=3, softcap=5.0),
     dict(seed=7, B=1, S=384, H=2, nfunc=3, alibi=True),
     dict(seed=8, B=2, S=333, H=2, nfunc=1, softcap=50.0, alibi=True),
+    # the softcap's tanh is evaluated three ways, chosen per warp from the
+    # largest |scale * s / softcap| it holds: below 0.125, below 0.5, above;
+    # unit-variance scores put softcap 50 in the first, 12 in the second and
+    # 2 in the third
+    dict(seed=13, B=1, S=384, H=2, nfunc=3, softcap=12.0),
+    dict(seed=14, B=1, S=384, H=2, nfunc=3, softcap=2.0, alibi=True),
 ])
 def test_random_small_all_rows(d, case):
     w = _random_problem(d=d, **case)
