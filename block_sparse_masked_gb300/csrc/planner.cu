@@ -601,7 +601,7 @@ __device__ __forceinline__ int task_bucket(const SchedParams& p, int cost) {
 }
 
 // One CTA builds the whole schedule with bounded counting:
-//  1. histogram of (section, cost bucket) over every task;
+//  1. histogram of (section, cost bucket) over every task, one warp per section;
 //  2. offsets: positive-cost tasks of section s start after every positive
 //     task of sections < s, ordered by bucket (cost descending); zero-cost
 //     tasks follow every positive task, sections in order;
@@ -615,11 +615,13 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   const long long nb = static_cast<long long>(p.NS) * (C + 1);
   for (long long i = threadIdx.x; i < nb; i += blockDim.x) p.hist[i] = 0;
   __syncthreads();
-  for (int sct = 0; sct < p.NS; ++sct) {
+  // one warp per section (the sections are many and small: one per sample
+  // and K/V head, a few dozen tasks each)
+  for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
     const int b = sct / p.Hk, hk = sct % p.Hk;
     const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5];
     const int n = group * nrows;
-    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+    for (int t = threadIdx.x & 31; t < n; t += 32) {
       const int h = hk * group + t / nrows, m = t % nrows;
       atomicAdd(&p.hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, h, begin + m))], 1);
     }
