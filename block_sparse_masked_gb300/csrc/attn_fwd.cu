@@ -828,10 +828,21 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t st, const char** why) {
   return halves ? launch_impl<D, false, true>(a, st, why) : launch_impl<D, false, false>(a, st, why);
 }
 
+// Interval-mask plans without score mods run two Q tiles per task
+// (attn_fwd_pair.cu): neighbouring Q tiles see mostly the same K tiles, and
+// the shared K/V stream halves the bytes each SM loads per score.  With score
+// mods the softmax (tanh series, ALiBi) is the bound, and the kernel here,
+// with two warpgroups per tile, runs it faster; block-mask plans also stay
+// here, with empty 64-key halves skipped.
+static bool use_pair(const FwdLaunch& a) {
+  return a.plan->mask_kind == MASK_INTERVALS && (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) == 0;
+}
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why) {
+  if (use_pair(a)) return launch_fwd_pair_d64(a, st, why);
   return launch_d<64>(a, st, why);
 }
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why) {
+  if (use_pair(a)) return launch_fwd_pair_d128(a, st, why);
   return launch_d<128>(a, st, why);
 }
 

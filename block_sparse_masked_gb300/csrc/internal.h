@@ -131,6 +131,9 @@ struct FwdLaunch {
 };
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why);
+// two Q tiles per task sharing one K/V stream (attn_fwd_pair.cu; interval masks)
+cudaError_t launch_fwd_pair_d64(const FwdLaunch& a, cudaStream_t st, const char** why);
+cudaError_t launch_fwd_pair_d128(const FwdLaunch& a, cudaStream_t st, const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
 
