@@ -63,10 +63,17 @@ def load_peaks():
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "ptx.cuh", "internal.h"):
+    for f in ("attn_fwd.cu", "attn_fwd_pair.cu", "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "block_sparse_masked_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def fwd_kernel_name(w) -> str:
+    """The forward kernel the library launches for this workload."""
+    if w.mask_kind == "intervals" and not (w.softcap and w.softcap > 0) and w.alibi_slopes is None:
+        return "k_fwd_pair (attention forward, two Q tiles per task)"
+    return "k_fwd (attention forward, one Q tile per task)"
 
 
 def known_traffic(workload: str):
@@ -358,7 +365,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": fwd_tflops / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone per event pair)",
-                     "kernel": "k_fwd (attention forward)"},
+                     "kernel": fwd_kernel_name(w)},
         "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "clocks": clk,
