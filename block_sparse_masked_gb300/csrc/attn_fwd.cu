@@ -820,12 +820,15 @@ cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Interval masks without score mods run in attn_fwd_pair.cu (see use_pair
+// below), so every plan that reaches this kernel either has score mods or is
+// a block-mask plan.
 template <int D>
 cudaError_t launch_d(const FwdLaunch& a, cudaStream_t st, const char** why) {
   const bool mods = (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) != 0;
   const bool halves = a.plan->mask_kind == MASK_BLOCKS;
   if (mods) return halves ? launch_impl<D, true, true>(a, st, why) : launch_impl<D, true, false>(a, st, why);
-  return halves ? launch_impl<D, false, true>(a, st, why) : launch_impl<D, false, false>(a, st, why);
+  return launch_impl<D, false, true>(a, st, why);
 }
 
 // Interval-mask plans without score mods run two Q tiles per task

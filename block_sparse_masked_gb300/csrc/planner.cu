@@ -604,7 +604,8 @@ __device__ __forceinline__ int task_bucket(const SchedParams& p, int cost) {
 //  1. histogram of (section, cost bucket) over every task, one warp per section;
 //  2. offsets: positive-cost tasks of section s start after every positive
 //     task of sections < s, ordered by bucket (cost descending); zero-cost
-//     tasks follow every positive task, sections in order;
+//     tasks follow every positive task, sections in order (section totals
+//     and bucket cursors one warp per section, starts by a block scan);
 //  3. scatter: one warp per section walks its tasks in tie order (head in the
 //     section's group, then m_block), 32 at a time; lanes with the same
 //     bucket take consecutive slots in lane order, so the sort is stable.
@@ -627,23 +628,28 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     }
   }
   __syncthreads();
+  const int lane = threadIdx.x & 31;
+  // 2a. positive-cost tasks per section (one warp per section, lanes over
+  //     buckets); kept in the section's bucket-0 cursor until 2b
+  for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
+    const int32_t* h = p.hist + static_cast<long long>(sct) * (C + 1);
+    long long tot = 0;
+    for (int c = lane; c < C; c += 32) tot += h[c];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
+    if (lane == 0) p.cursors[static_cast<long long>(sct) * (C + 1)] = static_cast<int32_t>(tot);
+  }
+  __syncthreads();
+  // 2b. section starts: positive tasks of section s after those of sections
+  //     < s; zero-cost tasks after every positive task, sections in order
   __shared__ long long s_tot_pos;
   long long carry_pos = 0;
   for (int base = 0; base < p.NS; base += 1024) {
     const int sct = base + threadIdx.x;
-    long long pos = 0;
-    if (sct < p.NS)
-      for (int c = 0; c < C; ++c) pos += p.hist[static_cast<long long>(sct) * (C + 1) + c];
+    const long long pos = (sct < p.NS) ? p.cursors[static_cast<long long>(sct) * (C + 1)] : 0;
     long long tot;
     const long long start = carry_pos + block_excl_scan(pos, &tot);
-    if (sct < p.NS) {
-      long long run = start;
-      for (int c = 0; c < C; ++c) {
-        const long long i = static_cast<long long>(sct) * (C + 1) + c;
-        p.cursors[i] = static_cast<int32_t>(run);
-        run += p.hist[i];
-      }
-    }
+    if (sct < p.NS) p.cursors[static_cast<long long>(sct) * (C + 1)] = static_cast<int32_t>(start);
     carry_pos += tot;
   }
   if (threadIdx.x == 0) s_tot_pos = carry_pos;
@@ -658,7 +664,26 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     carry_zero += tot;
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
+  // 2c. bucket cursors inside each section: its start plus an exclusive scan
+  //     of its bucket counts (one warp per section, 32 buckets at a time)
+  for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
+    const int32_t* h = p.hist + static_cast<long long>(sct) * (C + 1);
+    int32_t* cur = p.cursors + static_cast<long long>(sct) * (C + 1);
+    long long run = cur[0];
+    __syncwarp();
+    for (int c0 = 0; c0 < C; c0 += 32) {
+      const int c = c0 + lane;
+      const long long v = (c < C) ? h[c] : 0;
+      long long x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c < C) cur[c] = static_cast<int32_t>(run + x - v);
+      run += __shfl_sync(kFull, x, 31);
+    }
+  }
   for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
     const int b = sct / p.Hk, hk = sct % p.Hk;
     const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5], q_len = p.seq[8 * b + 2];
