@@ -267,7 +267,7 @@ def main():
     info = fa.fa_plan_info_get(plan, count_visible=True)
     plan.free()
     flops_step = visible_flops(info, w.Hq, w.d)
-    launches_per_step = 8 + (1 if info["header"][1] > 0 else 0) + 1  # planner kernels + forward
+    launches_per_step = 3 + 1  # planner (front, schedule, back) + forward
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
     def step(ev=None):

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "internal.h"
 
@@ -93,14 +94,76 @@ struct Carver {
   }
 };
 
+// Host memory the front stage writes the header into: 8 values, then the
+// build's ticket, published last.  One per host thread: a thread waits for
+// its header before it starts another build.
 long long* pinned_header() {
   thread_local long long* h = nullptr;
   if (!h) {
     void* p = nullptr;
-    if (cudaMallocHost(&p, 8 * sizeof(long long)) != cudaSuccess) return nullptr;
+    if (cudaMallocHost(&p, 16 * sizeof(long long)) != cudaSuccess) return nullptr;
     h = static_cast<long long*>(p);
+    for (int i = 0; i < 16; ++i) h[i] = 0;
   }
   return h;
+}
+
+// Event recorded after the front launch, per host thread and device: the
+// header wait polls it to notice a failed launch.
+cudaEvent_t front_event(int dev) {
+  thread_local cudaEvent_t ev[128] = {};
+  if (dev < 0 || dev >= 128) return nullptr;
+  if (!ev[dev] && cudaEventCreateWithFlags(&ev[dev], cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  return ev[dev];
+}
+
+// Control words of the front stage (two device words, zero at launch and
+// left at zero by it): a per-device free list hands each in-flight build
+// its own pair.  New pairs are zeroed in stream order before their first use.
+std::mutex g_ctl_mu;
+std::vector<unsigned*> g_ctl_free[128];
+
+unsigned* ctl_take(int dev, cudaStream_t st) {
+  if (dev < 0 || dev >= 128) return nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ctl_mu);
+    if (!g_ctl_free[dev].empty()) {
+      unsigned* p = g_ctl_free[dev].back();
+      g_ctl_free[dev].pop_back();
+      return p;
+    }
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, 256) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemsetAsync(p, 0, 8, st) != cudaSuccess) {
+    cudaFree(p);
+    return nullptr;
+  }
+  return static_cast<unsigned*>(p);
+}
+
+void ctl_give(int dev, unsigned* p) {
+  std::lock_guard<std::mutex> lk(g_ctl_mu);
+  g_ctl_free[dev].push_back(p);
+}
+
+// Waits until the front stage has published `ticket`, polling host memory;
+// every 64 polls the event after the launch is checked, so that a failed
+// launch or a kernel that ended without publishing returns an error.
+cudaError_t wait_header(long long* hh, long long ticket, cudaEvent_t ev) {
+  for (unsigned spin = 1;; ++spin) {
+    if (__atomic_load_n(hh + 8, __ATOMIC_ACQUIRE) == ticket) return cudaSuccess;
+    if ((spin & 63) == 0) {
+      const cudaError_t q = cudaEventQuery(ev);
+      if (q == cudaErrorNotReady) continue;
+      if (q != cudaSuccess) return q;
+      if (__atomic_load_n(hh + 8, __ATOMIC_ACQUIRE) == ticket) return cudaSuccess;
+      return cudaErrorUnknown;
+    }
+  }
 }
 
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -180,28 +243,30 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   // because the geometry stage clamps every sample length to max_seqlen_q.
   const long long rows_ub_ll = static_cast<long long>(B) * nq_max;
   if (rows_ub_ll > (1LL << 26)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles");
+  if (rows_ub_ll * margs.Hmask >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles x mask heads");
   const int rows_ub = static_cast<int>(rows_ub_ll);
   const int words = std::max(1, cdiv(kt_ub, 32));
   const int Hmask = margs.Hmask;
 
   bsm::PlanWorkspace ws{};
   ws.rows_ub = rows_ub;
+  ws.nq_max = nq_max;
   ws.kt_ub = kt_ub;
   ws.words = words;
   const long long nflat_ub = static_cast<long long>(Hmask) * rows_ub;
   const int NS = B * g.heads_k;  // schedule sections
   const int C = kt_ub;           // largest task cost
   Carver c1;
-  const size_t o_err = c1.take(4), o_hdr = c1.take(64), o_cur = c1.take(4ull * (B + 1)),
+  const size_t o_hdr = c1.take(64), o_cur = c1.take(4ull * (B + 1)),
                o_seq = c1.take(32ull * B), o_rb = c1.take(4ull * rows_ub),
                o_vis = c1.take(4ull * nflat_ub * words), o_full = c1.take(4ull * nflat_ub * words),
                o_pc = c1.take(4ull * nflat_ub), o_fc = c1.take(4ull * nflat_ub),
                o_po = c1.take(4ull * (nflat_ub + 1)), o_fo = c1.take(4ull * (nflat_ub + 1)),
-               o_hist = c1.take(4ull * NS * (C + 1)), o_cursor = c1.take(4ull * NS * (C + 1));
+               o_hist = c1.take(4ull * NS * (C + 1)), o_cursor = c1.take(4ull * NS * (C + 1)),
+               o_work = c1.take(16ull * rows_ub * g.heads_q);
   Alloc al{allocator, dev, st};
   uint8_t* w1 = static_cast<uint8_t*>(al.get(c1.off));
   if (!w1) return fail(FA_ERR_ALLOC, "workspace allocation of %zu bytes failed", c1.off);
-  ws.err = reinterpret_cast<uint32_t*>(w1 + o_err);
   ws.header = reinterpret_cast<long long*>(w1 + o_hdr);
   ws.cu_rows = reinterpret_cast<int32_t*>(w1 + o_cur);
   ws.seq = reinterpret_cast<int32_t*>(w1 + o_seq);
@@ -214,21 +279,30 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   ws.f_off = reinterpret_cast<int32_t*>(w1 + o_fo);
   ws.hist = reinterpret_cast<int32_t*>(w1 + o_hist);
   ws.cursors = reinterpret_cast<int32_t*>(w1 + o_cursor);
+  ws.work = reinterpret_cast<int32_t*>(w1 + o_work);
 
   auto bail = [&](int code) {
     al.put(w1, c1.off);
     return code;
   };
 
-  // the geometry kernel zeroes the error word before anything sets it
-  cudaError_t e = bsm::launch_geometry(g, gi->cu_seqlens_q, gi->cu_seqlens_k, ws, st);
-  if (!e) e = bsm::launch_classify(g, margs, ws, st);
-  if (!e) e = bsm::launch_scan_header(g, Hmask, ws, st);
   long long* hh = pinned_header();
   if (!hh) return bail(fail(FA_ERR_ALLOC, "pinned header buffer"));
-  if (!e) e = cudaMemcpyAsync(hh, ws.header, 64, cudaMemcpyDeviceToHost, st);
-  if (!e) e = cudaStreamSynchronize(st);  // the one host/device synchronisation of a build
-  if (e) return bail(cuda_fail(e, "planner (classify/scan/header)"));
+  cudaEvent_t ev = front_event(dev);
+  if (!ev) return bail(fail(FA_ERR_CUDA, "event creation failed"));
+  ws.ctl = ctl_take(dev, st);
+  if (!ws.ctl) return bail(fail(FA_ERR_ALLOC, "planner control words"));
+  thread_local long long t_ticket = 0;
+  const long long ticket = ++t_ticket;
+  // front stage, then the schedule, which the GPU runs while this thread
+  // waits for the header, sizes the plan and allocates it
+  cudaError_t e = bsm::launch_front(g, margs, ws, gi->cu_seqlens_q, gi->cu_seqlens_k, hh, ticket, st);
+  if (!e) e = cudaEventRecord(ev, st);
+  if (!e) e = bsm::launch_schedule(g, ws, Hmask, NS, C, st);
+  if (!e) e = wait_header(hh, ticket, ev);  // the one host/device synchronisation of a build
+  // after a failure the control words are not known to be zero: they are not reused
+  if (e) return bail(cuda_fail(e, "planner (front stage/header)"));
+  ctl_give(dev, ws.ctl);
   long long hdr[8];
   std::memcpy(hdr, hh, sizeof(hdr));
   const uint32_t err = static_cast<uint32_t>(hdr[7]);
@@ -287,13 +361,12 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   plan->entry_row = reinterpret_cast<int32_t*>(pm + q_er);
   plan->halves = pm + q_hv;
 
-  // exact-size copies, CSR lists, payloads (two launches), schedule (one launch)
-  e = bsm::launch_materialize(g, margs, ws, plan, gi->cu_seqlens_q, gi->cu_seqlens_k, st);
-  if (!e) e = bsm::launch_schedule(g, plan, ws.hist, ws.cursors, NS, C, st);
+  // exact-size copies (the schedule included), CSR lists, payloads: one launch
+  e = bsm::launch_back(g, margs, ws, plan, gi->cu_seqlens_q, gi->cu_seqlens_k, st);
   if (e) {
     free_plan_mem(plan, st);
     delete plan;
-    return bail(cuda_fail(e, "planner (materialize/payload/schedule)"));
+    return bail(cuda_fail(e, "planner (back stage)"));
   }
   al.put(w1, c1.off);
   plan->build_us =

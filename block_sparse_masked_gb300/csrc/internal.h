@@ -73,21 +73,24 @@ struct fa_plan {
 namespace bsm {
 
 // ---- planner launchers (planner.cu) -------------------------------------
+// Padded rows: rows_ub = batch * nq_max (nq_max = Q tiles of the longest
+// sample); padded row (b, lr) is b * nq_max + lr.
 struct PlanWorkspace {
-  uint32_t* err;
+  unsigned* ctl;          // front stage control words [2]: zero before and after its launch
   long long* header;      // 8 values
   int32_t* cu_rows;       // [B+1]
   int32_t* seq;           // [B*8]
   int32_t* row_batch;     // [rows_ub]
-  uint32_t* vis_bits;     // [Hmask*rows_ub*words]
+  uint32_t* vis_bits;     // [Hmask*rows_ub*words], padded rows
   uint32_t* full_bits;
-  int32_t* p_cnt;         // [Hmask*rows_ub]
+  int32_t* p_cnt;         // [Hmask*rows_ub], padded rows
   int32_t* f_cnt;
-  int32_t* p_off;         // [Hmask*rows_ub+1]
+  int32_t* p_off;         // [Hmask*rows+1], compact rows
   int32_t* f_off;
   int32_t* hist;          // schedule counting buffers [num_sections*(max_cost+1)]
   int32_t* cursors;
-  int rows_ub, kt_ub, words;
+  int32_t* work;          // schedule output [rows_ub*heads_q*4]
+  int rows_ub, nq_max, kt_ub, words;
 };
 
 struct MaskArgs {
@@ -99,20 +102,20 @@ struct MaskArgs {
   int Hmask;
 };
 
-cudaError_t launch_geometry(const Geometry& g, const int32_t* cu_q, const int32_t* cu_k,
-                            const PlanWorkspace& ws, cudaStream_t st);
-cudaError_t launch_classify(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
-                            cudaStream_t st);
-cudaError_t launch_scan_header(const Geometry& g, int Hmask, const PlanWorkspace& ws,
-                               cudaStream_t st);
-// After the header: exact-size copies into the plan, CSR lists, the
-// entry->row map, payloads (one launch each for CSR+copies and payload) and
-// the schedule (one launch).
-cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
-                               fa_plan* plan, const int32_t* cu_q_src, const int32_t* cu_k_src,
-                               cudaStream_t st);
-cudaError_t launch_schedule(const Geometry& g, fa_plan* plan, int32_t* hist, int32_t* cursors,
-                            int num_sections, int max_cost, cudaStream_t st);
+// Front stage (one launch): classification, then in its last CTA the
+// sample descriptors, row prefixes, count scans and the header, which also
+// goes to host_header[0..7] followed by host_header[8] = ticket when
+// host_header is not null.  ws.ctl must be zero at launch (it is again after).
+cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
+                         const int32_t* cu_q, const int32_t* cu_k, long long* host_header,
+                         long long ticket, cudaStream_t st);
+// Task order into ws.work; needs only the front stage's outputs.
+cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmask, int num_sections,
+                            int max_cost, cudaStream_t st);
+// Back stage (one launch), once the plan is allocated from the header:
+// exact-size copies into the plan, CSR lists, the entry->row map, payloads.
+cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws, fa_plan* plan,
+                        const int32_t* cu_q_src, const int32_t* cu_k_src, cudaStream_t st);
 cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, cudaStream_t st);
 
 // ---- forward (attn_fwd*.cu) ---------------------------------------------

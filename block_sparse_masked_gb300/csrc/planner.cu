@@ -1,17 +1,25 @@
-// planner.cu -- GPU mask planner: mask -> MaskPlan.
+// planner.cu -- GPU mask planner: mask -> MaskPlan, in three launches.
 //
 // Stages follow "Flex Attention Mask Plan Design" (cuDNN frontend docs):
-//   k_geometry         §4.2 compact row prefixes + §3.2 prefix validation,
-//                      sequence descriptors of §4.8
-//   k_classify_*       §4.3 Q2K classification into visible/full bitsets and
-//                      per-row partial/full counts; endpoints validated and
-//                      clamped (§3.3); block masks use the logical-block
-//                      expansion E(M) of "Decoupling Logical Masks from GPU
-//                      Execution for Dynamic Block-Sparse Attention" §2
-//   k_scan_header      §4.5 exclusive scans and the 8-value allocation header
-//   k_materialize      §4.6 independent partial / full CSR index lists
-//   k_payload          §5 packed predicate payload, bit-packed with warp ballots
-//   k_sched_*          §4.8 forward task order by bounded counting
+//   k_front_*   one CTA per (mask head, sample, Q tile row of the sample):
+//               §4.3 Q2K classification into visible/full bitsets and
+//               per-row partial/full counts, endpoints validated and clamped
+//               (§3.3); block masks use the logical-block expansion E(M) of
+//               "Decoupling Logical Masks from GPU Execution for Dynamic
+//               Block-Sparse Attention" §2.  The last CTA to finish builds
+//               the §4.2 compact row prefixes with the §3.2 prefix
+//               validation and the §4.8 sequence descriptors, runs the §4.5
+//               exclusive scans and writes the 8-value allocation header,
+//               also straight into host memory for the one host read-back.
+//   k_schedule  §4.8 forward task order by bounded counting (runs while the
+//               host reads the header and allocates the plan).
+//   k_back_*    one CTA per (Q tile row, mask head): exact-size copies into
+//               the plan, §4.6 partial / full CSR index lists and the §5
+//               packed predicate payload of the row's partial tiles.
+// Every GPU launch costs a few microseconds of device time on its own, so
+// the stages are fused into as few launches as their data dependences
+// allow: the counts must be scanned before anything is sized, and the plan
+// can only be written once the host has sized and allocated it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -35,10 +43,11 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int w) {
   return static_cast<uint32_t>(m);
 }
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+// Block-wide exclusive scan of one value per thread (blockDim.x a multiple
+// of 32, at most 1024); *total receives the block's sum.
 __device__ __forceinline__ long long block_excl_scan(long long v, long long* total) {
   __shared__ long long s_warp[32];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -48,7 +57,7 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long* tot
   if (lane == 31) s_warp[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    long long s = s_warp[lane];
+    long long s = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       long long y = __shfl_up_sync(kFull, s, o);
@@ -58,127 +67,89 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long* tot
   }
   __syncthreads();
   const long long warp_prefix = wid ? s_warp[wid - 1] : 0;
-  *total = s_warp[31];
+  *total = s_warp[nw - 1];
   __syncthreads();
   return warp_prefix + x - v;
 }
 
-// ------------------------------------------------------------ geometry
-struct GeoParams {
-  int layout, B, Sq, Sk, total_q, total_k;
+// ------------------------------------------------------------ front
+struct FrontParams {
+  int layout, B, Sq, Sk, total_q, total_k, nq_max;
   const int32_t* cu_q;
   const int32_t* cu_k;
-  int32_t* cu_rows;
-  int32_t* seq;
-  int32_t* row_batch;
-  uint32_t* err;
-  int rows_ub;
-};
-
-__global__ void __launch_bounds__(1024) k_geometry(GeoParams g) {
-  if (threadIdx.x == 0) *g.err = 0;  // the build's error word starts here
-  __syncthreads();
-  long long carry = 0;
-  for (int base = 0; base < g.B; base += 1024) {
-    const int b = base + threadIdx.x;
-    int q_off = 0, k_off = 0, q_len = 0, k_len = 0;
-    if (b < g.B) {
-      if (g.layout == FA_LAYOUT_BSHD) {
-        q_off = b * g.Sq;
-        k_off = b * g.Sk;
-        q_len = g.Sq;
-        k_len = g.Sk;
-      } else {
-        const int a = g.cu_q[b], e = g.cu_q[b + 1];
-        const int c = g.cu_k[b], f = g.cu_k[b + 1];
-        bool bad = false;
-        if (b == 0 && (a != 0 || c != 0)) bad = true;
-        if (b == g.B - 1 && (e != g.total_q || f != g.total_k)) bad = true;
-        if (e < a || f < c) bad = true;
-        if (e - a > g.Sq || f - c > g.Sk) bad = true;
-        if (a < 0 || c < 0 || e > g.total_q || f > g.total_k) bad = true;
-        if (bad) atomicOr(g.err, PLANERR_SEQLENS);
-        // clamp so that later stages index safely before the error is read
-        q_off = min(max(a, 0), g.total_q);
-        k_off = min(max(c, 0), g.total_k);
-        q_len = min(max(e - a, 0), min(g.Sq, g.total_q - q_off));
-        k_len = min(max(f - c, 0), min(g.Sk, g.total_k - k_off));
-      }
-    }
-    const int nrows = (b < g.B) ? cdiv(q_len, kTile) : 0;
-    long long tot;
-    const long long begin = carry + block_excl_scan(nrows, &tot);
-    if (b < g.B) {
-      int32_t* s = g.seq + 8 * b;
-      s[0] = q_off;
-      s[1] = k_off;
-      s[2] = q_len;
-      s[3] = k_len;
-      s[4] = static_cast<int32_t>(begin);
-      s[5] = nrows;
-      s[6] = cdiv(k_len, kTile);
-      s[7] = 0;
-      g.cu_rows[b] = static_cast<int32_t>(begin);
-    }
-    carry += tot;
-  }
-  if (threadIdx.x == 0) g.cu_rows[g.B] = static_cast<int32_t>(carry);
-  __syncthreads();
-  for (int b = threadIdx.x; b < g.B; b += 1024) {
-    const int begin = g.seq[8 * b + 4], n = g.seq[8 * b + 5];
-    for (int r = 0; r < n && begin + r < g.rows_ub; ++r) g.row_batch[begin + r] = b;
-  }
-}
-
-// ------------------------------------------------------------ classify
-struct ClassifyParams {
-  const int32_t* seq;
-  const int32_t* row_batch;
-  const int32_t* cu_rows;
-  int B;
   // intervals
   const int32_t* mask_func;
-  int nfunc, total_q;
+  int nfunc;
   // blocks
   const uint8_t* block_mask;
   int block_q, block_kv, nbq, nbk;
-  // outputs
-  uint32_t* vis_bits;
+  int Hmask;
+  // per padded row (mask head, sample, Q tile row of the sample): flat index
+  // hm * rows_ub + b * nq_max + lr
+  uint32_t* vis_bits;  // [Hmask*rows_ub*words]
   uint32_t* full_bits;
-  int32_t* p_cnt;
+  int32_t* p_cnt;      // [Hmask*rows_ub]
   int32_t* f_cnt;
-  uint32_t* err;
   int rows_ub, words;
+  // written by the last CTA
+  int32_t* cu_rows;    // [B+1]
+  int32_t* seq;        // [B*8]
+  int32_t* row_batch;  // [rows]
+  int32_t* p_off;      // [Hmask*rows+1], compact order (hm, row)
+  int32_t* f_off;
+  long long* header;   // device, 8 values
+  long long* host_header;  // host memory, 8 values then the ticket; may be null
+  long long ticket;
+  unsigned* ctl;       // [0] CTAs arrived, [1] error bits; zero at launch, zero again at exit
 };
 
-// One CTA per (Q plan row, mask head); thread t owns Q row t of the tile.
-// Per row, each K tile is "touched" if a non-empty interval intersects it and
+struct SampleGeo {
+  int q_off, k_off, q_len, k_len;
+  bool bad;
+};
+
+// Sample b's offsets and lengths.  THD prefixes are validated (§3.2) and
+// clamped, so that every stage indexes safely before the host reads the
+// error bits.
+__device__ __forceinline__ SampleGeo sample_geo(const FrontParams& p, int b) {
+  SampleGeo s{};
+  if (p.layout == FA_LAYOUT_BSHD) {
+    s.q_off = b * p.Sq;
+    s.k_off = b * p.Sk;
+    s.q_len = p.Sq;
+    s.k_len = p.Sk;
+    s.bad = false;
+    return s;
+  }
+  const int a = __ldg(p.cu_q + b), e = __ldg(p.cu_q + b + 1);
+  const int c = __ldg(p.cu_k + b), f = __ldg(p.cu_k + b + 1);
+  bool bad = false;
+  if (b == 0 && (a != 0 || c != 0)) bad = true;
+  if (b == p.B - 1 && (e != p.total_q || f != p.total_k)) bad = true;
+  if (e < a || f < c) bad = true;
+  if (e - a > p.Sq || f - c > p.Sk) bad = true;
+  if (a < 0 || c < 0 || e > p.total_q || f > p.total_k) bad = true;
+  s.q_off = min(max(a, 0), p.total_q);
+  s.k_off = min(max(c, 0), p.total_k);
+  s.q_len = min(max(e - a, 0), min(p.Sq, p.total_q - s.q_off));
+  s.k_len = min(max(f - c, 0), min(p.Sk, p.total_k - s.k_off));
+  s.bad = bad;
+  return s;
+}
+
+// Interval masks, 128 threads: thread t owns Q row t of the tile.  Per row,
+// each K tile is "touched" if a non-empty interval intersects it and
 // "covered" if one maximal run of merged intervals contains the whole tile;
 // visible = OR over valid rows of touched, full = AND over all 128 rows of
 // covered (rows past the sample's q_len cover nothing, so a Q tail is never full).
-__global__ void __launch_bounds__(128) k_classify_intervals(ClassifyParams p) {
-  const int row = blockIdx.x, hm = blockIdx.y, t = threadIdx.x;
-  const int lane = t & 31, wid = t >> 5;
-  const long long ws_row = static_cast<long long>(hm) * p.rows_ub + row;
+__device__ __forceinline__ void classify_intervals(const FrontParams& p, const SampleGeo& sg,
+                                                   int lr, int hm, long long ws_row) {
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   __shared__ uint32_t s_v[4], s_f[4];
-  const int rows_total = p.cu_rows[p.B];
-  if (row >= rows_total) {
-    for (int w = t; w < p.words; w += 128) {
-      p.vis_bits[ws_row * p.words + w] = 0;
-      p.full_bits[ws_row * p.words + w] = 0;
-    }
-    if (t == 0) {
-      p.p_cnt[ws_row] = 0;
-      p.f_cnt[ws_row] = 0;
-    }
-    return;
-  }
-  const int b = p.row_batch[row];
-  const int32_t* s = p.seq + 8 * b;
-  const int q_off = s[0], q_len = s[2], k_len = s[3], row_begin = s[4];
-  const int q_local = (row - row_begin) * kTile + t;
-  const bool valid = q_local < q_len;
-  const int32_t* F = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off + q_local;
+  const int q_local = lr * kTile + t;
+  const int k_len = sg.k_len;
+  const bool valid = q_local < sg.q_len;
+  const int32_t* F = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + sg.q_off + q_local;
   const long long fstride = p.total_q;
 
   // validation: 0 <= F0 <= ... <= F(n-1) <= k_len
@@ -190,7 +161,7 @@ __global__ void __launch_bounds__(128) k_classify_intervals(ClassifyParams p) {
       if (e < prev || e > k_len) bad = true;  // e < 0 is caught by e < prev (prev starts at 0)
       prev = max(prev, e);
     }
-    if (bad) atomicOr(p.err, PLANERR_MASK);
+    if (bad) atomicOr(&p.ctl[1], PLANERR_MASK);
   }
 
   int pc = 0, fc = 0;
@@ -241,29 +212,26 @@ __global__ void __launch_bounds__(128) k_classify_intervals(ClassifyParams p) {
   }
 }
 
-// Block masks (fixed length): thread per K tile.  Tile (i, j) touches the
-// logical blocks [r0, r1] x [c0, c1] that overlap its in-bounds part; it is
-// visible if any is active and full if all are and the tile has no Q/K tail.
-// Words are bit-packed with warp ballots.
-__global__ void __launch_bounds__(256) k_classify_blocks(ClassifyParams p) {
-  const int row = blockIdx.x, hm = blockIdx.y, t = threadIdx.x;
-  const int lane = t & 31;
-  const long long ws_row = static_cast<long long>(hm) * p.rows_ub + row;
+// Block masks (fixed length), 256 threads: thread per K tile.  Tile (i, j)
+// touches the logical blocks [r0, r1] x [c0, c1] that overlap its in-bounds
+// part; it is visible if any is active and full if all are and the tile has
+// no Q/K tail.  Words are bit-packed with warp ballots.
+__device__ __forceinline__ void classify_blocks(const FrontParams& p, const SampleGeo& sg, int lr,
+                                                int hm, long long ws_row) {
+  const int t = threadIdx.x, lane = t & 31;
   __shared__ int s_pc, s_fc;
   if (t == 0) {
     s_pc = 0;
     s_fc = 0;
   }
   __syncthreads();
-  const int b = p.row_batch[row];
-  const int32_t* s = p.seq + 8 * b;
-  const int q_len = s[2], k_len = s[3], row_begin = s[4], nk = s[6];
-  const int q0 = (row - row_begin) * kTile, q1 = min(q0 + kTile, q_len);
+  const int q_len = sg.q_len, k_len = sg.k_len, nk = cdiv(k_len, kTile);
+  const int q0 = lr * kTile, q1 = min(q0 + kTile, q_len);
   const bool qtail = (q1 - q0) < kTile;
   const int r0 = q0 / p.block_q, r1 = (q1 - 1) / p.block_q;
   const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
   const int nwords_used = p.words * 32;
-  for (int j0 = 0; j0 < nwords_used; j0 += 256) {
+  for (int j0 = 0; j0 < nwords_used; j0 += blockDim.x) {
     const int j = j0 + t;
     bool vis = false, full = false;
     if (j < nk) {
@@ -299,36 +267,89 @@ __global__ void __launch_bounds__(256) k_classify_blocks(ClassifyParams p) {
   }
 }
 
-// ------------------------------------------------------------ scan + header
-struct ScanParams {
-  const int32_t* p_cnt;
-  const int32_t* f_cnt;
-  const int32_t* cu_rows;
-  int32_t* p_off;
-  int32_t* f_off;
-  long long* header;
-  const uint32_t* err;
-  int B, Hmask, rows_ub;
-};
+// Work of the last CTA of the front launch: sample descriptors, compact row
+// prefixes and the row -> sample map; exclusive scans of the per-row counts
+// in compact (mask head, row) order; the header; reset of the control words.
+constexpr int kScanItems = 8;
 
-__global__ void __launch_bounds__(1024) k_scan_header(ScanParams p) {
-  const int rows = p.cu_rows[p.B];
+__device__ void front_finish(const FrontParams& p) {
+  const int nt = blockDim.x;
+  long long carry = 0;
+  uint32_t err_local = 0;
+  for (int base = 0; base < p.B; base += nt) {
+    const int b = base + threadIdx.x;
+    SampleGeo sg{};
+    int nrows = 0;
+    if (b < p.B) {
+      sg = sample_geo(p, b);
+      nrows = cdiv(sg.q_len, kTile);
+      if (sg.bad) err_local |= PLANERR_SEQLENS;
+    }
+    long long tot;
+    const long long begin = carry + block_excl_scan(nrows, &tot);
+    if (b < p.B) {
+      int32_t* s = p.seq + 8 * b;
+      s[0] = sg.q_off;
+      s[1] = sg.k_off;
+      s[2] = sg.q_len;
+      s[3] = sg.k_len;
+      s[4] = static_cast<int32_t>(begin);
+      s[5] = nrows;
+      s[6] = cdiv(sg.k_len, kTile);
+      s[7] = 0;
+      p.cu_rows[b] = static_cast<int32_t>(begin);
+    }
+    carry += tot;
+  }
+  if (err_local) atomicOr(&p.ctl[1], err_local);
+  const int rows = static_cast<int>(carry);
+  if (threadIdx.x == 0) p.cu_rows[p.B] = rows;
+  __syncthreads();
+  // row -> sample: the last sample whose first row is <= r (a sample without
+  // rows shares its start with the next one, so it is never chosen)
+  for (int r = threadIdx.x; r < rows; r += nt) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.cu_rows[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    p.row_batch[r] = lo;
+  }
+  __syncthreads();
   const long long n = static_cast<long long>(p.Hmask) * rows;
   long long cp = 0, cf = 0;
-  for (long long base = 0; base < n; base += 1024) {
-    const long long i = base + threadIdx.x;
-    int vp = 0, vf = 0;
-    if (i < n) {
-      const long long hm = i / rows, r = i % rows;
-      vp = p.p_cnt[hm * p.rows_ub + r];
-      vf = p.f_cnt[hm * p.rows_ub + r];
+  for (long long base = 0; base < n; base += static_cast<long long>(nt) * kScanItems) {
+    const long long i0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
+    int vp[kScanItems], vf[kScanItems];
+    long long sp = 0, sf = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+      const long long i = i0 + k;
+      vp[k] = 0;
+      vf[k] = 0;
+      if (i < n) {
+        const int hm = static_cast<int>(i / rows), r = static_cast<int>(i % rows);
+        const int b = p.row_batch[r];
+        const long long ws_row = static_cast<long long>(hm) * p.rows_ub +
+                                 static_cast<long long>(b) * p.nq_max + (r - p.cu_rows[b]);
+        vp[k] = __ldcg(p.p_cnt + ws_row);
+        vf[k] = __ldcg(p.f_cnt + ws_row);
+      }
+      sp += vp[k];
+      sf += vf[k];
     }
     long long tp, tf;
-    const long long ep = block_excl_scan(vp, &tp);
-    const long long ef = block_excl_scan(vf, &tf);
-    if (i < n) {
-      p.p_off[i] = static_cast<int32_t>(cp + ep);
-      p.f_off[i] = static_cast<int32_t>(cf + ef);
+    long long ep = cp + block_excl_scan(sp, &tp);
+    long long ef = cf + block_excl_scan(sf, &tf);
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+      const long long i = i0 + k;
+      if (i < n) {
+        p.p_off[i] = static_cast<int32_t>(ep);
+        p.f_off[i] = static_cast<int32_t>(ef);
+      }
+      ep += vp[k];
+      ef += vf[k];
     }
     cp += tp;
     cf += tf;
@@ -336,95 +357,72 @@ __global__ void __launch_bounds__(1024) k_scan_header(ScanParams p) {
   if (threadIdx.x == 0) {
     p.p_off[n] = static_cast<int32_t>(cp);
     p.f_off[n] = static_cast<int32_t>(cf);
-    uint32_t e = *p.err;
+    uint32_t e = atomicExch(&p.ctl[1], 0u);  // read and reset the error bits
     if (cp > 0x3fffffffLL || cf > 0x3fffffffLL) e |= PLANERR_OVERFLOW;
-    p.header[0] = rows;
-    p.header[1] = cp;
-    p.header[2] = cf;
-    p.header[3] = 0;
-    p.header[4] = 0;
-    p.header[5] = 0;
-    p.header[6] = 0;
-    p.header[7] = e;
+    const long long h[8] = {rows, cp, cf, 0, 0, 0, 0, static_cast<long long>(e)};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) p.header[k] = h[k];
+    p.ctl[0] = 0u;  // every CTA has arrived: the control words are free again
+    if (p.host_header) {
+      volatile long long* hh = p.host_header;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) hh[k] = h[k];
+      __threadfence_system();
+      hh[8] = p.ticket;  // published last: the host reads the values after seeing it
+    }
   }
 }
 
-// ------------------------------------------------------------ materialize
-struct MatParams {
+// One CTA per padded row: blockIdx.x = b * nq_max + lr (rows past a sample's
+// end, and x >= rows_ub, only arrive), blockIdx.y = mask head.  The last CTA
+// to arrive (atomic count after a device-wide fence) finishes the stage.
+template <int KIND>
+__global__ void __launch_bounds__(KIND == MASK_INTERVALS ? 128 : 256) k_front(FrontParams p) {
+  const int x = blockIdx.x, hm = blockIdx.y;
+  if (x < p.rows_ub) {
+    const int b = x / p.nq_max, lr = x % p.nq_max;
+    const SampleGeo sg = sample_geo(p, b);
+    if (lr < cdiv(sg.q_len, kTile)) {
+      const long long ws_row = static_cast<long long>(hm) * p.rows_ub + x;
+      if (KIND == MASK_INTERVALS)
+        classify_intervals(p, sg, lr, hm, ws_row);
+      else
+        classify_blocks(p, sg, lr, hm, ws_row);
+    }
+  }
+  __shared__ unsigned s_last;
+  __threadfence();  // every thread's outputs are visible device-wide before the CTA arrives
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned total = gridDim.x * gridDim.y;
+    s_last = (atomicAdd(&p.ctl[0], 1u) == total - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  front_finish(p);
+}
+
+// ------------------------------------------------------------ back
+struct BackParams {
+  // exact-size copies from the workspace (and the caller's cu_seqlens)
+  const int32_t* src[7];
+  int32_t* dst[7];
+  long long count[7];
+  // workspace
   const uint32_t* vis_bits;
   const uint32_t* full_bits;
-  const int32_t* p_off;  // workspace offsets, exact [Hmask*rows+1] layout
+  const int32_t* p_off;  // compact [Hmask*rows+1]
   const int32_t* f_off;
+  const int32_t* row_batch;
+  const int32_t* seq;
+  // plan
   int32_t* p_idx;
   int32_t* f_idx;
   int32_t* entry_row;  // [P]: flat (hm*rows + row) of each partial entry
-  int rows, rows_ub, words;
-  // exact-size copies into the plan, done by the same launch
-  const int32_t* src[6];
-  int32_t* dst[6];
-  long long count[6];
-};
-
-// One warp per (row, mask head): lane w handles bitset word w; ranks come
-// from a warp scan of popcounts, so indices come out ascending.
-__global__ void __launch_bounds__(32) k_materialize(MatParams p) {
-  {
-    const long long tid = (static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x) * 32 + threadIdx.x;
-    const long long nthreads = static_cast<long long>(gridDim.x) * gridDim.y * 32;
-#pragma unroll
-    for (int a = 0; a < 6; ++a)
-      for (long long i = tid; i < p.count[a]; i += nthreads) p.dst[a][i] = p.src[a][i];
-  }
-  const int row = blockIdx.x, hm = blockIdx.y, lane = threadIdx.x;
-  if (row >= p.rows) return;
-  const long long flat = static_cast<long long>(hm) * p.rows + row;
-  const long long ws_row = static_cast<long long>(hm) * p.rows_ub + row;
-  int pbase = p.p_off[flat], fbase = p.f_off[flat];
-  for (int w0 = 0; w0 < p.words; w0 += 32) {
-    const int w = w0 + lane;
-    uint32_t vb = 0, fb = 0;
-    if (w < p.words) {
-      vb = p.vis_bits[ws_row * p.words + w];
-      fb = p.full_bits[ws_row * p.words + w];
-    }
-    uint32_t pb = vb & ~fb;
-    const int np = __popc(pb), nf = __popc(fb);
-    int xp = np, xf = nf;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int yp = __shfl_up_sync(kFull, xp, o), yf = __shfl_up_sync(kFull, xf, o);
-      if (lane >= o) {
-        xp += yp;
-        xf += yf;
-      }
-    }
-    int pp = pbase + xp - np, pf = fbase + xf - nf;
-    while (pb) {
-      const int bit = __ffs(pb) - 1;
-      pb &= pb - 1;
-      p.p_idx[pp] = w * 32 + bit;
-      p.entry_row[pp] = static_cast<int32_t>(flat);
-      ++pp;
-    }
-    while (fb) {
-      const int bit = __ffs(fb) - 1;
-      fb &= fb - 1;
-      p.f_idx[pf++] = w * 32 + bit;
-    }
-    pbase += __shfl_sync(kFull, xp, 31);
-    fbase += __shfl_sync(kFull, xf, 31);
-  }
-}
-
-// ------------------------------------------------------------ payload
-struct PayloadParams {
-  const int32_t* entry_row;
-  const int32_t* p_idx;
-  const int32_t* row_batch;
-  const int32_t* seq;
-  uint32_t* payload;
-  uint8_t* halves;  // [P] bit s: column half s of the entry has a visible element
-  int rows, P;
+  uint32_t* payload;   // [P*128*4]
+  uint8_t* halves;     // [P] bit s: column half s of the entry has a visible element
+  int rows, rows_ub, nq_max, words;
   // intervals
   const int32_t* mask_func;
   int nfunc, total_q;
@@ -433,109 +431,60 @@ struct PayloadParams {
   int block_q, block_kv, nbq, nbk;
 };
 
-template <int KIND>
-__device__ __forceinline__ bool visible_at(const PayloadParams& p, int hm, int q_off, int q_local,
-                                           int col) {
-  if (KIND == MASK_INTERVALS) {
-    const int32_t* F = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off + q_local;
-    const long long fs = p.total_q;
-    bool in = col < __ldg(F);
-    for (int i = 1; i + 1 < p.nfunc; i += 2)
-      in |= (col >= __ldg(F + i * fs)) && (col < __ldg(F + (i + 1) * fs));
-    return in;
-  } else {
-    const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
-    return __ldg(M + static_cast<long long>(q_local / p.block_q) * p.nbk + col / p.block_kv) != 0;
+// Endpoints of the CTA's 128 Q rows kept in shared memory for the payload
+// when a row has at most this many.
+constexpr int kSmemFuncs = 16;
+
+// OR the columns [lo, hi) of tile columns [c0, c0 + 128) into w[0..3]
+// (bit l of word wd = column c0 + 32 wd + l).
+__device__ __forceinline__ void add_columns(uint32_t (&w)[kPayloadWords], int c0, int lo, int hi) {
+  lo = max(lo, c0);
+  hi = min(hi, c0 + kTile);
+#pragma unroll
+  for (int wd = 0; wd < kPayloadWords; ++wd) {
+    const int base = c0 + 32 * wd;
+    const int L = max(lo, base), H = min(hi, base + 32);
+    if (L < H) w[wd] |= static_cast<uint32_t>(((uint64_t(1) << (H - L)) - 1) << (L - base));
   }
 }
 
-// Interval masks: one CTA (4 warps) per partial entry; warp wi packs rows
-// 32*wi .. 32*wi+31.  For each row the 32 lanes test 32 consecutive columns
-// and a ballot forms one uint32 word; lane i keeps the 4 words of row i and
-// the warp stores 32 rows x 16 bytes contiguously.  With at most kMaxFuncFast
-// endpoints per row, lane i loads row i's endpoints once and the warp
-// broadcasts them with shuffles; otherwise every lane reads them per row.
-constexpr int kMaxFuncFast = 9;
-
-template <bool FAST>
-__global__ void __launch_bounds__(128) k_payload_intervals(PayloadParams p) {
-  const long long e = blockIdx.x;
-  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-  const int flat = p.entry_row[e];
-  const int hm = flat / p.rows, row = flat % p.rows;
-  const int j = p.p_idx[e];
-  const int b = p.row_batch[row];
-  const int32_t* s = p.seq + 8 * b;
-  const int q_off = s[0], q_len = s[2], k_len = s[3], row_begin = s[4];
-  const int q0 = (row - row_begin) * kTile;
-  const int c0 = j * kTile;
-  const int32_t* Fbase = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off;
-  const long long fs = p.total_q;
-  int myF[kMaxFuncFast];
-  if (FAST) {
-    const int q_mine = q0 + wi * 32 + lane;
-#pragma unroll
-    for (int f = 0; f < kMaxFuncFast; ++f)
-      myF[f] = (f < p.nfunc && q_mine < q_len) ? __ldg(Fbase + f * fs + q_mine) : 0;
-  }
-  uint32_t mine[kPayloadWords] = {0, 0, 0, 0};
-  for (int i = 0; i < 32; ++i) {
-    const int q_local = q0 + wi * 32 + i;
-    if (q_local >= q_len) break;  // uniform: rows past the sample stay 0
-    bool in[kPayloadWords];
-    if (FAST) {
-      int F[kMaxFuncFast];
-#pragma unroll
-      for (int f = 0; f < kMaxFuncFast; ++f) F[f] = __shfl_sync(kFull, myF[f], i);
-#pragma unroll
-      for (int wd = 0; wd < kPayloadWords; ++wd) {
-        const int col = c0 + wd * 32 + lane;
-        bool v = col < F[0];
-#pragma unroll
-        for (int f = 1; f + 1 < kMaxFuncFast; f += 2)
-          if (f + 1 < p.nfunc) v |= (col >= F[f]) && (col < F[f + 1]);
-        in[wd] = v && (col < k_len);
-      }
-    } else {
-#pragma unroll
-      for (int wd = 0; wd < kPayloadWords; ++wd) {
-        const int col = c0 + wd * 32 + lane;
-        in[wd] = (col < k_len) && visible_at<MASK_INTERVALS>(p, hm, q_off, q_local, col);
-      }
-    }
-#pragma unroll
-    for (int wd = 0; wd < kPayloadWords; ++wd) {
-      const uint32_t word = __ballot_sync(kFull, in[wd]);
-      if (lane == i) mine[wd] = word;
-    }
-  }
-  uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + wi * 32 + lane;
-  *dst = make_uint4(mine[0], mine[1], mine[2], mine[3]);
-  // which 64-column halves hold a visible element (OR over the 128 rows)
-  __shared__ uint32_t s_half[4];
-  const uint32_t hb = ((mine[0] | mine[1]) ? 1u : 0u) | ((mine[2] | mine[3]) ? 2u : 0u);
-  const uint32_t hw = __reduce_or_sync(kFull, hb);
-  if (lane == 0) s_half[wi] = hw;
-  __syncthreads();
-  if (threadIdx.x == 0) p.halves[e] = static_cast<uint8_t>(s_half[0] | s_half[1] | s_half[2] | s_half[3]);
-}
-
-// Block masks: one warp per partial entry.  The rows of a tile that fall in
-// the same logical block row have identical predicate words, so the warp
-// walks the tile's row segments (one per logical block row, clipped to the
-// sample) and forms each segment's 4 words with 4 ballots over the columns;
-// lane l then stores rows l, l+32, l+64, l+96 (16 bytes each, coalesced).
-__global__ void __launch_bounds__(128) k_payload_blocks(PayloadParams p) {
-  const long long e = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+// Interval payload of one partial entry (tile column j), one warp: lane l
+// forms the 4 words of rows l, l+32, l+64, l+96 from the row's intervals
+// [0, F0), [F1, F2), ... clipped to the tile and to k_len; rows past the
+// sample stay 0.  Returns the OR of the column-half bits over the rows.
+__device__ __forceinline__ uint32_t payload_intervals_entry(const BackParams& p, long long e, int j,
+                                                            int q_len, int k_len, int q0, int hm,
+                                                            int q_off, const int32_t (*sF)[kTile],
+                                                            bool smem) {
   const int lane = threadIdx.x & 31;
-  if (e >= p.P) return;
-  const int flat = p.entry_row[e];
-  const int hm = flat / p.rows, row = flat % p.rows;
-  const int j = p.p_idx[e];
-  const int b = p.row_batch[row];
-  const int32_t* s = p.seq + 8 * b;
-  const int q_len = s[2], k_len = s[3], row_begin = s[4];
-  const int q0 = (row - row_begin) * kTile;
+  const int c0 = j * kTile;
+  const int32_t* Fg = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off;
+  uint32_t hb = 0;
+  uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = lane + 32 * i;
+    uint32_t w[kPayloadWords] = {0, 0, 0, 0};
+    if (q0 + t < q_len) {
+      auto F = [&](int f) { return smem ? sF[f][t] : __ldg(Fg + static_cast<long long>(f) * p.total_q + q0 + t); };
+      add_columns(w, c0, 0, min(F(0), k_len));
+      for (int f = 1; f + 1 < p.nfunc; f += 2) add_columns(w, c0, F(f), min(F(f + 1), k_len));
+    }
+    dst[t] = make_uint4(w[0], w[1], w[2], w[3]);
+    hb |= ((w[0] | w[1]) ? 1u : 0u) | ((w[2] | w[3]) ? 2u : 0u);
+  }
+  return hb;
+}
+
+// Block payload of one partial entry, one warp.  The rows of a tile that
+// fall in the same logical block row have identical predicate words, so the
+// warp walks the tile's row segments (one per logical block row, clipped to
+// the sample) and forms each segment's 4 words with 4 ballots over the
+// columns; lane l then stores rows l, l+32, l+64, l+96 (16 bytes each,
+// coalesced).
+__device__ __forceinline__ uint32_t payload_blocks_entry(const BackParams& p, long long e, int j,
+                                                         int q_len, int k_len, int q0, int hm) {
+  const int lane = threadIdx.x & 31;
   const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
   int cb[kPayloadWords];
   bool cin[kPayloadWords];
@@ -575,23 +524,109 @@ __global__ void __launch_bounds__(128) k_payload_blocks(PayloadParams p) {
     dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
     hb |= ((mine[i][0] | mine[i][1]) ? 1u : 0u) | ((mine[i][2] | mine[i][3]) ? 2u : 0u);
   }
-  hb = __reduce_or_sync(kFull, hb);
-  if (lane == 0) p.halves[e] = static_cast<uint8_t>(hb);
+  return hb;
+}
+
+// One CTA (4 warps) per (Q plan row, mask head).  All CTAs share the
+// exact-size copies.  Warp 0 turns the row's bitsets into its CSR entries
+// (lane w handles bitset word w; ranks come from a warp scan of popcounts,
+// so indices come out ascending); then the 4 warps take the row's partial
+// entries in turn and write their payloads.
+template <int KIND>
+__global__ void __launch_bounds__(128) k_back(BackParams p) {
+  {
+    const long long tid = (static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * gridDim.y * blockDim.x;
+#pragma unroll
+    for (int a = 0; a < 7; ++a)
+      for (long long i = tid; i < p.count[a]; i += nthreads) p.dst[a][i] = __ldg(p.src[a] + i);
+  }
+  const int row = blockIdx.x, hm = blockIdx.y;
+  if (row >= p.rows) return;
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int b = __ldg(p.row_batch + row);
+  const int32_t* s = p.seq + 8 * b;
+  const int q_off = __ldg(s + 0), q_len = __ldg(s + 2), k_len = __ldg(s + 3), row_begin = __ldg(s + 4);
+  const int lr = row - row_begin;
+  const long long flat = static_cast<long long>(hm) * p.rows + row;
+  const long long ws_row = static_cast<long long>(hm) * p.rows_ub + static_cast<long long>(b) * p.nq_max + lr;
+  const int pstart = __ldg(p.p_off + flat), np = __ldg(p.p_off + flat + 1) - pstart;
+  if (wi == 0) {
+    int pbase = pstart, fbase = __ldg(p.f_off + flat);
+    for (int w0 = 0; w0 < p.words; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t vb = 0, fb = 0;
+      if (w < p.words) {
+        vb = __ldg(p.vis_bits + ws_row * p.words + w);
+        fb = __ldg(p.full_bits + ws_row * p.words + w);
+      }
+      uint32_t pb = vb & ~fb;
+      const int npw = __popc(pb), nfw = __popc(fb);
+      int xp = npw, xf = nfw;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yp = __shfl_up_sync(kFull, xp, o), yf = __shfl_up_sync(kFull, xf, o);
+        if (lane >= o) {
+          xp += yp;
+          xf += yf;
+        }
+      }
+      int pp = pbase + xp - npw, pf = fbase + xf - nfw;
+      while (pb) {
+        const int bit = __ffs(pb) - 1;
+        pb &= pb - 1;
+        p.p_idx[pp] = w * 32 + bit;
+        p.entry_row[pp] = static_cast<int32_t>(flat);
+        ++pp;
+      }
+      while (fb) {
+        const int bit = __ffs(fb) - 1;
+        fb &= fb - 1;
+        p.f_idx[pf++] = w * 32 + bit;
+      }
+      pbase += __shfl_sync(kFull, xp, 31);
+      fbase += __shfl_sync(kFull, xf, 31);
+    }
+  }
+  const int q0 = lr * kTile;
+  __shared__ int32_t sF[KIND == MASK_INTERVALS ? kSmemFuncs : 1][kTile];
+  const bool smem = KIND == MASK_INTERVALS && p.nfunc <= kSmemFuncs;
+  if (KIND == MASK_INTERVALS && smem) {
+    const int t = threadIdx.x;
+    const int32_t* Fg = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off;
+    for (int f = 0; f < p.nfunc; ++f)
+      sF[f][t] = (q0 + t < q_len) ? __ldg(Fg + static_cast<long long>(f) * p.total_q + q0 + t) : 0;
+  }
+  __syncthreads();  // the row's p_idx (written by warp 0) and sF are visible to the CTA
+  for (int k = wi; k < np; k += 4) {
+    const long long e = pstart + k;
+    const int j = p.p_idx[e];
+    uint32_t hb;
+    if (KIND == MASK_INTERVALS)
+      hb = payload_intervals_entry(p, e, j, q_len, k_len, q0, hm, q_off, sF, smem);
+    else
+      hb = payload_blocks_entry(p, e, j, q_len, k_len, q0, hm);
+    hb = __reduce_or_sync(kFull, hb);
+    if (lane == 0) p.halves[e] = static_cast<uint8_t>(hb);
+  }
 }
 
 // ------------------------------------------------------------ schedule
+// Reads the front stage's outputs in the workspace (the number of rows
+// included) and writes work_desc there; the back stage copies it into the plan.
 struct SchedParams {
   const int32_t* seq;
+  const int32_t* cu_rows;
   const int32_t* p_off;
   const int32_t* f_off;
   int32_t* hist;     // [NS*(C+1)]
   int32_t* cursors;  // [NS*(C+1)]
   int32_t* work;     // [tasks*4]
-  int B, Hq, Hk, Hmask, rows, C, NS;
+  int B, Hq, Hk, Hmask, C, NS;
 };
 
-__device__ __forceinline__ int task_cost(const SchedParams& p, int h, int row) {
-  const long long flat = static_cast<long long>(p.Hmask == 1 ? 0 : h) * p.rows + row;
+__device__ __forceinline__ int task_cost(const SchedParams& p, int rows, int h, int row) {
+  const long long flat = static_cast<long long>(p.Hmask == 1 ? 0 : h) * rows + row;
   return (p.p_off[flat + 1] - p.p_off[flat]) + (p.f_off[flat + 1] - p.f_off[flat]);
 }
 
@@ -613,6 +648,7 @@ __device__ __forceinline__ int task_bucket(const SchedParams& p, int cost) {
 __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   const int C = p.C;
   const int group = p.Hq / p.Hk;
+  const int rows = p.cu_rows[p.B];
   const long long nb = static_cast<long long>(p.NS) * (C + 1);
   for (long long i = threadIdx.x; i < nb; i += blockDim.x) p.hist[i] = 0;
   __syncthreads();
@@ -624,7 +660,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     const int n = group * nrows;
     for (int t = threadIdx.x & 31; t < n; t += 32) {
       const int h = hk * group + t / nrows, m = t % nrows;
-      atomicAdd(&p.hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, h, begin + m))], 1);
+      atomicAdd(&p.hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, rows, h, begin + m))], 1);
     }
   }
   __syncthreads();
@@ -695,7 +731,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
       const unsigned amask = __ballot_sync(kFull, act);
       if (act) {
         const int h = hk * group + t / nrows, m = t % nrows;
-        const int bucket = task_bucket(p, task_cost(p, h, begin + m));
+        const int bucket = task_bucket(p, task_cost(p, rows, h, begin + m));
         const unsigned same = __match_any_sync(amask, bucket);
         const int rank = __popc(same & ((1u << lane) - 1));
         const int pos = cur[bucket] + rank;
@@ -726,22 +762,93 @@ __global__ void k_count_visible(const uint32_t* payload, long long nwords, long 
 
 }  // namespace
 
+
 // ====================================================================== host
-cudaError_t launch_geometry(const Geometry& g, const int32_t* cu_q, const int32_t* cu_k,
-                            const PlanWorkspace& ws, cudaStream_t st) {
-  GeoParams p{g.layout, g.batch, g.seqlen_q, g.seqlen_k, g.total_q, g.total_k, cu_q, cu_k,
-              ws.cu_rows, ws.seq, ws.row_batch, ws.err, ws.rows_ub};
-  k_geometry<<<1, 1024, 0, st>>>(p);
+cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
+                         const int32_t* cu_q, const int32_t* cu_k, long long* host_header,
+                         long long ticket, cudaStream_t st) {
+  FrontParams p{};
+  p.layout = g.layout;
+  p.B = g.batch;
+  p.Sq = g.seqlen_q;
+  p.Sk = g.seqlen_k;
+  p.total_q = g.total_q;
+  p.total_k = g.total_k;
+  p.nq_max = ws.nq_max;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.mask_func = m.mask_func;
+  p.nfunc = m.nfunc;
+  p.block_mask = m.block_mask;
+  p.block_q = m.block_q;
+  p.block_kv = m.block_kv;
+  p.nbq = m.nbq;
+  p.nbk = m.nbk;
+  p.Hmask = m.Hmask;
+  p.vis_bits = ws.vis_bits;
+  p.full_bits = ws.full_bits;
+  p.p_cnt = ws.p_cnt;
+  p.f_cnt = ws.f_cnt;
+  p.rows_ub = ws.rows_ub;
+  p.words = ws.words;
+  p.cu_rows = ws.cu_rows;
+  p.seq = ws.seq;
+  p.row_batch = ws.row_batch;
+  p.p_off = ws.p_off;
+  p.f_off = ws.f_off;
+  p.header = ws.header;
+  p.host_header = host_header;
+  p.ticket = ticket;
+  p.ctl = ws.ctl;
+  // at least one CTA, so that the last-CTA stage also runs without rows
+  const dim3 grid(ws.rows_ub > 0 ? ws.rows_ub : 1, m.Hmask);
+  if (m.kind == MASK_INTERVALS)
+    k_front<MASK_INTERVALS><<<grid, 128, 0, st>>>(p);
+  else
+    k_front<MASK_BLOCKS><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_classify(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
-                            cudaStream_t st) {
-  ClassifyParams p{};
-  p.seq = ws.seq;
+cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmask, int num_sections,
+                            int max_cost, cudaStream_t st) {
+  if (ws.rows_ub == 0) return cudaSuccess;
+  SchedParams p{ws.seq, ws.cu_rows, ws.p_off, ws.f_off, ws.hist, ws.cursors, ws.work,
+                g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections};
+  k_schedule<<<1, 1024, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws, fa_plan* plan,
+                        const int32_t* cu_q_src, const int32_t* cu_k_src, cudaStream_t st) {
+  const int rows = static_cast<int>(plan->rows);
+  const long long nflat = static_cast<long long>(m.Hmask) * rows;
+  BackParams p{};
+  const int32_t* src[7] = {ws.cu_rows, ws.seq, ws.p_off, ws.f_off, cu_q_src, cu_k_src, ws.work};
+  int32_t* dst[7] = {plan->cu_q_rows, plan->seq_desc, plan->p_off, plan->f_off, plan->cu_seqlens_q,
+                     plan->cu_seqlens_k, plan->work_desc};
+  const long long cnt[7] = {g.batch + 1LL, 8LL * g.batch, nflat + 1, nflat + 1,
+                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0,
+                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0, 4LL * plan->tasks};
+  for (int a = 0; a < 7; ++a) {
+    p.src[a] = src[a];
+    p.dst[a] = dst[a];
+    p.count[a] = cnt[a];
+  }
+  p.vis_bits = ws.vis_bits;
+  p.full_bits = ws.full_bits;
+  p.p_off = ws.p_off;
+  p.f_off = ws.f_off;
   p.row_batch = ws.row_batch;
-  p.cu_rows = ws.cu_rows;
-  p.B = g.batch;
+  p.seq = ws.seq;
+  p.p_idx = plan->p_idx;
+  p.f_idx = plan->f_idx;
+  p.entry_row = plan->entry_row;
+  p.payload = plan->payload;
+  p.halves = plan->halves;
+  p.rows = rows;
+  p.rows_ub = ws.rows_ub;
+  p.nq_max = ws.nq_max;
+  p.words = ws.words;
   p.mask_func = m.mask_func;
   p.nfunc = m.nfunc;
   p.total_q = g.total_q;
@@ -750,93 +857,11 @@ cudaError_t launch_classify(const Geometry& g, const MaskArgs& m, const PlanWork
   p.block_kv = m.block_kv;
   p.nbq = m.nbq;
   p.nbk = m.nbk;
-  p.vis_bits = ws.vis_bits;
-  p.full_bits = ws.full_bits;
-  p.p_cnt = ws.p_cnt;
-  p.f_cnt = ws.f_cnt;
-  p.err = ws.err;
-  p.rows_ub = ws.rows_ub;
-  p.words = ws.words;
-  if (ws.rows_ub == 0) return cudaSuccess;
-  dim3 grid(ws.rows_ub, m.Hmask);
+  const dim3 grid(rows > 0 ? rows : 1, rows > 0 ? m.Hmask : 1);
   if (m.kind == MASK_INTERVALS)
-    k_classify_intervals<<<grid, 128, 0, st>>>(p);
+    k_back<MASK_INTERVALS><<<grid, 128, 0, st>>>(p);
   else
-    k_classify_blocks<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scan_header(const Geometry& g, int Hmask, const PlanWorkspace& ws,
-                               cudaStream_t st) {
-  ScanParams p{ws.p_cnt, ws.f_cnt, ws.cu_rows, ws.p_off, ws.f_off, ws.header, ws.err,
-               g.batch, Hmask, ws.rows_ub};
-  k_scan_header<<<1, 1024, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_materialize(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws,
-                               fa_plan* plan, const int32_t* cu_q_src, const int32_t* cu_k_src,
-                               cudaStream_t st) {
-  const int rows = static_cast<int>(plan->rows);
-  const long long nflat = static_cast<long long>(m.Hmask) * rows;
-  MatParams mp{};
-  mp.vis_bits = ws.vis_bits;
-  mp.full_bits = ws.full_bits;
-  mp.p_off = ws.p_off;
-  mp.f_off = ws.f_off;
-  mp.p_idx = plan->p_idx;
-  mp.f_idx = plan->f_idx;
-  mp.entry_row = plan->entry_row;
-  mp.rows = rows;
-  mp.rows_ub = ws.rows_ub;
-  mp.words = ws.words;
-  const int32_t* src[6] = {ws.cu_rows, ws.seq, ws.p_off, ws.f_off, cu_q_src, cu_k_src};
-  int32_t* dst[6] = {plan->cu_q_rows, plan->seq_desc, plan->p_off, plan->f_off, plan->cu_seqlens_q,
-                     plan->cu_seqlens_k};
-  const long long cnt[6] = {g.batch + 1LL, 8LL * g.batch, nflat + 1, nflat + 1,
-                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0,
-                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0};
-  for (int a = 0; a < 6; ++a) {
-    mp.src[a] = src[a];
-    mp.dst[a] = dst[a];
-    mp.count[a] = cnt[a];
-  }
-  k_materialize<<<dim3(rows > 0 ? rows : 1, rows > 0 ? m.Hmask : 1), 32, 0, st>>>(mp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || plan->P == 0) return e;
-  PayloadParams pp{};
-  pp.entry_row = plan->entry_row;
-  pp.p_idx = plan->p_idx;
-  pp.row_batch = ws.row_batch;
-  pp.seq = ws.seq;
-  pp.payload = plan->payload;
-  pp.halves = plan->halves;
-  pp.rows = rows;
-  pp.P = static_cast<int>(plan->P);
-  pp.mask_func = m.mask_func;
-  pp.nfunc = m.nfunc;
-  pp.total_q = g.total_q;
-  pp.block_mask = m.block_mask;
-  pp.block_q = m.block_q;
-  pp.block_kv = m.block_kv;
-  pp.nbq = m.nbq;
-  pp.nbk = m.nbk;
-  if (m.kind == MASK_INTERVALS && m.nfunc <= kMaxFuncFast)
-    k_payload_intervals<true><<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
-  else if (m.kind == MASK_INTERVALS)
-    k_payload_intervals<false><<<static_cast<unsigned>(plan->P), 128, 0, st>>>(pp);
-  else
-    k_payload_blocks<<<static_cast<unsigned>((plan->P + 3) / 4), 128, 0, st>>>(pp);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_schedule(const Geometry& g, fa_plan* plan, int32_t* hist, int32_t* cursors,
-                            int num_sections, int max_cost, cudaStream_t st) {
-  if (plan->tasks == 0) return cudaSuccess;
-  SchedParams p{plan->seq_desc, plan->p_off, plan->f_off, hist, cursors, plan->work_desc,
-                g.batch, g.heads_q, g.heads_k, plan->Hmask, static_cast<int>(plan->rows),
-                max_cost, num_sections};
-  k_schedule<<<1, 1024, 0, st>>>(p);
+    k_back<MASK_BLOCKS><<<grid, 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -851,9 +876,8 @@ cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, c
 }  // namespace bsm
 
 // ================================================= allocation-free sizing
-// Scratch of fa_plan_header_noalloc: the geometry, classification and scan
-// stages above write their workspace here instead of into memory obtained
-// from an allocator.  Every device on which the library is loaded holds
+// Scratch of fa_plan_header_noalloc: the front stage above writes its
+// workspace here instead of into memory obtained from an allocator.  Every device on which the library is loaded holds
 // this array until the process exits.
 static constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -909,7 +933,7 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   const long long words = kt_ub > 0 ? (kt_ub + 31) / 32 : 1;
   const long long nflat = static_cast<long long>(Hmask) * rows_ub;
   // same sub-arrays as the allocating build's first workspace
-  const size_t sizes[] = {4, 64, 4ull * (B + 1), 32ull * B, 4ull * rows_ub, 4ull * nflat * words,
+  const size_t sizes[] = {8, 64, 4ull * (B + 1), 32ull * B, 4ull * rows_ub, 4ull * nflat * words,
                           4ull * nflat * words, 4ull * nflat, 4ull * nflat, 4ull * (nflat + 1),
                           4ull * (nflat + 1)};
   size_t off[11], need = 0;
@@ -928,7 +952,7 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address(dev, &e));
   if (!base) return report_error(FA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
   PlanWorkspace ws{};
-  ws.err = reinterpret_cast<uint32_t*>(base + off[0]);
+  ws.ctl = reinterpret_cast<unsigned*>(base + off[0]);
   ws.header = reinterpret_cast<long long*>(header_out);  // the scan writes the header straight to the output
   ws.cu_rows = reinterpret_cast<int32_t*>(base + off[2]);
   ws.seq = reinterpret_cast<int32_t*>(base + off[3]);
@@ -940,6 +964,7 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   ws.p_off = reinterpret_cast<int32_t*>(base + off[9]);
   ws.f_off = reinterpret_cast<int32_t*>(base + off[10]);
   ws.rows_ub = static_cast<int>(rows_ub);
+  ws.nq_max = static_cast<int>(nq_max);
   ws.kt_ub = static_cast<int>(kt_ub);
   ws.words = static_cast<int>(words);
   MaskArgs m{};
@@ -948,12 +973,12 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   m.nfunc = nfunc;
   m.Hmask = Hmask;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the error word must start at zero
-  e = cudaMemsetAsync(ws.err, 0, 4, st);
-  if (e == cudaSuccess) e = launch_geometry(g, geom->cu_seqlens_q, geom->cu_seqlens_k, ws, st);
-  if (e == cudaSuccess) e = launch_classify(g, m, ws, st);
-  if (e == cudaSuccess) e = launch_scan_header(g, Hmask, ws, st);
-  if (e != cudaSuccess) return report_error(FA_ERR_CUDA, "allocation-free planner stages: %s", cudaGetErrorString(e));
+  // the front stage leaves its control words at zero, but a call whose
+  // launch failed half-way is not known to have: start from zero every time
+  e = cudaMemsetAsync(ws.ctl, 0, 8, st);
+  if (e == cudaSuccess)
+    e = launch_front(g, m, ws, geom->cu_seqlens_q, geom->cu_seqlens_k, nullptr, 0, st);
+  if (e != cudaSuccess) return report_error(FA_ERR_CUDA, "allocation-free planner stage: %s", cudaGetErrorString(e));
   return FA_OK;
 }
 
