@@ -28,6 +28,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "masked attn fwd TFLOPS on visible pairs, % of GB300 BF16 roofline; plan build µs"
+# clock cycles of the sleep kernel queued ahead of each timed forward launch (about 0.1 ms)
+SLEEP_CYCLES = 200_000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOAD_DESC = {
     "tiny_causal": "tiny causal B=1 H=2 S=256 d=64 BSHD",
@@ -304,13 +306,30 @@ def main():
     if world > 1:
         dist.barrier()
     t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    fwd_in_step_ms = [e[1].elapsed_time(e[2]) for e in evs]
     tot_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = tot_ms / args.steps
     value = whole_job_tflops(flops_step, world, ms_per_step)
+
+    # The forward kernel alone, for the roofline: a queued sleep keeps the
+    # host ahead of the GPU, so each event pair brackets the launch itself
+    # (in the step above the GPU can wait for the host between plan and
+    # forward).  L2 is flushed before every launch.
+    plan_f = runner.build_plan(dp)
+    torch.cuda.synchronize()
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        kev[i][0].record(stream)
+        runner.forward(dp, plan_f)
+        kev[i][1].record(stream)
+    torch.cuda.synchronize()
+    plan_f.free()
+    clk = clocks.stop()
+    fwd_ms = [a.elapsed_time(b) for a, b in kev]
     fwd_mean = statistics.mean(fwd_ms)
     fwd_tflops = flops_step / (fwd_mean * 1e-3) / 1e12
 
@@ -360,11 +379,14 @@ def main():
         "plan_build_us": statistics.median(build_us),
         "plan_gpu_ms": statistics.median(plan_ms),
         "fwd_ms": fwd_mean,
+        "fwd_ms_in_step": statistics.mean(fwd_in_step_ms),
         "fwd_tflops": fwd_tflops,
         "visible_pairs": info["visible_pairs"] * (w.Hq if info["mask_heads"] == 1 else 1),
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": fwd_tflops / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone per event pair)",
+                     "timing": "forward launch between two events queued behind a sleep kernel, "
+                               "L2 flushed before each launch",
                      "kernel": fwd_kernel_name(w)},
         "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},

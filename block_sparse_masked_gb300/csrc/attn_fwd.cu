@@ -8,10 +8,11 @@
 // Eq. 1, softmax(mod(Q K^T * scale)) V, with an online softmax: the score
 // matrix is never stored.
 //
-// Persistent CTAs (one per SM) take tasks in work_desc order from a
-// call-local atomic counter ("Flex Attention Mask Plan Design" §4.8: the
-// queue counter is per-call workspace, so one plan can serve concurrent
-// calls).  576 threads, warp-specialised:
+// Persistent CTAs (one per SM) take tasks in work_desc order from an atomic
+// counter that belongs to the launching stream, not to the plan ("Flex
+// Attention Mask Plan Design" §4.8: the queue counter is per-call state, so
+// one plan can serve concurrent calls on different streams); the last CTA to
+// finish resets it.  576 threads, warp-specialised:
 //   warp 16     TMA producer: Q tiles into a 2-deep ring; K and V tiles into
 //               one ring, issued in the order the MMAs consume them (K of
 //               tile g+1 before V of tile g).
@@ -90,7 +91,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int Hq, Hk, Hmask, rows, total_q, ntasks;
-  int* counter;      // task queue head (zeroed before the launch)
+  int* counter;      // task queue [2]: next task, CTAs finished (zero at launch, reset by the last CTA)
   int flags;
   float scale;       // multiplies Q K^T
   float scale_log2;  // scale * log2(e)
@@ -204,7 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(sizeof(Task) * kTaskRing <= 256, "task ring");
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
     // dynamic shared memory not aligned as expected: report and stop (uniform exit)
-    if (threadIdx.x == 0) atomicOr(&g_fwd_err, DEVERR_SMEM_ALIGN);
+    if (threadIdx.x == 0) {
+      atomicOr(&g_fwd_err, DEVERR_SMEM_ALIGN);
+      task_queue_release(p.counter);
+    }
     return;
   }
 
@@ -708,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) task_queue_release(p.counter);  // every fetch of this CTA is done
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

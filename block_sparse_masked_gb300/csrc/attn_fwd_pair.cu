@@ -98,7 +98,7 @@ struct PairParams {
   float* lse;
   uint32_t* err;     // the forward kernels' error word
   int Hq, Hk, Hmask, rows, total_q, ntasks;
-  int* counter;      // task queue head (zeroed before the launch)
+  int* counter;      // task queue [2]: next task, CTAs finished (zero at launch, reset by the last CTA)
   float scale_log2;  // scale * log2(e)
 };
 
@@ -196,7 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
-    if (threadIdx.x == 0) atomicOr(p.err, DEVERR_SMEM_ALIGN);
+    if (threadIdx.x == 0) {
+      atomicOr(p.err, DEVERR_SMEM_ALIGN);
+      task_queue_release(p.counter);
+    }
     return;
   }
   const uint32_t sQ = base + C::kOffQ;
@@ -569,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) task_queue_release(p.counter);  // every fetch of this CTA is done
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

@@ -7,6 +7,18 @@
 
 namespace bsm {
 
+// Task queue of a persistent kernel: counter[0] = next task, counter[1] =
+// CTAs that have finished.  Both are zero at launch; the last CTA to finish
+// sets them back to zero, so consecutive launches on one stream can share
+// the pair.  Called by one thread of each CTA after its last fetch.
+__device__ __forceinline__ void task_queue_release(int* counter) {
+  __threadfence();
+  if (atomicAdd(counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(counter, 0);
+    atomicExch(counter + 1, 0);
+  }
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -167,9 +167,14 @@ typedef struct {
  * Every base pointer must be 16-byte aligned.  The geometry must equal the
  * one the plan was built for (FA_ERR_PLAN_MISMATCH otherwise).  The call
  * is asynchronous on `stream`; one plan may be used concurrently on
- * several streams.  Each call takes a 4-byte task-queue counter from the
- * plan's allocator (or the library pool) in stream order and returns it
- * after the launch.
+ * several streams.  The kernel's task queue (two device ints) belongs to
+ * the stream: the library keeps one pair per (device, stream), zeroed once
+ * and left at zero by every launch, so a call issues no other device work.
+ * While `stream` is being captured into a graph, the call instead takes a
+ * pair of its own (from device memory the library set aside at a plan build;
+ * FA_ERR_ALLOC once about a thousand captured calls have used it up) and
+ * zeroes it with a memset node, so that replays of different graphs cannot
+ * share one.
  */
 int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, void* o,
            float* lse, const fa_geometry* geom, float scale, const fa_mods* mods,
