@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(sizeof(Task) * kTaskRing <= 256, "task ring");
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
     // dynamic shared memory not aligned as expected: report and stop (uniform exit)
+    grid_dependency_wait();
     if (threadIdx.x == 0) {
       atomicOr(&g_fwd_err, DEVERR_SMEM_ALIGN);
       task_queue_release(p.counter);
@@ -244,6 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up above overlaps the previous kernel of the stream; the plan, the
+  // task queue, Q/K/V and O belong to work that may still be finishing
+  grid_dependency_wait();
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -796,10 +800,21 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
     *why = "device attribute / cudaFuncSetAttribute failed";
     return e;
   }
-  // persistent: one CTA per SM (shared memory keeps it to one), tasks by static stride
+  // persistent: one CTA per SM (shared memory keeps it to one), tasks from the queue;
+  // launched with programmatic stream serialization, so that its set-up
+  // overlaps the end of the previous kernel in the stream
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(pl->tasks, sms));
-  kern<<<grid, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, mo, mkh, mvh, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, mkh, mvh, p);
   if (e != cudaSuccess) *why = "forward kernel launch failed";
   return e;
 }

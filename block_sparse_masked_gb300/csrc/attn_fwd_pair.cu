@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
+    grid_dependency_wait();
     if (threadIdx.x == 0) {
       atomicOr(p.err, DEVERR_SMEM_ALIGN);
       task_queue_release(p.counter);
@@ -256,6 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // set-up above overlaps the previous kernel of the stream; the plan, the
+  // task queue, Q/K/V and O belong to work that may still be finishing
+  grid_dependency_wait();
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -655,10 +659,21 @@ cudaError_t launch_pair_impl(const FwdLaunch& a, cudaStream_t st, const char** w
     *why = "device attribute / cudaFuncSetAttribute failed";
     return e;
   }
-  // persistent: one CTA per SM; about half the work_desc entries are pairs
+  // persistent: one CTA per SM; about half the work_desc entries are pairs.
+  // Launched with programmatic stream serialization, so that its set-up
+  // overlaps the end of the previous kernel in the stream.
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((pl->tasks + 1) / 2, sms));
-  kern<<<grid, kThreads, PCfg<D>::kSmem, st>>>(mq, mk, mv, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = PCfg<D>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
   if (e != cudaSuccess) *why = "forward kernel launch failed";
   return e;
 }

@@ -19,6 +19,13 @@ __device__ __forceinline__ void task_queue_release(int* counter) {
   }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel in its stream has
+// finished; this waits until that kernel has completed and its memory
+// operations are visible (a no-op for an ordinary launch).  Everything that
+// reads or writes global memory another kernel may touch comes after it.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -71,6 +71,22 @@ def test_plan_parity_fuzz(seed, shape):
     plan.free()
 
 
+@pytest.mark.parametrize("seed", range(2))
+@pytest.mark.parametrize("shape", [
+    # more endpoints per row than the back stage keeps in shared memory
+    dict(B=1, S=400, nfunc=17), dict(B=2, S=300, nfunc=15),
+    # more samples than the front stage's last CTA has threads, empty ones at
+    # both ends and in runs (rows of a sample found by binary search)
+    dict(B=0, S=0, nfunc=3, lens=[0, 0] + [int(x) for x in
+                                           np.random.default_rng(5).integers(0, 300, 297)] + [0, 0]),
+])
+def test_plan_parity_wide(seed, shape):
+    w = _interval_workload(seed, **shape)
+    dp, plan = PT.gpu_plan(w)
+    PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w))
+    plan.free()
+
+
 @pytest.mark.parametrize("geom", [(64, 64), (48, 80), (128, 32), (200, 300), (16, 128)])
 @pytest.mark.parametrize("S", [700, 1024])
 def test_block_plan_parity_geometries(geom, S):
