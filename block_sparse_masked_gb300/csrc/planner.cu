@@ -22,6 +22,7 @@
 // can only be written once the host has sized and allocated it.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -623,6 +624,7 @@ struct SchedParams {
   int32_t* cursors;  // [NS*(C+1)]
   int32_t* work;     // [tasks*4]
   int B, Hq, Hk, Hmask, C, NS;
+  int in_smem;       // 1: histogram and cursors live in dynamic shared memory (2*NS*(C+1) ints)
 };
 
 __device__ __forceinline__ int task_cost(const SchedParams& p, int rows, int h, int row) {
@@ -650,7 +652,10 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   const int group = p.Hq / p.Hk;
   const int rows = p.cu_rows[p.B];
   const long long nb = static_cast<long long>(p.NS) * (C + 1);
-  for (long long i = threadIdx.x; i < nb; i += blockDim.x) p.hist[i] = 0;
+  extern __shared__ int32_t s_counts[];
+  int32_t* const hist = p.in_smem ? s_counts : p.hist;
+  int32_t* const cursors = p.in_smem ? s_counts + nb : p.cursors;
+  for (long long i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   // one warp per section (the sections are many and small: one per sample
   // and K/V head, a few dozen tasks each)
@@ -660,7 +665,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     const int n = group * nrows;
     for (int t = threadIdx.x & 31; t < n; t += 32) {
       const int h = hk * group + t / nrows, m = t % nrows;
-      atomicAdd(&p.hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, rows, h, begin + m))], 1);
+      atomicAdd(&hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, rows, h, begin + m))], 1);
     }
   }
   __syncthreads();
@@ -668,12 +673,12 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   // 2a. positive-cost tasks per section (one warp per section, lanes over
   //     buckets); kept in the section's bucket-0 cursor until 2b
   for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
-    const int32_t* h = p.hist + static_cast<long long>(sct) * (C + 1);
+    const int32_t* h = hist + static_cast<long long>(sct) * (C + 1);
     long long tot = 0;
     for (int c = lane; c < C; c += 32) tot += h[c];
 #pragma unroll
     for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
-    if (lane == 0) p.cursors[static_cast<long long>(sct) * (C + 1)] = static_cast<int32_t>(tot);
+    if (lane == 0) cursors[static_cast<long long>(sct) * (C + 1)] = static_cast<int32_t>(tot);
   }
   __syncthreads();
   // 2b. section starts: positive tasks of section s after those of sections
@@ -682,10 +687,10 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   long long carry_pos = 0;
   for (int base = 0; base < p.NS; base += 1024) {
     const int sct = base + threadIdx.x;
-    const long long pos = (sct < p.NS) ? p.cursors[static_cast<long long>(sct) * (C + 1)] : 0;
+    const long long pos = (sct < p.NS) ? cursors[static_cast<long long>(sct) * (C + 1)] : 0;
     long long tot;
     const long long start = carry_pos + block_excl_scan(pos, &tot);
-    if (sct < p.NS) p.cursors[static_cast<long long>(sct) * (C + 1)] = static_cast<int32_t>(start);
+    if (sct < p.NS) cursors[static_cast<long long>(sct) * (C + 1)] = static_cast<int32_t>(start);
     carry_pos += tot;
   }
   if (threadIdx.x == 0) s_tot_pos = carry_pos;
@@ -693,18 +698,18 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   long long carry_zero = s_tot_pos;
   for (int base = 0; base < p.NS; base += 1024) {
     const int sct = base + threadIdx.x;
-    const long long z = (sct < p.NS) ? p.hist[static_cast<long long>(sct) * (C + 1) + C] : 0;
+    const long long z = (sct < p.NS) ? hist[static_cast<long long>(sct) * (C + 1) + C] : 0;
     long long tot;
     const long long start = carry_zero + block_excl_scan(z, &tot);
-    if (sct < p.NS) p.cursors[static_cast<long long>(sct) * (C + 1) + C] = static_cast<int32_t>(start);
+    if (sct < p.NS) cursors[static_cast<long long>(sct) * (C + 1) + C] = static_cast<int32_t>(start);
     carry_zero += tot;
   }
   __syncthreads();
   // 2c. bucket cursors inside each section: its start plus an exclusive scan
   //     of its bucket counts (one warp per section, 32 buckets at a time)
   for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
-    const int32_t* h = p.hist + static_cast<long long>(sct) * (C + 1);
-    int32_t* cur = p.cursors + static_cast<long long>(sct) * (C + 1);
+    const int32_t* h = hist + static_cast<long long>(sct) * (C + 1);
+    int32_t* cur = cursors + static_cast<long long>(sct) * (C + 1);
     long long run = cur[0];
     __syncwarp();
     for (int c0 = 0; c0 < C; c0 += 32) {
@@ -724,7 +729,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     const int b = sct / p.Hk, hk = sct % p.Hk;
     const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5], q_len = p.seq[8 * b + 2];
     const int n = group * nrows;
-    int32_t* cur = p.cursors + static_cast<long long>(sct) * (C + 1);
+    int32_t* cur = cursors + static_cast<long long>(sct) * (C + 1);
     for (int t0 = 0; t0 < n; t0 += 32) {
       const int t = t0 + lane;
       const bool act = t < n;
@@ -813,8 +818,27 @@ cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmas
                             int max_cost, cudaStream_t st) {
   if (ws.rows_ub == 0) return cudaSuccess;
   SchedParams p{ws.seq, ws.cu_rows, ws.p_off, ws.f_off, ws.hist, ws.cursors, ws.work,
-                g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections};
-  k_schedule<<<1, 1024, 0, st>>>(p);
+                g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections, 0};
+  // histogram and cursors in shared memory when they fit (shared-memory
+  // atomics and the single CTA's scans then stay on chip)
+  constexpr size_t kSchedSmemMax = 160 * 1024;
+  const size_t bytes = 8ull * num_sections * (max_cost + 1);
+  size_t dyn = 0;
+  if (bytes <= kSchedSmemMax) {
+    static std::atomic<bool> attr_set[128];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+      if (cudaFuncSetAttribute(k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSchedSmemMax)) != cudaSuccess)
+        return cudaGetLastError();
+      attr_set[dev].store(true, std::memory_order_release);
+    }
+    p.in_smem = 1;
+    dyn = bytes;
+  }
+  k_schedule<<<1, 1024, dyn, st>>>(p);
   return cudaGetLastError();
 }
 

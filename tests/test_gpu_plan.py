@@ -156,3 +156,17 @@ def test_empty_query_geometry():
     runner.forward(dp, plan)
     torch.cuda.synchronize()
     plan.free()
+
+
+def test_plan_parity_schedule_counts_in_global_memory():
+    # 256 K/V heads x 81 cost buckets: the schedule's counting arrays (2 x 20736
+    # ints) exceed what it keeps in shared memory and live in the workspace
+    B, Sq, Sk, H = 1, 128, 10240, 256
+    mf = W.random_intervals(31, B, Sq, Sk, 3, 1)
+    q = torch.zeros(B, Sq, H, 64, dtype=torch.bfloat16)
+    kv = torch.zeros(1, 1, 1, 1, dtype=torch.bfloat16).expand(B, Sk, H, 64)
+    w = W.Workload("many_heads", W.LAYOUT_BSHD, B, Sq, Sk, H, H, 64, q, kv, kv, 1.0, "intervals",
+                   mask_func=mf)
+    dp, plan = PT.gpu_plan(w)
+    PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w))
+    plan.free()
