@@ -8,11 +8,12 @@
 // Eq. 1, softmax(mod(Q K^T * scale)) V, with an online softmax: the score
 // matrix is never stored.
 //
-// Persistent CTAs (one per SM) take tasks in work_desc order from an atomic
-// counter that belongs to the launching stream, not to the plan ("Flex
-// Attention Mask Plan Design" §4.8: the queue counter is per-call state, so
-// one plan can serve concurrent calls on different streams); the last CTA to
-// finish resets it.  576 threads, warp-specialised:
+// Tasks are scheduled in work_desc order by the GPU's cluster launch control
+// ("Flex Attention Mask Plan Design" §4.8: the SM100/SM103 forward takes its
+// tasks from the hardware CLC queue): the kernel is launched with one CTA per
+// task, shared memory keeps one CTA per SM, and each running CTA handles its
+// own task and then takes over tasks of CTAs that have not started yet.  No
+// state outlives a launch, so one plan serves concurrent calls on any streams.  576 threads, warp-specialised:
 //   warp 16     TMA producer: Q tiles into a 2-deep ring; K and V tiles into
 //               one ring, issued in the order the MMAs consume them (K of
 //               tile g+1 before V of tile g).
@@ -91,7 +92,6 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int Hq, Hk, Hmask, rows, total_q, ntasks;
-  int* counter;      // task queue [2]: next task, CTAs finished (zero at launch, reset by the last CTA)
   int flags;
   float scale;       // multiplies Q K^T
   float scale_log2;  // scale * log2(e)
@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_drain = b_pvdone + 24;
   const uint32_t b_tfull = b_drain + 8;          // [kTaskRing] task ring
   const uint32_t b_tempty = b_tfull + 8 * kTaskRing;
+  const uint32_t b_clc = b_tempty + 8 * kTaskRing;  // cluster launch control response
 
   uint8_t* small = gbase + C::kOffSmall;
   int* slot_hm = reinterpret_cast<int*>(small + 400);  // [NS] key halves of the K tile in each ring slot
@@ -200,16 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   Task* tring = reinterpret_cast<Task*>(small + 512);    // [kTaskRing]
   Task* tdec = reinterpret_cast<Task*>(small + 768);     // [2] task as seen by the softmax warps
   float* xmax = reinterpret_cast<float*>(small + 896);  // [2 parity][kWG][128]; also the per-task sum exchange
-  static_assert(16 + 16 + 16 * C::kSlots + 3 * 24 + 8 + 16 * kTaskRing <= 400, "barrier slots");
+  const uint32_t clc_resp = smem_u32(small + 864);      // [2] 16-byte cluster launch control responses
+  static_assert(16 + 16 + 16 * C::kSlots + 3 * 24 + 8 + 16 * kTaskRing + 8 <= 400, "barrier slots");
+  static_assert(768 + 2 * sizeof(Task) <= 864, "task broadcast");
   static_assert(C::kSlots * 4 <= 80, "slot tags");
   static_assert(sizeof(Task) * kTaskRing <= 256, "task ring");
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
     // dynamic shared memory not aligned as expected: report and stop (uniform exit)
-    grid_dependency_wait();
-    if (threadIdx.x == 0) {
-      atomicOr(&g_fwd_err, DEVERR_SMEM_ALIGN);
-      task_queue_release(p.counter);
-    }
+    if (threadIdx.x == 0) atomicOr(&g_fwd_err, DEVERR_SMEM_ALIGN);
     return;
   }
 
@@ -230,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_pvdone + 8 * i, 1);
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_clc, 1);
     for (int i = 0; i < kTaskRing; ++i) {
       mbar_init(b_tfull + 8 * i, 1);
       mbar_init(b_tempty + 8 * i, 2);  // the MMA issuer and softmax thread 0
@@ -305,11 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ++ti;
     };
+    ClcTasks tasks{clc_resp, b_clc};
     for (;;) {
-      int t = 0;
-      if (leader) t = atomicAdd(p.counter, 1);
+      int t = -1;
+      if (leader) t = tasks.next(abort_flag, &g_fwd_err, kWaitTimeoutNs);
       t = __shfl_sync(0xffffffffu, t, 0);
-      if (t >= p.ntasks) break;
+      if (t < 0 || t >= p.ntasks) break;
       const Task k = load_task(p, t);
       publish(k);
       if (k.n == 0) continue;
@@ -364,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(b_qfull + 8 * (u & 1), (u >> 1) & 1, kWaitTimeoutNs);
       for (int u = (c_issued > NS ? c_issued - NS : 0); u < c_issued; ++u)
         mbar_wait_drain(b_full + 8 * (u % NS), (u / NS) & 1, kWaitTimeoutNs);
+      tasks.drain(kWaitTimeoutNs);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -716,7 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) task_queue_release(p.counter);  // every fetch of this CTA is done
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -767,7 +768,6 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   }
   FwdParams p{};
   p.ntasks = static_cast<int>(pl->tasks);
-  p.counter = a.counter;
   p.work = pl->work_desc;
   p.seq = pl->seq_desc;
   p.p_off = pl->p_off;
@@ -800,10 +800,12 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
     *why = "device attribute / cudaFuncSetAttribute failed";
     return e;
   }
-  // persistent: one CTA per SM (shared memory keeps it to one), tasks from the queue;
-  // launched with programmatic stream serialization, so that its set-up
-  // overlaps the end of the previous kernel in the stream
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(pl->tasks, sms));
+  // one CTA per task; shared memory keeps one per SM and the running CTAs
+  // take over the rest (cluster launch control).  Launched with programmatic
+  // stream serialization, so that its set-up overlaps the end of the
+  // previous kernel in the stream.
+  (void)sms;
+  const unsigned grid = static_cast<unsigned>(pl->tasks);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -98,7 +98,6 @@ struct PairParams {
   float* lse;
   uint32_t* err;     // the forward kernels' error word
   int Hq, Hk, Hmask, rows, total_q, ntasks;
-  int* counter;      // task queue [2]: next task, CTAs finished (zero at launch, reset by the last CTA)
   float scale_log2;  // scale * log2(e)
 };
 
@@ -196,11 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   if ((base - raw) + C::kNeed > static_cast<uint32_t>(C::kSmem)) {
-    grid_dependency_wait();
-    if (threadIdx.x == 0) {
-      atomicOr(p.err, DEVERR_SMEM_ALIGN);
-      task_queue_release(p.counter);
-    }
+    if (threadIdx.x == 0) atomicOr(p.err, DEVERR_SMEM_ALIGN);
     return;
   }
   const uint32_t sQ = base + C::kOffQ;
@@ -217,12 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_drain = b_pvdone + 16;       // [2] S issuer, PV issuer
   const uint32_t b_tfull = b_drain + 16;        // [kTaskRing]
   const uint32_t b_tempty = b_tfull + 8 * kTaskRing;
+  const uint32_t b_clc = b_tempty + 8 * kTaskRing;  // cluster launch control response
   uint8_t* small = gbase + C::kOffSmall;
   int* slot_tag = reinterpret_cast<int*>(small + 400);            // [NS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + 464);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(small + 468);
   PairTask* tring = reinterpret_cast<PairTask*>(small + 512);     // [kTaskRing]
-  static_assert(8 + 8 + 16 * NS + 16 + 8 + 16 + 16 + 16 + 16 * kTaskRing <= 400, "barrier slots");
+  const uint32_t clc_resp = smem_u32(small + 672);                 // [2] 16-byte cluster launch control responses
+  static_assert(8 + 8 + 16 * NS + 16 + 8 + 16 + 16 + 16 + 16 * kTaskRing + 8 <= 400, "barrier slots");
+  static_assert(512 + sizeof(PairTask) * kTaskRing <= 672 && 672 + 32 <= C::kSmallBytes, "task ring, responses");
   static_assert(NS * 4 <= 64, "slot tags");
   static_assert(sizeof(PairTask) * kTaskRing <= 512, "task ring");
 
@@ -242,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_sfree, 4);
     mbar_init(b_drain, 1);
     mbar_init(b_drain + 8, 1);
+    mbar_init(b_clc, 1);
     for (int i = 0; i < kTaskRing; ++i) {
       mbar_init(b_tfull + 8 * i, 1);
       mbar_init(b_tempty + 8 * i, kTaskConsumers);
@@ -291,9 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(b_tfull + 8 * slot);
         ++ti;
       };
+      ClcTasks tasks{clc_resp, b_clc};
       for (;;) {
-        const int t = *abort_flag ? p.ntasks : atomicAdd(p.counter, 1);
-        if (t >= p.ntasks) break;
+        const int t = tasks.next(abort_flag, p.err, kWaitTimeoutNs);
+        if (t < 0 || t >= p.ntasks) break;
         const PairTask k = load_pair(p, t);
         if (k.skip) continue;
         publish(k);
@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_issued > 0) mbar_wait_drain(b_qfull, (q_issued - 1) & 1, kWaitTimeoutNs);
         for (int u = (c_issued > NS ? c_issued - NS : 0); u < c_issued; ++u)
           mbar_wait_drain(b_full + 8 * (u % NS), (u / NS) & 1, kWaitTimeoutNs);
+        tasks.drain(kWaitTimeoutNs);
       }
     }
   } else if (warp == kWarpMma || warp == kWarpPv) {
@@ -576,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) task_queue_release(p.counter);  // every fetch of this CTA is done
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -640,7 +640,6 @@ cudaError_t launch_pair_impl(const FwdLaunch& a, cudaStream_t st, const char** w
   p.rows = static_cast<int>(pl->rows);
   p.total_q = static_cast<int>(rows_q);
   p.ntasks = static_cast<int>(pl->tasks);
-  p.counter = a.counter;
   p.scale_log2 = a.scale * kLog2e;
   if (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) {
     *why = "score mods are not supported by the two-tile forward";
@@ -659,10 +658,13 @@ cudaError_t launch_pair_impl(const FwdLaunch& a, cudaStream_t st, const char** w
     *why = "device attribute / cudaFuncSetAttribute failed";
     return e;
   }
-  // persistent: one CTA per SM; about half the work_desc entries are pairs.
-  // Launched with programmatic stream serialization, so that its set-up
-  // overlaps the end of the previous kernel in the stream.
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((pl->tasks + 1) / 2, sms));
+  // one CTA per work_desc entry (the odd ones find nothing to do and take
+  // over others at once); shared memory keeps one per SM and the running
+  // CTAs take over the rest (cluster launch control).  Launched with
+  // programmatic stream serialization, so that its set-up overlaps the end
+  // of the previous kernel in the stream.
+  (void)sms;
+  const unsigned grid = static_cast<unsigned>(pl->tasks);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -9,10 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
-#include <map>
 #include <string>
-#include <thread>
-#include <tuple>
 #include <vector>
 
 #include "internal.h"
@@ -153,77 +150,6 @@ void ctl_give(int dev, unsigned* p) {
   g_ctl_free[dev].push_back(p);
 }
 
-// ---------------------------------------------------------------- task queues
-// The forward's task queue is two device ints, zero at launch, that the
-// kernel's last CTA sets back to zero.  Launches on one stream run one after
-// another, so each (device, stream) keeps one pair for good (the per-thread
-// default stream is a different stream in every thread, so it is keyed by
-// thread too).  A launch captured into a graph gets a pair of its own, which
-// a memset node zeroes at every replay: replays of different graphs may run
-// at the same time.  Pairs are carved 64 bytes apart from slabs that are
-// allocated and zeroed outside stream capture only: the first plan build on
-// a device (builds synchronise, so they are never captured) makes one.
-struct TaskQueues {
-  using Key = std::tuple<int, uintptr_t, std::thread::id>;
-  static constexpr int kPerSlab = 1024, kIntsApart = 16;
-  std::mutex mu;
-  std::map<Key, int*> by_stream;
-  int* slab[128] = {};
-  int left[128] = {};
-
-  // a new zeroed slab for device dev (caller holds mu; st is not capturing)
-  bool grow(int dev, cudaStream_t st) {
-    void* p = nullptr;
-    if (cudaMalloc(&p, sizeof(int) * kIntsApart * kPerSlab) != cudaSuccess) {
-      cudaGetLastError();
-      return false;
-    }
-    if (cudaMemsetAsync(p, 0, sizeof(int) * kIntsApart * kPerSlab, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess) {  // zero before any stream uses a pair
-      cudaFree(p);
-      return false;
-    }
-    slab[dev] = static_cast<int*>(p);
-    left[dev] = kPerSlab;
-    return true;
-  }
-  int* carve(int dev) {
-    if (left[dev] == 0) return nullptr;
-    int* q = slab[dev] + static_cast<size_t>(kPerSlab - left[dev]) * kIntsApart;
-    --left[dev];
-    return q;
-  }
-};
-
-TaskQueues& task_queues() {
-  static TaskQueues tq;
-  return tq;
-}
-
-// Called by every plan build (never under capture): makes sure the device has pairs.
-bool task_queues_ready(int dev, cudaStream_t st) {
-  if (dev < 0 || dev >= 128) return false;
-  TaskQueues& tq = task_queues();
-  std::lock_guard<std::mutex> lk(tq.mu);
-  return tq.left[dev] > 0 || tq.grow(dev, st);
-}
-
-// The pair of `st` (capturing = false) or a fresh pair for a captured launch.
-int* task_queue(int dev, cudaStream_t st, bool capturing) {
-  if (dev < 0 || dev >= 128) return nullptr;
-  TaskQueues& tq = task_queues();
-  std::lock_guard<std::mutex> lk(tq.mu);
-  if (capturing) return tq.carve(dev);  // no allocation can happen during capture
-  const TaskQueues::Key key{dev, reinterpret_cast<uintptr_t>(st),
-                            st == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id()};
-  auto it = tq.by_stream.find(key);
-  if (it != tq.by_stream.end()) return it->second;
-  if (tq.left[dev] == 0 && !tq.grow(dev, st)) return nullptr;
-  int* q = tq.carve(dev);
-  tq.by_stream.emplace(key, q);
-  return q;
-}
-
 // Waits until the front stage has published `ticket`, polling host memory;
 // every 64 polls the event after the launch is checked, so that a failed
 // launch or a kernel that ended without publishing returns an error.
@@ -362,7 +288,6 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
 
   long long* hh = pinned_header();
   if (!hh) return bail(fail(FA_ERR_ALLOC, "pinned header buffer"));
-  if (!task_queues_ready(dev, st)) return bail(fail(FA_ERR_ALLOC, "forward task queues"));
   cudaEvent_t ev = front_event(dev);
   if (!ev) return bail(fail(FA_ERR_CUDA, "event creation failed"));
   ws.ctl = ctl_take(dev, st);
@@ -566,18 +491,8 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
   }
   const char* why = "";
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Task queue: the stream's own pair, which needs no per-call zeroing; a
-  // launch captured into a graph gets its own pair and a memset node.
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaError_t ce = cudaStreamIsCapturing(st, &cap)) return cuda_fail(ce, "cudaStreamIsCapturing");
-  const bool capturing = cap != cudaStreamCaptureStatusNone;
-  a.counter = task_queue(plan->device, st, capturing);
-  if (!a.counter)
-    return fail(FA_ERR_ALLOC, capturing ? "no task queue left for a captured launch (build a plan outside "
-                                          "capture to add more)"
-                                        : "task queue allocation failed");
-  cudaError_t e = capturing ? cudaMemsetAsync(a.counter, 0, 2 * sizeof(int), st) : cudaSuccess;
-  if (!e) e = (g.head_dim == 64) ? bsm::launch_fwd_d64(a, st, &why) : bsm::launch_fwd_d128(a, st, &why);
+  // one launch: tasks are scheduled on the device (cluster launch control), no per-call state
+  const cudaError_t e = (g.head_dim == 64) ? bsm::launch_fwd_d64(a, st, &why) : bsm::launch_fwd_d128(a, st, &why);
   if (e) return fail(FA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   return FA_OK;
 }

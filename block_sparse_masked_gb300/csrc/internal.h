@@ -130,7 +130,6 @@ struct FwdLaunch {
   int flags;
   float softcap;
   const float* slopes;  // host, heads_q
-  int* counter;         // device, two ints, zero at launch: task queue head, CTAs finished
 };
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why);

@@ -7,18 +7,6 @@
 
 namespace bsm {
 
-// Task queue of a persistent kernel: counter[0] = next task, counter[1] =
-// CTAs that have finished.  Both are zero at launch; the last CTA to finish
-// sets them back to zero, so consecutive launches on one stream can share
-// the pair.  Called by one thread of each CTA after its last fetch.
-__device__ __forceinline__ void task_queue_release(int* counter) {
-  __threadfence();
-  if (atomicAdd(counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-    atomicExch(counter, 0);
-    atomicExch(counter + 1, 0);
-  }
-}
-
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start before the previous kernel in its stream has
 // finished; this waits until that kernel has completed and its memory
@@ -62,6 +50,38 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
       : "r"(bar), "r"(parity)
       : "memory");
   return ok;
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Persistent scheduling without a counter: a kernel launched with one CTA
+// per task handles its own task first, then takes over the tasks of CTAs
+// that have not started yet -- clusterlaunchcontrol.try_cancel cancels one
+// such CTA (it will never run) and returns its coordinates -- until a
+// request fails, which means no CTA is left waiting.  One request is in
+// flight per CTA; its 16-byte response lands in shared memory and completes
+// an mbarrier phase like a TMA copy.
+__device__ __forceinline__ void clc_request(uint32_t resp, uint32_t bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier reads of the slot come first
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], 16;\n\t}" ::"r"(bar)
+               : "memory");
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(resp), "r"(bar)
+               : "memory");
+}
+// Read a completed response: the cancelled CTA's blockIdx.x, or -1 if none was cancelled.
+__device__ __forceinline__ int clc_response(uint32_t resp) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 q;\n\t"
+      "ld.shared.b128 q, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, q;\n\t"
+      "}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
 }
 
 // Error bits reported by kernels.
@@ -369,5 +389,36 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                "r"(d)
                : "memory");
 }
+
+// The task sequence of one CTA (one thread calls next()): blockIdx.x, then
+// tasks taken over from CTAs that have not started, then -1.  resp is two
+// 16-byte shared-memory slots (used alternately), bar an mbarrier with
+// arrival count 1.  After an abort (bounded wait given up) it returns -1;
+// drain() then waits, bounded, for a request still in flight before exit.
+struct ClcTasks {
+  uint32_t resp, bar;
+  int nreq = 0;
+  bool started = false, done = false, in_flight = false;
+  __device__ __forceinline__ int next(volatile int* abort, uint32_t* err, uint64_t timeout_ns) {
+    if (!started) {
+      started = true;
+      return static_cast<int>(blockIdx.x);
+    }
+    if (done || *abort) return -1;
+    const uint32_t slot = resp + 16u * (nreq & 1);
+    clc_request(slot, bar);
+    in_flight = true;
+    if (!mbar_wait(bar, nreq & 1, abort, err, timeout_ns)) return -1;
+    in_flight = false;
+    ++nreq;
+    const int t = clc_response(slot);
+    if (t < 0) done = true;
+    return t;
+  }
+  __device__ __forceinline__ void drain(uint64_t timeout_ns) {
+    if (in_flight) mbar_wait_drain(bar, nreq & 1, timeout_ns);
+    in_flight = false;
+  }
+};
 
 }  // namespace bsm

@@ -166,15 +166,11 @@ typedef struct {
  *   may be NULL.
  * Every base pointer must be 16-byte aligned.  The geometry must equal the
  * one the plan was built for (FA_ERR_PLAN_MISMATCH otherwise).  The call
- * is asynchronous on `stream`; one plan may be used concurrently on
- * several streams.  The kernel's task queue (two device ints) belongs to
- * the stream: the library keeps one pair per (device, stream), zeroed once
- * and left at zero by every launch, so a call issues no other device work.
- * While `stream` is being captured into a graph, the call instead takes a
- * pair of its own (from device memory the library set aside at a plan build;
- * FA_ERR_ALLOC once about a thousand captured calls have used it up) and
- * zeroes it with a memset node, so that replays of different graphs cannot
- * share one.
+ * is asynchronous on `stream` and issues exactly one kernel launch: the
+ * kernel schedules its tasks on the device (one CTA per task, running CTAs
+ * take over CTAs that have not started, through the GPU's cluster launch
+ * control), so a call keeps no state between launches.  One plan may be
+ * used concurrently on several streams and captured into graphs.
  */
 int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, void* o,
            float* lse, const fa_geometry* geom, float scale, const fa_mods* mods,

@@ -1,10 +1,11 @@
-"""The forward's task queue belongs to the launching stream: every launch
-must find it at zero and leave it at zero.  Repeated launches on one stream,
-launches on two streams at once, the two forward kernels one after the other
-on the same stream, and a graph replayed several times must all give the
-output of the first launch bit for bit (each task is computed by one CTA in a
-fixed order, so the forward is deterministic), and that output must match the
-oracle."""
+"""The forward schedules its tasks on the device (one CTA per task; running
+CTAs take over CTAs that have not started), with no state kept between
+launches.  Repeated launches on one stream, launches on two streams at once,
+the two forward kernels one after the other on the same stream, and a graph
+replayed several times must all give the output of the first launch bit for
+bit (each task is computed by one CTA in a fixed order, so the forward is
+deterministic), and that output must match the oracle: a task handled twice
+or not at all would show."""
 import math
 
 import pytest
@@ -118,7 +119,7 @@ def test_graph_replays():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(dp.o, ref)
-    # the stream's own queue is still usable after the capture
+    # an ordinary launch after the capture
     dp.o.zero_()
     runner.forward(dp, plan)
     torch.cuda.synchronize()
