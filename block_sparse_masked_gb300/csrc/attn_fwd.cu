@@ -13,18 +13,22 @@
 // tasks from the hardware CLC queue): the kernel is launched with one CTA per
 // task, shared memory keeps one CTA per SM, and each running CTA handles its
 // own task and then takes over tasks of CTAs that have not started yet.  No
-// state outlives a launch, so one plan serves concurrent calls on any streams.  576 threads, warp-specialised:
-//   warp 16     TMA producer: Q tiles into a 2-deep ring; K and V tiles into
+// state outlives a launch, so one plan serves concurrent calls on any
+// streams.  320 threads, warp-specialised:
+//   warp 8      TMA producer: Q tiles into a 2-deep ring; K and V tiles into
 //               one ring, issued in the order the MMAs consume them (K of
 //               tile g+1 before V of tile g).
-//   warp 17     TMEM allocator and MMA issuer (one thread): S(g) = Q K^T into
+//   warp 9      TMEM allocator and MMA issuer (one thread): S(g) = Q K^T into
 //               one of three TMEM score buffers, then O += P(g-1) V with P
 //               read from TMEM (it overwrites its score buffer in bf16).
-//   warps 0-15  four softmax warpgroups; thread r of warpgroup w owns score
-//               row r, columns 32w..32w+31 (TMEM lane r).  Per tile they
+//   warps 0-7   two softmax warpgroups; thread r of warpgroup w owns score
+//               row r, columns 64w..64w+63 (TMEM lane r).  Per tile they
 //               exchange the row max through shared memory, write P to TMEM,
-//               rescale their quarter of O when the reference max moves, and
-//               store their quarter of the output at the end of the task.
+//               rescale their half of O when the reference max moves, and
+//               store their half of the output at the end of the task.
+// Block-mask plans run in steps of two 64-key positions (next_step below):
+// tiles with one live key half are paired, so that each step multiplies and
+// exponentiates 128 keys.
 // Every wait is an mbarrier wait with a global-timer limit (the softmax
 // warps synchronise through an mbarrier too, not a named barrier).  After a
 // timeout the CTA records an error bit, stops waiting, drains copies and
@@ -137,6 +141,72 @@ __device__ __forceinline__ int tile_index(const FwdParams& p, const Task& k, int
 __device__ __forceinline__ int tile_halves(const FwdParams& p, const Task& k, int j) {
   return (j < k.np) ? static_cast<int>(__ldg(p.halves + k.p0 + j)) : 3;
 }
+
+// Block-mask plans (HALVES): one ring slot, score buffer and P V step
+// ("step") carries 128 keys in two 64-key positions.  A tile whose two
+// halves are live fills both positions; tiles with one live half are paired
+// in list order, the first at position 0 and the second at position 1, and
+// an unpaired last one runs alone at position 0.  The producer, the MMA
+// issuer and the softmax warps derive the same sequence from the plan.
+// The walk is warp-uniform: lane l keeps the halves of entries base+l (hc)
+// and base+32+l (hn, loaded one batch ahead), read by shuffle.
+struct StepIter {
+  int j;       // next plan entry to examine
+  int pend;    // entry with one live half waiting for a partner, or -1
+  int pend_h;  // its halves
+  int base;    // first entry of the batch in hc
+  int hc, hn;  // this lane's halves of entries base+lane, base+32+lane
+};
+__device__ __forceinline__ void step_begin(const FwdParams& p, const Task& k, StepIter& it, int lane) {
+  it.j = 0;
+  it.pend = -1;
+  it.pend_h = 0;
+  it.base = 0;
+  it.hc = tile_halves(p, k, lane);
+  it.hn = tile_halves(p, k, 32 + lane);
+}
+// Next step of the task: entries ea (position 0) and eb (position 1; eb ==
+// ea for a tile with both halves live, -1 when position 1 is empty) and
+// their halves ha, hb.  Returns false when the task has no step left.
+__device__ __forceinline__ bool next_step(const FwdParams& p, const Task& k, StepIter& it, int lane, int& ea,
+                                          int& eb, int& ha, int& hb) {
+  while (it.j < k.n) {
+    const int j = it.j++;
+    while (j >= it.base + 32) {
+      it.base += 32;
+      it.hc = it.hn;
+      it.hn = tile_halves(p, k, it.base + 32 + lane);
+    }
+    const int h = __shfl_sync(0xffffffffu, it.hc, j - it.base);
+    if (h == 3) {
+      ea = eb = j;
+      ha = hb = 3;
+      return true;
+    }
+    if (it.pend < 0) {
+      it.pend = j;
+      it.pend_h = h;
+      continue;
+    }
+    ea = it.pend;
+    ha = it.pend_h;
+    eb = j;
+    hb = h;
+    it.pend = -1;
+    return true;
+  }
+  if (it.pend >= 0) {
+    ea = it.pend;
+    ha = it.pend_h;
+    eb = -1;
+    hb = 0;
+    it.pend = -1;
+    return true;
+  }
+  return false;
+}
+// Slot tags written by the producer for the MMA issuer (HALVES).
+constexpr int kPos0 = 1, kPos1 = 2, kLastStep = 4;
 
 // tanh(y) for |y| < 0.5 on a pair of columns in packed fp32: Maclaurin
 // series through y^13 (truncation error below 1e-6 relative at |y| = 0.5).
@@ -261,38 +331,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      if (HALVES) {
+        tma_prefetch_desc(&tmKh);
+        tma_prefetch_desc(&tmVh);
+      }
     }
     int tq = 0, c = 0;               // tasks with tiles, ring loads
     int q_issued = 0, c_issued = 0;  // loads actually started (for the abort drain)
     bool pend = false;
     int pv_row = 0, pv_hk = 0, pv_hm = 3;
-    // hm = key halves to load: 3 = the whole 128-row tile, 1 or 2 = only
-    // rows 0-63 or 64-127 (placed where the full tile would put them)
-    auto load_tile = [&](const CUtensorMap* map, const CUtensorMap* hmap, int row, int hk, int hm) {
+    // a whole 128-row tile, stored [chunk][128 rows][128 bytes]
+    auto load_tile = [&](const CUtensorMap* map, int row, int hk) {
       if (leader) {
         const int slot = c % NS;
         if (c >= NS) mbar_wait(b_empty + 8 * slot, ((c / NS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         if (!*abort_flag) {
           c_issued = c + 1;
-          if (HALVES) slot_hm[slot] = hm;  // published to the MMA issuer by the arrive below
-          if (hm == 3) {
-            mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes);
+          mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes);
 #pragma unroll
-            for (int ch = 0; ch < C::kChunks; ++ch)
-              tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384, map, b_full + 8 * slot, hk * D + ch * 64, row);
-          } else {
-            const int sh = hm >> 1;
-            mbar_arrive_expect_tx(b_full + 8 * slot, C::kTileBytes / 2);
+          for (int ch = 0; ch < C::kChunks; ++ch)
+            tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384, map, b_full + 8 * slot, hk * D + ch * 64, row);
+        }
+      }
+      __syncwarp();
+      ++c;
+    };
+    // HALVES: one step into a ring slot, position 0 from source row r0 and
+    // (tag & kPos1) position 1 from r1; a position is one 64-row box per
+    // 64-column chunk, stored where rows 0-63 (64-127) of a whole tile go
+    auto load_step = [&](const CUtensorMap* map64, int r0, int r1, int hk, int tag) {
+      if (leader) {
+        const int slot = c % NS;
+        if (c >= NS) mbar_wait(b_empty + 8 * slot, ((c / NS) - 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        if (!*abort_flag) {
+          c_issued = c + 1;
+          slot_hm[slot] = tag;  // published to the MMA issuer by the arrive below
+          const bool two = (tag & kPos1) != 0;
+          const uint32_t dst = sKV + slot * C::kTileBytes;
+          mbar_arrive_expect_tx(b_full + 8 * slot, two ? C::kTileBytes : C::kTileBytes / 2);
 #pragma unroll
-            for (int ch = 0; ch < C::kChunks; ++ch)
-              tma_load_2d(sKV + slot * C::kTileBytes + ch * 16384 + sh * 8192, hmap, b_full + 8 * slot,
-                          hk * D + ch * 64, row + 64 * sh);
+          for (int ch = 0; ch < C::kChunks; ++ch) {
+            tma_load_2d(dst + ch * 16384, map64, b_full + 8 * slot, hk * D + ch * 64, r0);
+            if (two) tma_load_2d(dst + ch * 16384 + 8192, map64, b_full + 8 * slot, hk * D + ch * 64, r1);
           }
         }
       }
       __syncwarp();
       ++c;
     };
+    int pv_r1 = 0;  // HALVES: source row of the pending V's position 1
     int ti = 0;  // task ring position
     auto publish = [&](const Task& k) {
       if (leader) {
@@ -327,6 +414,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+      // HALVES: steps in next_step order (K of step s, then V of step s-1)
+      int pr_row = -1;  // source row of a one-half tile waiting for a partner
+      bool first = true;
+      auto emit = [&](int r0, int r1, int tag) {
+        if (first && pend) {
+          load_step(&tmVh, pv_row, pv_r1, pv_hk, pv_hm);
+          pend = false;
+        }
+        first = false;
+        load_step(&tmKh, r0, r1, k.hk, tag);
+        if (pend) load_step(&tmVh, pv_row, pv_r1, pv_hk, pv_hm);
+        pend = true;
+        pv_row = r0;
+        pv_r1 = r1;
+        pv_hk = k.hk;
+        pv_hm = tag;
+      };
       for (int j0 = 0; j0 < k.n; j0 += 32) {
         int my_kt = 0, my_hm = 3;
         if (j0 + lane < k.n) {
@@ -338,21 +442,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = j0 + jj;
           const int krow = k.k_off + __shfl_sync(0xffffffffu, my_kt, jj) * kTile;
           const int hm = __shfl_sync(0xffffffffu, my_hm, jj);
-          if (j == 0 && pend) {
-            load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
-            pend = false;
+          if constexpr (HALVES) {
+            // the softmax warps read this entry's predicate words a few
+            // steps from now: bring them into L2 (the payload is read once)
+            if (leader && j < k.np)
+              bulk_prefetch_l2(p.payload + static_cast<long long>(k.p0 + j) * kTile * 4, kTile * 4 * 4);
+            const bool end = j == k.n - 1;
+            if (hm == 3) {
+              emit(krow, krow + 64, kPos0 | kPos1 | ((end && pr_row < 0) ? kLastStep : 0));
+            } else if (pr_row < 0) {
+              pr_row = krow + 64 * (hm >> 1);
+            } else {
+              const int r0 = pr_row;
+              pr_row = -1;
+              emit(r0, krow + 64 * (hm >> 1), kPos0 | kPos1 | (end ? kLastStep : 0));
+            }
+          } else {
+            if (j == 0 && pend) {
+              load_tile(&tmV, pv_row, pv_hk);
+              pend = false;
+            }
+            load_tile(&tmK, krow, k.hk);
+            if (pend) load_tile(&tmV, pv_row, pv_hk);
+            pend = true;
+            pv_row = krow;
+            pv_hk = k.hk;
           }
-          load_tile(&tmK, &tmKh, krow, k.hk, hm);
-          if (pend) load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
-          pend = true;
-          pv_row = krow;
-          pv_hk = k.hk;
-          pv_hm = hm;
         }
       }
+      if (HALVES && pr_row >= 0) emit(pr_row, 0, kPos0 | kLastStep);
       ++tq;
     }
-    if (pend) load_tile(&tmV, &tmVh, pv_row, pv_hk, pv_hm);
+    if (pend) {
+      if constexpr (HALVES) load_step(&tmVh, pv_row, pv_r1, pv_hk, pv_hm);
+      else load_tile(&tmV, pv_row, pv_hk);
+    }
     {
       Task end{};
       end.n = -1;  // end of this CTA's tasks
@@ -392,13 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag) return;
         tc_fence_after();
         const uint32_t pcol = tmem + 128u * sb;
-        const int kk0 = (hm & 1) ? 0 : 4, kk1 = (hm & 2) ? 8 : 4;  // 16-key steps of the live halves
         const uint64_t dV = dV0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
+        // 16-key steps (HALVES: of the occupied positions, hm = the slot tag)
+        const int kk1 = (HALVES && !(hm & kPos1)) ? 4 : 8;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          if (kk >= kk0 && kk < kk1)
+          if (kk < kk1)
             umma_bf16_ts(tmem + C::kColO, pcol + 8u * kk, dV + static_cast<uint64_t>((kk * 2048) >> 4), idO,
-                         (acc || kk > kk0) ? 1u : 0u);
+                         (acc || kk > 0) ? 1u : 0u);
         umma_commit(b_empty + 8 * slot);
         umma_commit(b_pvdone + 8 * sb);
       };
@@ -418,6 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int qb = tq & 1;  // (its buffer is handed back by the softmax epilogue)
         mbar_wait(b_qfull + 8 * qb, (tq >> 1) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
+        // HALVES: one step per slot until the producer's last-step tag (at
+        // most one per plan entry)
+        int nsteps = k.n;
         for (int j = 0; j < k.n; ++j) {
           const int gi = g + j;
           const int sb = gi % 3, slot = c % NS;
@@ -429,21 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t dQ = dQ0 + static_cast<uint64_t>((qb * C::kTileBytes) >> 4);
             const uint64_t dK = dK0 + static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
-            if (hm == 3) {
+            // a step with position 0 only multiplies 64 keys (N = 64)
+            const uint32_t idQK = (HALVES && !(hm & kPos1)) ? idS64 : idS;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                umma_bf16_ss(tmem + 128u * sb, dQ + off16, dK + off16, idS, kk > 0);
-              }
-            } else {
-              // one live half: N = 64 keys, written to the score columns of that half
-              const int sh = hm >> 1;
-              const uint64_t dKh = dK + static_cast<uint64_t>((sh * 8192) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                umma_bf16_ss(tmem + 128u * sb + 64u * sh, dQ + off16, dKh + off16, idS64, kk > 0);
-              }
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off16 = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              umma_bf16_ss(tmem + 128u * sb, dQ + off16, dK + off16, idQK, kk > 0);
             }
             umma_commit(b_sfull + 8 * sb);
             umma_commit(b_empty + 8 * slot);
@@ -453,8 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           pg = gi;
           pacc = j > 0;
           phm = hm;
+          if (HALVES && ((hm & kLastStep) || *abort_flag)) {
+            nsteps = j + 1;
+            break;
+          }
         }
-        g += k.n;
+        g += nsteps;
         ++tq;
       }
       if (pend) issue_pv(pg, pacc, phm);
@@ -505,22 +628,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODS && (p.flags & FA_MOD_ALIBI)) slope2 = p.slopes[k.h] * kLog2e;
       const int q_local = k.m_block * kTile + r;
       float m_run = -INFINITY, l_part = 0.0f;
-      // predicate words of this warpgroup's 64 columns, fetched one tile ahead
+      // predicate words of this warpgroup's 64 columns of this thread's row
       const uint2* pay = reinterpret_cast<const uint2*>(p.payload + static_cast<long long>(k.p0) * kTile * 4 + r * 4) + wg;
-      uint2 pw_next = (k.np > 0) ? __ldg(pay) : make_uint2(~0u, ~0u);
-      int kt_next = MODS ? tile_index(p, k, 0) : 0;
-      for (int j = 0; j < k.n; ++j) {
+      // One step (tile) of the online softmax: plan entry e supplies these
+      // 64 columns (-1: an empty position), hh is its 64-key half, pw the
+      // predicate words of this row (all ones unless partial), kt its K tile.
+      auto step = [&](const int j, const int e, const int hh, const bool partial, const uint2 pw, const int kt) {
         const int gi = g + j;
         const int sb = gi % 3;
-        const bool partial = j < k.np;
-        const uint2 pw = partial ? pw_next : make_uint2(~0u, ~0u);
-        if (j + 1 < k.np) pw_next = __ldg(pay + static_cast<long long>(j + 1) * kTile * 2);
-        const int kt = kt_next;  // key tile (for ALiBi positions), also fetched one tile ahead
-        if (MODS && j + 1 < k.n) kt_next = tile_index(p, k, j + 1);
-        // a warp whose 32 rows see none of this warpgroup's 64 columns (one
-        // key half) has nothing to exponentiate: its P is 0 (that score half
-        // is not even computed when the whole key half is empty)
-        const bool dead = HALVES && partial && __all_sync(0xffffffffu, (pw.x | pw.y) == 0u);
+        // a warp whose 32 rows see none of this warpgroup's 64 columns (an
+        // empty position, or a key half with no visible key in these rows)
+        // has nothing to exponentiate: its P is 0
+        const bool dead = HALVES && (e < 0 || (partial && __all_sync(0xffffffffu, (pw.x | pw.y) == 0u)));
         mbar_wait(b_sfull + 8 * sb, (gi / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
         tc_fence_after();
         float s[kCols];
@@ -556,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kCols; c += 2) f2_unpack(f2_mul(f2_pack(s[c], s[c + 1]), sc2), s[c], s[c + 1]);
           }
           if (p.flags & FA_MOD_ALIBI) {
-            const float fd0 = static_cast<float>(kt * kTile + wg * kCols - q_local);  // k - q at column 0
+            const float fd0 = static_cast<float>(kt * kTile + hh * kCols - q_local);  // k - q at column 0
             const uint64_t sl = f2_pack(slope2, slope2);
 #pragma unroll
             for (int c = 0; c < kCols; c += 2) {
@@ -653,8 +772,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_pfull + 8 * sb);
+      };
+      if constexpr (HALVES) {
+        // Block masks: the sources of the next two steps are held in two
+        // buffers used in turn, so that predicate words (read once, from
+        // HBM) are requested two steps before they are needed.
+        struct Src {
+          int e, h, kt;
+          uint2 pw;
+        };
+        StepIter it;
+        step_begin(p, k, it, lane);
+        auto fetch = [&](Src& q) {
+          int ea = -1, eb = -1, ha = 0, hb = 0;
+          if (!next_step(p, k, it, lane, ea, eb, ha, hb)) return false;
+          if (ea == eb) {
+            q.e = ea;
+            q.h = wg;
+          } else {
+            q.e = wg ? eb : ea;
+            q.h = (wg ? hb : ha) >> 1;
+          }
+          q.pw = make_uint2(~0u, ~0u);
+          if (q.e >= 0 && q.e < k.np) q.pw = __ldg(pay - wg + static_cast<long long>(q.e) * kTile * 2 + q.h);
+          q.kt = (MODS && q.e >= 0) ? tile_index(p, k, q.e) : 0;
+          return true;
+        };
+        Src qa, qb;
+        bool va = fetch(qa);  // a task with tiles has at least one step
+        bool vb = fetch(qb);
+        int j = 0;
+        for (;;) {
+          if (!va) break;
+          {
+            const int e = qa.e, hh = qa.h, kt = qa.kt;
+            const bool partial = e >= 0 && e < k.np;
+            const uint2 pw = partial ? qa.pw : make_uint2(~0u, ~0u);
+            va = fetch(qa);  // step j + 2
+            step(j++, e, hh, partial, pw, kt);
+          }
+          if (!vb) break;
+          {
+            const int e = qb.e, hh = qb.h, kt = qb.kt;
+            const bool partial = e >= 0 && e < k.np;
+            const uint2 pw = partial ? qb.pw : make_uint2(~0u, ~0u);
+            vb = fetch(qb);  // step j + 2
+            step(j++, e, hh, partial, pw, kt);
+          }
+        }
+        g += j;
+      } else {
+        // interval masks: predicate words and K tile fetched one tile ahead
+        uint2 pw_next = (k.np > 0) ? __ldg(pay) : make_uint2(~0u, ~0u);
+        int kt_next = MODS ? tile_index(p, k, 0) : 0;
+        for (int j = 0; j < k.n; ++j) {
+          const bool partial = j < k.np;
+          const uint2 pw = partial ? pw_next : make_uint2(~0u, ~0u);
+          const int kt = kt_next;
+          if (j + 1 < k.np) pw_next = __ldg(pay + static_cast<long long>(j + 1) * kTile * 2);
+          if (MODS && j + 1 < k.n) kt_next = tile_index(p, k, j + 1);
+          step(j, j, wg, partial, pw, kt);
+        }
+        g += k.n;
       }
-      g += k.n;
       // ---------------------------------------------------------- epilogue
       mbar_wait(b_pvdone + 8 * ((g - 1) % 3), ((g - 1) / 3) & 1, abort_flag, &g_fwd_err, kWaitTimeoutNs);
       tc_fence_after();
@@ -760,9 +940,16 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   const int64_t rows_q = (g.layout == FA_LAYOUT_BSHD) ? int64_t(g.batch) * g.seqlen_q : g.total_q;
   const int64_t rows_k = (g.layout == FA_LAYOUT_BSHD) ? int64_t(g.batch) * g.seqlen_k : g.total_k;
   CUtensorMap mq, mk, mv, mo, mkh, mvh;
-  if (!make_map(&mq, a.q, rows_q, g.heads_q, D) || !make_map(&mk, a.k, rows_k, g.heads_k, D) ||
-      !make_map(&mv, a.v, rows_k, g.heads_k, D) || !make_map(&mo, a.o, rows_q, g.heads_q, D) ||
-      !make_map(&mkh, a.k, rows_k, g.heads_k, D, 64) || !make_map(&mvh, a.v, rows_k, g.heads_k, D, 64)) {
+  bool ok = make_map(&mq, a.q, rows_q, g.heads_q, D) && make_map(&mk, a.k, rows_k, g.heads_k, D) &&
+            make_map(&mv, a.v, rows_k, g.heads_k, D) && make_map(&mo, a.o, rows_q, g.heads_q, D);
+  // 64-row boxes of K and V for block-mask plans (two per ring slot)
+  if (HALVES) {
+    ok = ok && make_map(&mkh, a.k, rows_k, g.heads_k, D, 64) && make_map(&mvh, a.v, rows_k, g.heads_k, D, 64);
+  } else {
+    mkh = mk;
+    mvh = mv;
+  }
+  if (!ok) {
     *why = "cuTensorMapEncodeTiled failed (pointer alignment or driver entry point)";
     return cudaErrorInvalidValue;
   }

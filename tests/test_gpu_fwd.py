@@ -109,6 +109,29 @@ def test_block_mask_small_all_rows(d):
     plan.free()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mods", [False, True])
+def test_block_mask_64_blocks_all_rows(d, mods):
+    # 64x64 logical blocks under 128x128 tiles at low density: most visited
+    # tiles have one live 64-key half, and the forward runs two such tiles per
+    # step (an odd count leaves the last one alone); two samples, GQA, a
+    # ragged last tile, per-head masks, and softcap + ALiBi positions per half
+    B, S, H, Hk, blk = 2, 1000, 4, 2, 64
+    gen = torch.Generator().manual_seed(21)
+    q = torch.randn(B, S, H, d, generator=gen).bfloat16()
+    k, v = (torch.randn(B, S, Hk, d, generator=gen).bfloat16() for _ in range(2))
+    nb = -(-S // blk)
+    bm = W.random_block_mask(21, H, nb, nb, 0.12)
+    w = W.Workload("blk64", W.LAYOUT_BSHD, B, S, S, H, Hk, d, q, k, v, 1 / math.sqrt(d), "blocks",
+                   block_mask=bm, block_q=blk, block_kv=blk)
+    if mods:
+        w.softcap = 20.0
+        w.alibi_slopes = W.alibi_slopes(H)
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
 def test_rows_without_visible_keys():
     w = _random_problem(10, B=1, S=300, H=2, d=64, nfunc=3)
     w.mask_func[:] = 0               # nothing visible anywhere
