@@ -101,6 +101,7 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   float y_scale;     // scale / softcap: argument of tanh per unit of Q K^T
   float cap_log2;    // softcap * log2(e)
+  float c1, c3, c5;  // cap_log2 * tanh(y_scale * s) ~ s * (c1 + s^2 * (c3 + s^2 * c5)) for small y
   float slopes[kMaxHeads];
 };
 
@@ -219,13 +220,6 @@ __device__ __forceinline__ uint64_t tanh_series13(uint64_t y) {
   s = f2_fma(s, y2, f2_pack(2.0f / 15.0f, 2.0f / 15.0f));
   s = f2_fma(s, y2, f2_pack(-1.0f / 3.0f, -1.0f / 3.0f));
   return f2_fma(f2_mul(s, y2), y, y);
-}
-// tanh(y) for |y| < 0.125, pair of columns: the same series through y^5
-// (the first omitted term, 17 y^7 / 315, is below 3e-7 of y there).
-__device__ __forceinline__ uint64_t tanh_series5(uint64_t y) {
-  const uint64_t y2 = f2_mul(y, y);
-  const uint64_t q = f2_fma(y2, f2_pack(2.0f / 15.0f, 2.0f / 15.0f), f2_pack(-1.0f / 3.0f, -1.0f / 3.0f));
-  return f2_fma(f2_mul(y, y2), q, y);
 }
 // tanh(y) for any y, from tanh(y) = 1 - 2 / (exp(2y) + 1).
 __device__ __forceinline__ float tanh_exp(float y) {
@@ -666,9 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < kCols; c += 2)
                 f2_unpack(f2_mul(tanh_series13(f2_mul(f2_pack(s[c], s[c + 1]), ys)), cl), s[c], s[c + 1]);
             } else {
+              // |y| < 0.125: the series through y^5 (the first omitted term,
+              // 17 y^7 / 315, is below 3e-7 of y there), with y_scale and
+              // cap_log2 folded into its coefficients: a polynomial in the
+              // raw score s and u = s^2
+              const uint64_t k1 = f2_pack(p.c1, p.c1), k3 = f2_pack(p.c3, p.c3), k5 = f2_pack(p.c5, p.c5);
 #pragma unroll
-              for (int c = 0; c < kCols; c += 2)
-                f2_unpack(f2_mul(tanh_series5(f2_mul(f2_pack(s[c], s[c + 1]), ys)), cl), s[c], s[c + 1]);
+              for (int c = 0; c < kCols; c += 2) {
+                const uint64_t x = f2_pack(s[c], s[c + 1]);
+                const uint64_t u = f2_mul(x, x);
+                f2_unpack(f2_mul(x, f2_fma(u, f2_fma(u, k5, k3), k1)), s[c], s[c + 1]);
+              }
             }
           } else {
 #pragma unroll
@@ -975,6 +977,13 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   p.scale_log2 = a.scale * kLog2e;
   p.y_scale = (a.softcap > 0.0f) ? a.scale / a.softcap : 0.0f;
   p.cap_log2 = a.softcap * kLog2e;
+  {
+    const double ys = (a.softcap > 0.0f) ? static_cast<double>(a.scale) / a.softcap : 0.0;
+    const double cl = static_cast<double>(a.softcap) * 1.4426950408889634;
+    p.c1 = static_cast<float>(cl * ys);
+    p.c3 = static_cast<float>(-cl * ys * ys * ys / 3.0);
+    p.c5 = static_cast<float>(2.0 * cl * ys * ys * ys * ys * ys / 15.0);
+  }
   if (a.flags & FA_MOD_ALIBI)
     for (int h = 0; h < g.heads_q; ++h) p.slopes[h] = a.slopes[h];
   auto kern = k_fwd<D, MODS, HALVES>;
