@@ -342,30 +342,38 @@ def main():
     h2d = sum(t.numel() * t.element_size() for t in hq) + hmask.numel() * hmask.element_size()
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
-    # Host->device copies go on two side streams (two copy engines) once the
-    # previous forward has read the inputs; the device->host copies of O and
-    # LSE go on a third, overlapping the next step's inputs.
+    # Two device copies of the inputs and outputs, used in turn: a step's
+    # host->device copies (two side streams) run while the previous step's
+    # plan and forward use the other copy, once the forward two steps back
+    # has read this one; O and LSE leave on a third stream.
+    dps = [dp, runner.to_device(w)]
     s_in = [torch.cuda.Stream(), torch.cuda.Stream()]
     s_out = torch.cuda.Stream()
-    fwd_done, out_done = torch.cuda.Event(), torch.cuda.Event()
-    out_done.record(stream)
+    used = [torch.cuda.Event(), torch.cuda.Event()]  # the last forward on copy i has finished
+    outd = [torch.cuda.Event(), torch.cuda.Event()]  # copy i's O/LSE have reached the host
+    for ev in used + outd:
+        ev.record(stream)
+    n_e2e = [0]
 
     def e2e_step():
-        for i, (dst, src) in enumerate(zip((dp.q, dp.k, dp.v, dp.mask), (*hq, hmask))):
-            s_in[i % 2].wait_stream(stream)  # the previous forward has read the inputs
-            with torch.cuda.stream(s_in[i % 2]):
+        i = n_e2e[0] % 2
+        n_e2e[0] += 1
+        b = dps[i]
+        for j, (dst, src) in enumerate(zip((b.q, b.k, b.v, b.mask), (*hq, hmask))):
+            s_in[j % 2].wait_event(used[i])
+            with torch.cuda.stream(s_in[j % 2]):
                 dst.copy_(src, non_blocking=True)
         for si in s_in:
             stream.wait_stream(si)
-        stream.wait_event(out_done)  # the previous O/LSE have left the device
-        p = runner.build_plan(dp)
-        runner.forward(dp, p)
-        fwd_done.record(stream)
-        s_out.wait_event(fwd_done)
+        stream.wait_event(outd[i])  # this copy's previous O/LSE have left the device
+        p = runner.build_plan(b)
+        runner.forward(b, p)
+        used[i].record(stream)
+        s_out.wait_event(used[i])
         with torch.cuda.stream(s_out):
-            ho.copy_(dp.o, non_blocking=True)
-            hl.copy_(dp.lse, non_blocking=True)
-        out_done.record(s_out)
+            ho.copy_(b.o, non_blocking=True)
+            hl.copy_(b.lse, non_blocking=True)
+        outd[i].record(s_out)
         p.free()
 
     for _ in range(3):

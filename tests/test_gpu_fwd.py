@@ -132,6 +132,35 @@ def test_block_mask_64_blocks_all_rows(d, mods):
     plan.free()
 
 
+def test_heads_at_limit_with_alibi():
+    # 256 Q heads (the largest count the forward's parameters hold slopes
+    # for) sharing 8 K/V heads, per-head masks, ALiBi slope per head
+    w = _random_problem(31, B=1, S=130, H=256, Hk=8, d=64, nfunc=3, Hmask=256, alibi=True)
+    dp, plan = run(w)
+    rows = {(0, h): list(range(0, 130, 7)) + [127, 128, 129] for h in range(0, 256, 5)}
+    PT.check_rows(w, dp.o, dp.lse, rows)
+    plan.free()
+
+
+@pytest.mark.parametrize("mods", [False, True])
+def test_block_mask_unequal_lengths(mods):
+    # Sq != Sk with ragged last tiles on both axes: one-half tiles of the
+    # last K tile pair with others, rows past Sq stay out of the output
+    B, Sq, Sk, H, blk, d = 2, 700, 1100, 2, 64, 128
+    gen = torch.Generator().manual_seed(33)
+    q = torch.randn(B, Sq, H, d, generator=gen).bfloat16()
+    k, v = (torch.randn(B, Sk, H, d, generator=gen).bfloat16() for _ in range(2))
+    bm = W.random_block_mask(33, H, -(-Sq // blk), -(-Sk // blk), 0.15, diagonal=False)
+    w = W.Workload("blk_qk", W.LAYOUT_BSHD, B, Sq, Sk, H, H, d, q, k, v, 1 / math.sqrt(d), "blocks",
+                   block_mask=bm, block_q=blk, block_kv=blk)
+    if mods:
+        w.softcap = 30.0
+        w.alibi_slopes = W.alibi_slopes(H)
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
 def test_rows_without_visible_keys():
     w = _random_problem(10, B=1, S=300, H=2, d=64, nfunc=3)
     w.mask_func[:] = 0               # nothing visible anywhere
