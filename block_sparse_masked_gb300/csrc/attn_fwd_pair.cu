@@ -15,13 +15,15 @@
 // Used for interval-mask plans without score mods (with mods the softmax is
 // the bound and attn_fwd.cu, two warpgroups per tile, runs it faster).
 //
-// 320 threads, warp-specialised:
+// Tasks come from cluster launch control as in attn_fwd.cu (one CTA per
+// work_desc entry; a running CTA takes over entries of CTAs that have not
+// started).  352 threads, warp-specialised:
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread r owns
 //               score row r (TMEM lane r) and all 128 key columns, so the row
 //               max and sum stay in the thread.  Each group walks its own
 //               tiles (a merge of its partial and full lists) in the same
 //               ascending order.
-//   warp 8      producer (lane 0): claims tasks, loads the two Q tiles, and
+//   warp 8      producer (lane 0): takes tasks, loads the two Q tiles, and
 //               K(u), V(u-1) of every union tile u into one ring, tagging each
 //               K slot with the tiles that use it.
 //   warp 9      TMEM allocator and issuer of the Q K^T MMAs (lane 0).
