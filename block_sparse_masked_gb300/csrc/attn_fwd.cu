@@ -686,7 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (partial && !dead) {
+        // (a warp whose rows see every one of its 64 columns skips it)
+        if (partial && !dead && !__all_sync(0xffffffffu, (pw.x & pw.y) == ~0u)) {
 #pragma unroll
           for (int c = 0; c < kCols; ++c)
             if (!((((c < 32) ? pw.x : pw.y) >> (c & 31)) & 1u)) s[c] = -INFINITY;
