@@ -229,3 +229,34 @@ def test_brute_force_triple_loop():
         for t in range(d):
             ref = sum(p * v[j, t] for j, p in w_) / tot
             assert math.isclose(o[i, t], ref, abs_tol=1e-12)
+
+
+def test_gqa_heads_and_per_head_masks_equal_sdpa():
+    """Q head h reads K/V head h // (Hq / Hk) and, with one mask per Q head,
+    its own intervals: per-head sliding windows of different widths, checked
+    against fp64 SDPA on explicitly selected K/V heads (a mapping by h % Hk,
+    or every head reading mask 0, fails)."""
+    B, S, Hq, Hk, d = 2, 40, 6, 2, 8
+    gen = torch.Generator().manual_seed(23)
+    q = torch.randn(B, S, Hq, d, generator=gen).bfloat16()
+    k = torch.randn(B, S, Hk, d, generator=gen).bfloat16()
+    v = torch.randn(B, S, Hk, d, generator=gen).bfloat16()
+    qi = np.arange(S)
+    wins = [3 + 4 * h for h in range(Hq)]
+    mf = np.zeros((Hq, 3, B * S), np.int32)
+    for h, win in enumerate(wins):
+        lo = np.maximum(0, qi + 1 - win)
+        mf[h, 1] = np.tile(lo, B)                # [0,0) U [lo, q+1)
+        mf[h, 2] = np.tile(qi + 1, B)
+    w = W.Workload("gqa", W.LAYOUT_BSHD, B, S, S, Hq, Hk, d, q, k, v, 0.3, "intervals",
+                   mask_func=mf)
+    kk = np.arange(S)
+    for b in range(B):
+        for h in range(Hq):
+            o, lse = A.attention_rows(w, b, h)
+            vis = (kk[None, :] <= qi[:, None]) & (kk[None, :] >= qi[:, None] + 1 - wins[h])
+            qh = q[b, :, h].double().numpy()
+            kh = k[b, :, h // (Hq // Hk)].double().numpy()
+            vh = v[b, :, h // (Hq // Hk)].double().numpy()
+            assert np.allclose(o, _sdpa(qh, kh, vh, bool_mask=vis, scale=0.3), atol=1e-12)
+            assert np.allclose(lse, _lse_ref(qh, kh, vis, 0.3), atol=1e-12)
