@@ -12,6 +12,7 @@ from block_sparse_masked_gb300 import runner
 from block_sparse_masked_gb300 import workloads as W
 
 import parity as PT
+from oracle import plan as OP
 
 pytestmark = pytest.mark.gpu
 
@@ -158,6 +159,32 @@ def test_block_mask_unequal_lengths(mods):
         w.alibi_slopes = W.alibi_slopes(H)
     dp, plan = run(w)
     PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+@pytest.mark.parametrize("d,mods", [(64, False), (128, False), (128, True)])
+def test_varlen_unequal_q_and_k_lengths(d, mods):
+    # THD samples whose Q and K lengths differ (cu_seqlens_q != cu_seqlens_k),
+    # including a sample with no keys and one with no queries; GQA; the plan
+    # is compared bit-exactly and every row's output
+    lq, lk = np.array([70, 300, 1, 129, 0, 260]), np.array([200, 300, 517, 0, 64, 130])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    H, Hk = 4, 2
+    gen = torch.Generator().manual_seed(41)
+    q = torch.randn(int(lq.sum()), H, d, generator=gen).bfloat16()
+    k = torch.randn(int(lk.sum()), Hk, d, generator=gen).bfloat16()
+    v = torch.randn(int(lk.sum()), Hk, d, generator=gen).bfloat16()
+    mf = W.random_intervals(41, len(lq), 0, 0, 3, 1, lens_q=lq, lens_k=lk)
+    w = W.Workload("vqk", W.LAYOUT_THD, len(lq), int(lq.max()), int(lk.max()), H, Hk, d, q, k, v,
+                   1 / math.sqrt(d), "intervals", mask_func=mf, cu_seqlens_q=cq, cu_seqlens_k=ck)
+    if mods:
+        w.softcap = 20.0
+        w.alibi_slopes = W.alibi_slopes(H)
+    dp, plan = run(w)
+    PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w))
+    rows = {(b, h): list(range(int(lq[b]))) for b in range(len(lq)) for h in range(H) if lq[b] > 0}
+    PT.check_rows(w, dp.o, dp.lse, rows)
     plan.free()
 
 

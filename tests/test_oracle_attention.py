@@ -260,3 +260,32 @@ def test_gqa_heads_and_per_head_masks_equal_sdpa():
             vh = v[b, :, h // (Hq // Hk)].double().numpy()
             assert np.allclose(o, _sdpa(qh, kh, vh, bool_mask=vis, scale=0.3), atol=1e-12)
             assert np.allclose(lse, _lse_ref(qh, kh, vis, 0.3), atol=1e-12)
+
+
+def test_varlen_unequal_q_and_k_lengths_equal_sdpa():
+    """THD samples whose Q and K lengths differ (cu_seqlens_q != cu_seqlens_k):
+    sample b's rows read keys [cu_k[b], cu_k[b+1]) with sample-local
+    positions; a mask that ends every row's keys at q + 1 + (k_len - q_len)
+    (queries aligned to the end of their keys) is checked against fp64 SDPA
+    on explicitly sliced keys."""
+    lq, lk = np.array([5, 17, 1, 9]), np.array([12, 17, 30, 9])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    H, d = 2, 8
+    gen = torch.Generator().manual_seed(29)
+    q = torch.randn(int(lq.sum()), H, d, generator=gen).bfloat16()
+    k = torch.randn(int(lk.sum()), H, d, generator=gen).bfloat16()
+    v = torch.randn(int(lk.sum()), H, d, generator=gen).bfloat16()
+    F0 = np.concatenate([np.arange(n) + 1 + (m - n) for n, m in zip(lq, lk)]).astype(np.int32)
+    w = W.Workload("varlen_qk", W.LAYOUT_THD, len(lq), int(lq.max()), int(lk.max()), H, H, d, q, k, v,
+                   0.35, "intervals", mask_func=F0[None, None, :], cu_seqlens_q=cq, cu_seqlens_k=ck)
+    for b in range(len(lq)):
+        n, m = int(lq[b]), int(lk[b])
+        vis = np.arange(m)[None, :] < (np.arange(n) + 1 + (m - n))[:, None]
+        for h in range(H):
+            o, lse = A.attention_rows(w, b, h)
+            qh = q[cq[b]:cq[b + 1], h].double().numpy()
+            kh = k[ck[b]:ck[b + 1], h].double().numpy()
+            vh = v[ck[b]:ck[b + 1], h].double().numpy()
+            assert np.allclose(o, _sdpa(qh, kh, vh, bool_mask=vis, scale=0.35), atol=1e-12)
+            assert np.allclose(lse, _lse_ref(qh, kh, vis, 0.35), atol=1e-12)
