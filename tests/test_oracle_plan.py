@@ -224,3 +224,34 @@ def test_sequence_desc_and_workload_shapes():
     assert p.sequence_desc.tolist() == [[0, 0, 256, 256, 0, 2, 2, 0]]
     assert p.partial_idx.tolist() == [0, 1] and p.full_idx.tolist() == [0]
     assert p.visible_pairs == 256 * 257 // 2
+
+
+def test_plan_unequal_q_and_k_lengths():
+    """THD with cu_seqlens_q != cu_seqlens_k (a sample without keys, one
+    without queries): the plan equals the per-element brute force, its tiles
+    reproduce the dense visibility, and K tiles count from each sample's keys."""
+    import torch
+    lq, lk = np.array([70, 150, 1, 129, 0, 60]), np.array([200, 150, 300, 0, 64, 130])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    mf = W.random_intervals(17, len(lq), 0, 0, 3, 2, lens_q=lq, lens_k=lk)
+    zq = torch.zeros(int(lq.sum()), 2, 8, dtype=torch.bfloat16)
+    zk = torch.zeros(int(lk.sum()), 2, 8, dtype=torch.bfloat16)
+    w = W.Workload("vqk", W.LAYOUT_THD, len(lq), int(lq.max()), int(lk.max()), 2, 2, 8, zq, zk, zk,
+                   1.0, "intervals", mask_func=mf, cu_seqlens_q=cq, cu_seqlens_k=ck)
+    for T in ((64, 64), (128, 128)):
+        p = P.build_plan(w, *T)
+        ref = _brute_plan(w, *T)
+        for hm in range(2):
+            for r in range(p.rows):
+                b, m = int(p.row_batch[r]), int(p.row_mblock[r])
+                plist, flist, pays = ref[(hm, b, m)]
+                f = hm * p.rows + r
+                assert p.partial_idx[p.partial_offset[f]:p.partial_offset[f + 1]].tolist() == plist
+                assert p.full_idx[p.full_offset[f]:p.full_offset[f + 1]].tolist() == flist
+                assert p.payload[p.partial_offset[f]:p.partial_offset[f + 1]].tolist() == pays
+            for b in range(len(lq)):
+                vis = M.visible_rows(w, hm, b, np.arange(lq[b]))
+                assert np.array_equal(P.visible_from_plan(p, hm, b, int(lq[b]), int(lk[b])), vis)
+        assert p.rows == sum(-(-int(n) // T[0]) for n in lq)
+        assert [int(x) for x in p.sequence_desc[:, 6]] == [-(-int(m) // T[1]) for m in lk]
