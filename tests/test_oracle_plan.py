@@ -255,3 +255,95 @@ def test_plan_unequal_q_and_k_lengths():
                 assert np.array_equal(P.visible_from_plan(p, hm, b, int(lq[b]), int(lk[b])), vis)
         assert p.rows == sum(-(-int(n) // T[0]) for n in lq)
         assert [int(x) for x in p.sequence_desc[:, 6]] == [-(-int(m) // T[1]) for m in lk]
+
+
+def _small_block_workload(H, S, BQ, BKV, seed, density=0.25):
+    import torch
+    nbq, nbk = -(-S // BQ), -(-S // BKV)
+    bm = W.random_block_mask(seed, H, nbq, nbk, density)
+    z = torch.zeros(1, S, H, 0, dtype=torch.bfloat16)
+    return W.Workload("blk", W.LAYOUT_BSHD, 1, S, S, H, H, 8, z, z, z, 1.0, "blocks",
+                      block_mask=bm, block_q=BQ, block_kv=BKV)
+
+
+def _assert_same_plan(a, b):
+    for f in ("rows", "Hmask", "visible_pairs"):
+        assert getattr(a, f) == getattr(b, f), f
+    for f in ("cu_q_rows", "k_tiles", "row_batch", "row_mblock", "row_qvalid", "partial_count",
+              "full_count", "partial_offset", "full_offset", "partial_idx", "full_idx", "payload",
+              "halves", "sequence_desc", "work_desc"):
+        x, y = getattr(a, f), getattr(b, f)
+        assert x.shape == y.shape and np.array_equal(x, y), f
+
+
+@pytest.mark.parametrize("kind", ["blocks", "intervals"])
+def test_plan_by_heads_equals_single_process_plan(kind):
+    """The per-head merge used for the large block-sparse plan gives, array
+    for array, the plan built in one pass: the CSR of "Flex Attention Mask
+    Plan Design" §4.6 is row-major over (mask head, row), so per-head parts
+    concatenated in head order must reproduce offsets, lists, payloads and
+    halves, and the §4.8 schedule built from the merged counts is the same."""
+    if kind == "blocks":
+        w = _small_block_workload(3, 333, 64, 64, seed=5)
+    else:
+        w = _tiny_interval_workload(seed=31, B=0, S=0, nfunc=3, Hmask=3, H=3,
+                                    varlen_lens=[260, 1, 129, 75])
+    one = P.build_plan(w)
+    merged = P.build_plan_by_heads(w.mask_only(), processes=2)
+    _assert_same_plan(one, merged)
+    # and it is not a trivial match: the heads differ from one another
+    assert one.partial_count[0].tolist() != one.partial_count[1].tolist() or \
+        one.partial_idx.size != 0
+
+
+def _gqa_workload(Hmask):
+    import torch
+    lens = np.array([300, 40, 520, 129])
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tot = int(lens.sum())
+    mf = W.random_intervals(23, len(lens), 0, 0, 3, Hmask, lens_q=lens, lens_k=lens)
+    zq = torch.zeros(tot, 4, 0, dtype=torch.bfloat16)
+    zk = torch.zeros(tot, 2, 0, dtype=torch.bfloat16)
+    return W.Workload("gqa", W.LAYOUT_THD, len(lens), int(lens.max()), int(lens.max()), 4, 2, 8,
+                      zq, zk, zk, 1.0, "intervals", mask_func=mf, cu_seqlens_q=cu,
+                      cu_seqlens_k=cu.copy())
+
+
+@pytest.mark.parametrize("Hmask", [1, 4])
+def test_schedule_gqa_sections(Hmask):
+    """§4.8 order with grouped-query heads (Hq=4, Hk=2): the L2 section of a
+    task is (sample, K/V head) and Q heads 2g and 2g+1 share K/V head g, so
+    they must be interleaved by cost inside one section; a `sample*Hq + head`
+    section would split them.  The expected order is built here by explicit
+    grouping: sections in (sample, K/V head) order, inside each the positive
+    cost tasks by descending cost with ties in (head, m_block) order, then all
+    zero-cost tasks in (sample, head, m_block) order."""
+    w = _gqa_workload(Hmask)
+    p = P.build_plan(w, 128, 128)
+    Hq, Hk = 4, 2
+    cost = {}
+    for r in range(p.rows):
+        b, m = int(p.row_batch[r]), int(p.row_mblock[r])
+        for h in range(Hq):
+            hm = 0 if Hmask == 1 else h
+            cost[(b, h, m)] = (int(p.partial_count[hm, r] + p.full_count[hm, r]), int(p.row_qvalid[r]))
+    want = []
+    for b in range(w.B):
+        for g in range(Hk):
+            sect = [(c, h, m, qv) for (bb, h, m), (c, qv) in cost.items()
+                    if bb == b and h // (Hq // Hk) == g and c > 0]
+            by_cost = {}
+            for c, h, m, qv in sect:
+                by_cost.setdefault(c, []).append((h, m, qv))
+            for c in sorted(by_cost, reverse=True):
+                for h, m, qv in sorted(by_cost[c]):
+                    want.append((m, h, b, qv))
+    zero = sorted((b, h, m, qv) for (b, h, m), (c, qv) in cost.items() if c == 0)
+    want += [(m, h, b, qv) for (b, h, m, qv) in zero]
+    got = [tuple(x) for x in p.work_desc.tolist()]
+    assert got == want
+    # both Q heads of a group appear inside one section run
+    first = got[:sum(1 for v in cost.values() if v[0] > 0)]
+    secs = [(b, h // 2) for (m, h, b, qv) in first]
+    assert secs == sorted(secs)
+    assert any(h % 2 == 1 for (m, h, b, qv) in first) and any(h % 2 == 0 for (m, h, b, qv) in first)
