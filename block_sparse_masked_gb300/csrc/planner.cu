@@ -909,10 +909,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 namespace bsm {
 namespace {
 
-// Device address of g_noalloc_scratch for device `dev`, looked up once per
-// device (with that device current) and cached.  In host code the symbol
-// itself is only a host-side stand-in, so kernels must get this address.
-void* noalloc_scratch_address(int dev, cudaError_t* err) {
+// Device address of g_noalloc_scratch for device `dev` (current).  In host
+// code the symbol itself is only a host-side stand-in, so kernels must get
+// this address.  Outside stream capture it is looked up on every call (a
+// cheap host-side query), so that a device reset or another context on the
+// device is picked up; during capture, where the lookup might have to load
+// the module, the address from the last call outside capture is used.
+void* noalloc_scratch_address(int dev, cudaStream_t st, cudaError_t* err) {
   static std::mutex mu;
   static void* addr[128] = {};
   *err = cudaSuccess;
@@ -920,8 +923,10 @@ void* noalloc_scratch_address(int dev, cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lk(mu);
-  if (!addr[dev]) {
+  if (!capturing || !addr[dev]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) {
@@ -973,7 +978,7 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return report_error(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address(dev, &e));
+  uint8_t* base = static_cast<uint8_t*>(noalloc_scratch_address(dev, static_cast<cudaStream_t>(stream), &e));
   if (!base) return report_error(FA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
   PlanWorkspace ws{};
   ws.ctl = reinterpret_cast<unsigned*>(base + off[0]);

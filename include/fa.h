@@ -138,9 +138,12 @@ int fa_plan_build_blocks(const fa_geometry* geom, const uint8_t* block_mask, int
                          void* stream, fa_plan** out);
 
 /*
- * Release a plan.  NULL is accepted.  Device memory is returned in stream
- * order on `stream`: the caller must make sure no work that reads the plan
- * is still pending on any other stream.
+ * Release a plan ("Flex Attention Mask Plan Design" §8 Ownership: the plan
+ * owns every buffer it holds, including its cu_seqlens clones, and releases
+ * them itself).  NULL is accepted.  Device memory is returned in stream
+ * order on `stream` (through the plan's allocator when one was given): the
+ * caller must make sure no work that reads the plan is still pending on any
+ * other stream.
  */
 int fa_plan_free(fa_plan* plan, void* stream);
 
@@ -267,7 +270,10 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * scratch (about 8 bytes per (mask head, Q tile, 32 K tiles) plus small
  * per-sample arrays) exceeds 4 MiB are rejected with FA_ERR_UNSUPPORTED.
  * The first call on each device looks up the array's device address; make
- * that first call before any stream capture.  All calls on a device share
+ * that first call before any stream capture.  Later calls outside capture
+ * look it up again (so a cudaDeviceReset or a new context on the device is
+ * picked up); calls during capture reuse the address of the last call made
+ * outside capture on that device.  All calls on a device share
  * the array and it keeps the previous call's contents (the call clears what
  * must start at zero), so calls whose GPU work overlaps (e.g. on unordered
  * streams) race on it and give wrong results: order them.

@@ -36,10 +36,21 @@ def _cases():
     z = torch.zeros(tot, 2, 0, dtype=torch.bfloat16)
     out.append(W.Workload("fuzz", W.LAYOUT_THD, len(lens), 300, 300, 2, 2, 64, z, z, z, 1.0,
                           "intervals", mask_func=mf, cu_seqlens_q=cu, cu_seqlens_k=cu.copy()))
+    # per-sample Q and K lengths that differ, with a sample without keys and
+    # one without queries
+    lq, lk = np.array([70, 150, 1, 129, 0, 60]), np.array([200, 150, 300, 0, 64, 130])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    mf = W.random_intervals(17, len(lq), 0, 0, 3, 2, lens_q=lq, lens_k=lk)
+    zq = torch.zeros(int(lq.sum()), 2, 0, dtype=torch.bfloat16)
+    zk = torch.zeros(int(lk.sum()), 2, 0, dtype=torch.bfloat16)
+    out.append(W.Workload("vqk", W.LAYOUT_THD, len(lq), int(lq.max()), int(lk.max()), 2, 2, 64,
+                          zq, zk, zk, 1.0, "intervals", mask_func=mf, cu_seqlens_q=cq,
+                          cu_seqlens_k=ck))
     return out
 
 
-@pytest.mark.parametrize("case", range(4))
+@pytest.mark.parametrize("case", range(5))
 def test_noalloc_header_matches_allocating_build(case):
     w = _cases()[case]
     if w.d == 0:
