@@ -5,8 +5,11 @@ One step = one pass of the whole path over one batch: plan build from the
 mask (host checks, GPU planner, one header readback, exact allocation,
 CSR + payload + schedule) followed by the masked forward.  Metric: TFLOPS on
 visible (q, k) pairs (4 * d FLOPs per visible pair), per step, with the plan
-build time reported beside it.  Default workload: sliding window (1024) +
-4-key sink, B=4, H=16, S=4096, d=128, bf16.
+build time reported beside it.  Default workload: the largest single-GPU
+configuration, video-style block-sparse attention (B=1, H=24, S=32768,
+d=128, 64x64 logical blocks active at 10% plus the diagonal, bf16).  The same
+line carries `per_config`: forward time, TFLOPS on visible pairs, roofline
+fraction and plan build time for each of the five workloads.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle
 instead, on bounded samples of the same workload, on the host cores.
@@ -46,7 +49,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="sliding_sink", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--workload", default="video_block_sparse", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload table (the headline workload only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
@@ -173,6 +178,102 @@ def visible_flops(info: dict, Hq: int, d: int) -> float:
     return 4.0 * d * vp * heads
 
 
+def algorithmic_bytes(w, info: dict) -> float:
+    """Bytes one forward launch must move at least once: Q, K, V read, O and
+    LSE written, and the plan it reads (CSR offsets and lists, task list and
+    the packed predicate payload of the partial entries)."""
+    qkv = sum(t.numel() * t.element_size() for t in (w.q, w.k, w.v))
+    o = w.q.numel() * w.q.element_size()
+    lse = 4 * w.Hq * w.total_q
+    hdr = info["header"]
+    plan_meta = 4 * (2 * (info["mask_heads"] * hdr[0] + 1) + hdr[1] + hdr[2]) + 16 * info["num_tasks"]
+    return float(qkv + o + lse + plan_meta + info["payload_bytes"])
+
+
+def roofline(flops: float, alg_bytes: float, ms: float, peaks: dict, peak_src: str, traffic):
+    """The bound of one launch: tensor (visible FLOPs at the bf16 peak) or HBM
+    (algorithmic bytes at the copy bandwidth), whichever takes longer at its
+    peak; the fraction is the achieved rate of that resource over its peak."""
+    tflops_peak = float(peaks["bf16_tflops"])
+    gbs_peak = float(peaks["hbm_gbs"])
+    t_tensor = flops / (tflops_peak * 1e12)
+    t_hbm = alg_bytes / (gbs_peak * 1e9)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    if t_tensor >= t_hbm:
+        r = {"bound": "tensor", "achieved": tflops, "peak": tflops_peak, "unit": "TFLOP/s",
+             "frac": tflops / tflops_peak,
+             "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone per event pair)"}
+    else:
+        r = {"bound": "hbm", "achieved": gbs, "peak": gbs_peak, "unit": "GB/s", "frac": gbs / gbs_peak,
+             "peak_source": f"{peak_src} HBM copy bandwidth"}
+    r.update({"traffic": traffic, "alg_bytes": alg_bytes, "tflops": tflops, "alg_gbs": gbs,
+              "t_tensor_ms_at_peak": t_tensor * 1e3, "t_hbm_ms_at_peak": t_hbm * 1e3})
+    return r
+
+
+def time_forward_alone(runner, dp, plan, flush, stream, reps: int):
+    """Event pairs around each forward launch; L2 flushed first, and a queued
+    sleep keeps the host ahead so that the pair brackets the launch itself."""
+    import torch
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for i in range(reps):
+        flush.zero_()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        kev[i][0].record(stream)
+        runner.forward(dp, plan)
+        kev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in kev]
+
+
+def time_plan_builds(fa, runner, dp, flush, stream, reps: int):
+    """Host microseconds of each build (the call, including its one header
+    read-back) and stream milliseconds until its last planner kernel ends."""
+    import torch
+    host_us, gpu_ms = [], []
+    for _ in range(reps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        p = runner.build_plan(dp)
+        e1.record(stream)
+        host_us.append(fa.fa_plan_info_get(p)["build_us"])
+        torch.cuda.synchronize()
+        gpu_ms.append(e0.elapsed_time(e1))
+        p.free()
+    return statistics.median(host_us), statistics.median(gpu_ms)
+
+
+def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, seed: int):
+    """Forward alone, plan build and roofline of every workload (one seed)."""
+    import torch
+    out = {}
+    for name in WORKLOAD_DESC:
+        w = W.make(name, seed)
+        dp = runner.to_device(w)
+        plan = runner.build_plan(dp)
+        info = fa.fa_plan_info_get(plan, count_visible=True)
+        flops = visible_flops(info, w.Hq, w.d)
+        for _ in range(3):
+            runner.forward(dp, plan)
+        torch.cuda.synchronize()
+        ms = statistics.mean(time_forward_alone(runner, dp, plan, flush, stream, reps))
+        plan.free()
+        b_us, b_ms = time_plan_builds(fa, runner, dp, flush, stream, max(10, reps // 2))
+        rf = roofline(flops, algorithmic_bytes(w, info), ms, peaks, peak_src, known_traffic(name))
+        out[name] = {"workload": WORKLOAD_DESC[name], "fwd_ms": ms, "tflops": rf["tflops"],
+                     "frac_bf16_peak": rf["tflops"] / float(peaks["bf16_tflops"]),
+                     "bound": rf["bound"], "frac": rf["frac"], "alg_bytes": rf["alg_bytes"],
+                     "traffic": rf["traffic"], "plan_build_us": b_us, "plan_gpu_ms": b_ms,
+                     "visible_pairs": info["visible_pairs"] * (w.Hq if info["mask_heads"] == 1 else 1),
+                     "kernel": fwd_kernel_name(w)}
+        del dp, plan, w
+        torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline(w, budget_s: float):
     """Oracle (fp64, numpy) attention on a bounded sample of rows, visible TFLOPS."""
     import numpy as np
@@ -206,6 +307,13 @@ def cpu_baseline(w, budget_s: float):
                       f"{rows_done} rows, all visible keys, fp64 numpy, {dt:.1f} s"}
 
 
+def workload_config(args) -> dict:
+    """The `config` object of both arms: which workload, seed and step."""
+    return {"workload": WORKLOAD_DESC[args.workload], "seed": args.seed,
+            "step": "plan build + masked forward",
+            "l2": "256 MB buffer written between timed steps"}
+
+
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
@@ -227,7 +335,9 @@ def run_reference(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "l2": "n/a (CPU)"},
+        "config": workload_config(args),
+        "reference_timing": "fp64 oracle on bounded samples of the workload on the host cores; "
+                            "no GPU, so the L2 flush of the config does not apply",
         "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
         "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -313,23 +423,12 @@ def main():
     ms_per_step = tot_ms / args.steps
     value = whole_job_tflops(flops_step, world, ms_per_step)
 
-    # The forward kernel alone, for the roofline: a queued sleep keeps the
-    # host ahead of the GPU, so each event pair brackets the launch itself
-    # (in the step above the GPU can wait for the host between plan and
-    # forward).  L2 is flushed before every launch.
+    # The forward kernel alone, for the roofline (see time_forward_alone).
     plan_f = runner.build_plan(dp)
     torch.cuda.synchronize()
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()
-        torch.cuda._sleep(SLEEP_CYCLES)
-        kev[i][0].record(stream)
-        runner.forward(dp, plan_f)
-        kev[i][1].record(stream)
-    torch.cuda.synchronize()
+    fwd_ms = time_forward_alone(runner, dp, plan_f, flush, stream, args.steps)
     plan_f.free()
     clk = clocks.stop()
-    fwd_ms = [a.elapsed_time(b) for a, b in kev]
     fwd_mean = statistics.mean(fwd_ms)
     fwd_tflops = flops_step / (fwd_mean * 1e-3) / 1e12
 
@@ -392,34 +491,37 @@ def main():
     assert fa.fa_device_error_flags() == 0, "device error flags set"
 
     peaks, peak_src = load_peaks()
-    peak = float(peaks["bf16_tflops"])
-    traffic = known_traffic(args.workload)
+    rf = roofline(flops_step, algorithmic_bytes(w, info), fwd_mean, peaks, peak_src,
+                  known_traffic(args.workload))
+    rf.update({"timing": "forward launch between two events queued behind a sleep kernel, "
+                         "L2 flushed before each launch",
+               "kernel": fwd_kernel_name(w)})
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "seed": args.seed,
-                   "step": "plan build + masked forward",
-                   "l2": "256 MB buffer written between timed steps; inputs 201 MB > L2"
-                   if args.workload == "sliding_sink" else "256 MB buffer written between timed steps"},
+        "config": workload_config(args),
         "plan_build_us": statistics.median(build_us),
         "plan_gpu_ms": statistics.median(plan_ms),
         "fwd_ms": fwd_mean,
         "fwd_ms_in_step": statistics.mean(fwd_in_step_ms),
         "fwd_tflops": fwd_tflops,
         "visible_pairs": info["visible_pairs"] * (w.Hq if info["mask_heads"] == 1 else 1),
-        "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": fwd_tflops / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 dense burst (kernel timed alone per event pair)",
-                     "timing": "forward launch between two events queued behind a sleep kernel, "
-                               "L2 flushed before each launch",
-                     "kernel": fwd_kernel_name(w)},
+        "roofline": rf,
         "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "note": "host->device input copies (pinned, ~0.2 TB/s on this machine) bound this number"},
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
         "wall_s_timed": t_wall,
     }
+    if not args.no_per_config:
+        clocks2 = ClockSampler(local)
+        clocks2.start()
+        pc = per_config_table(fa, runner, W, flush, stream, peaks, peak_src, max(10, args.steps // 2),
+                              args.seed + rank)
+        line["per_config"] = pc
+        line["per_config_clocks"] = clocks2.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:

@@ -76,7 +76,7 @@ class FaPlanInfo(_c.Structure):
 class FaPlanHostView(_c.Structure):
     _fields_ = [("cu_q_rows", _vp), ("sequence_desc", _vp), ("partial_offset", _vp),
                 ("partial_idx", _vp), ("full_offset", _vp), ("full_idx", _vp), ("payload", _vp),
-                ("work_desc", _vp), ("halves", _vp)]
+                ("work_desc", _vp), ("halves", _vp), ("quads", _vp)]
 
 
 class FaError(RuntimeError):
@@ -172,8 +172,9 @@ def geometry(layout: int, batch: int, seqlen_q: int, seqlen_k: int, heads_q: int
 class Plan:
     """Owner of an fa_plan* handle."""
 
-    def __init__(self, handle: int):
+    def __init__(self, handle: int, allocator=None):
         self.handle = handle
+        self.allocator = allocator  # frees the plan's memory: keep it alive with the plan
 
     def free(self, stream=None):
         if self.handle:
@@ -188,20 +189,42 @@ class Plan:
             pass
 
 
+_ALLOC_FN = _c.CFUNCTYPE(_vp, _c.c_size_t, _vp, _vp)
+_FREE_FN = _c.CFUNCTYPE(None, _vp, _c.c_size_t, _vp, _vp)
+
+
+class Allocator:
+    """A caller allocator for plan and workspace memory (the fa_allocator
+    struct): ``alloc(bytes, stream) -> device address or 0`` and
+    ``free(address, bytes, stream)``, both called in stream order.  A plan
+    built with it keeps a reference, because the plan frees through it."""
+
+    def __init__(self, alloc, free):
+        self._alloc = _ALLOC_FN(lambda n, st, ctx: alloc(int(n), st or 0) or None)
+        self._free = _FREE_FN(lambda ptr, n, st, ctx: free(int(ptr), int(n), st or 0))
+        self.struct = FaAllocator(_c.cast(self._alloc, _vp), _c.cast(self._free, _vp), None)
+
+
+def _alloc_arg(allocator: Optional[Allocator]):
+    return _c.byref(allocator.struct) if allocator is not None else None
+
+
 def fa_plan_build_intervals(geom: FaGeometry, mask_func, Hmask: int, nfunc: int,
-                            stream=None) -> Plan:
+                            stream=None, allocator: Optional[Allocator] = None) -> Plan:
     out = _vp()
-    _check(lib().fa_plan_build_intervals(_c.byref(geom), _ptr(mask_func), Hmask, nfunc, None,
-                                         _stream_handle(stream), _c.byref(out)))
-    return Plan(out.value)
+    _check(lib().fa_plan_build_intervals(_c.byref(geom), _ptr(mask_func), Hmask, nfunc,
+                                         _alloc_arg(allocator), _stream_handle(stream),
+                                         _c.byref(out)))
+    return Plan(out.value, allocator)
 
 
 def fa_plan_build_blocks(geom: FaGeometry, block_mask, Hmask: int, block_q: int, block_kv: int,
-                         stream=None) -> Plan:
+                         stream=None, allocator: Optional[Allocator] = None) -> Plan:
     out = _vp()
     _check(lib().fa_plan_build_blocks(_c.byref(geom), _ptr(block_mask), Hmask, block_q, block_kv,
-                                      None, _stream_handle(stream), _c.byref(out)))
-    return Plan(out.value)
+                                      _alloc_arg(allocator), _stream_handle(stream),
+                                      _c.byref(out)))
+    return Plan(out.value, allocator)
 
 
 def fa_plan_free(plan: Plan, stream=None):
@@ -251,6 +274,7 @@ def fa_plan_export(plan: Plan) -> dict:
         "payload": np.zeros((P, FA_TILE_Q, FA_PAYLOAD_WORDS), np.uint32),
         "work_desc": np.zeros((T, 4), np.int32),
         "halves": np.zeros(P, np.uint8),
+        "quads": np.zeros(P, np.uint8),
     }
     view = FaPlanHostView(*[a.ctypes.data if a.size else None for a in arrs.values()])
     _check(lib().fa_plan_export(plan.handle, _c.byref(view)))

@@ -338,7 +338,7 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
                q_pay = c2.take(16ull * bsm::kTile * plan->P), q_work = c2.take(16ull * plan->tasks),
                q_cq = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
                q_ck = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
-               q_er = c2.take(4ull * plan->P), q_hv = c2.take(plan->P);
+               q_er = c2.take(4ull * plan->P), q_hv = c2.take(plan->P), q_qd = c2.take(plan->P);
   uint8_t* pm = static_cast<uint8_t*>(al.get(c2.off));
   if (!pm) {
     delete plan;
@@ -360,6 +360,9 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   }
   plan->entry_row = reinterpret_cast<int32_t*>(pm + q_er);
   plan->halves = pm + q_hv;
+  plan->quads = pm + q_qd;
+  plan->block_q = margs.block_q;
+  plan->block_kv = margs.block_kv;
 
   // exact-size copies (the schedule included), CSR lists, payloads: one launch
   e = bsm::launch_back(g, margs, ws, plan, gi->cu_seqlens_q, gi->cu_seqlens_k, st);
@@ -550,6 +553,7 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst) {
       {dst->payload, plan->payload, 16ull * bsm::kTile * plan->P},
       {dst->work_desc, plan->work_desc, 16ull * plan->tasks},
       {dst->halves, plan->halves, static_cast<size_t>(plan->P)},
+      {dst->quads, plan->quads, static_cast<size_t>(plan->P)},
   };
   for (auto& it : items) {
     if (!it.d || it.n == 0) continue;

@@ -68,6 +68,9 @@ struct fa_plan {
   int32_t* cu_seqlens_k = nullptr;
   int32_t* entry_row = nullptr;     // [P] planner scratch kept with the plan: flat row of each entry
   uint8_t* halves = nullptr;        // [P] bit s: key columns 64s..64s+63 of the entry hold a visible element
+  // [P] quadrant (a, s) = rows 64a.. x key columns 64s..: bit 2a+s any element visible, bit 4+2a+s all
+  uint8_t* quads = nullptr;
+  int32_t block_q = 0, block_kv = 0;  // logical block geometry of a block-mask plan
 };
 
 namespace bsm {
@@ -136,6 +139,10 @@ cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** wh
 // two Q tiles per task sharing one K/V stream (attn_fwd_pair.cu; interval masks)
 cudaError_t launch_fwd_pair_d64(const FwdLaunch& a, cudaStream_t st, const char** why);
 cudaError_t launch_fwd_pair_d128(const FwdLaunch& a, cudaStream_t st, const char** why);
+// keys-major forward for block-mask plans with 64-aligned logical blocks,
+// d = 128, no score mods (attn_fwd_kt.cu)
+bool fwd_kt_applies(const FwdLaunch& a);
+cudaError_t launch_fwd_kt(const FwdLaunch& a, cudaStream_t st, const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
 

@@ -423,6 +423,7 @@ struct BackParams {
   int32_t* entry_row;  // [P]: flat (hm*rows + row) of each partial entry
   uint32_t* payload;   // [P*128*4]
   uint8_t* halves;     // [P] bit s: column half s of the entry has a visible element
+  uint8_t* quads;      // [P] bit 2a+s / 4+2a+s: quadrant (row half a, column half s) any / all visible
   int rows, rows_ub, nq_max, words;
   // intervals
   const int32_t* mask_func;
@@ -430,6 +431,27 @@ struct BackParams {
   // blocks
   const uint8_t* block_mask;
   int block_q, block_kv, nbq, nbk;
+};
+
+// Quadrant bits of one partial entry, per lane and then reduced over the
+// warp: quadrant (a, s) = tile rows 64a..64a+63 x columns 64s..64s+63;
+// `live` bit 2a+s: a visible element, `full` bit 2a+s: every element visible.
+struct QuadBits {
+  uint32_t live = 0u, full = 0xFu;
+  // add tile row (lane + 32 i)'s four payload words
+  __device__ __forceinline__ void add(int i, const uint32_t (&w)[kPayloadWords]) {
+    const int a = i >> 1;
+    const uint32_t l = ((w[0] | w[1]) ? 1u : 0u) | ((w[2] | w[3]) ? 2u : 0u);
+    const uint32_t f = (((w[0] & w[1]) == kFull) ? 1u : 0u) | (((w[2] & w[3]) == kFull) ? 2u : 0u);
+    live |= l << (2 * a);
+    full &= ~((f ^ 3u) << (2 * a));
+  }
+  __device__ __forceinline__ void reduce() {
+    live = __reduce_or_sync(kFull, live);
+    full = __reduce_and_sync(kFull, full);
+  }
+  __device__ __forceinline__ uint32_t halves() const { return ((live & 5u) ? 1u : 0u) | ((live & 10u) ? 2u : 0u); }
+  __device__ __forceinline__ uint32_t quads() const { return live | (full << 4); }
 };
 
 // Endpoints of the CTA's 128 Q rows kept in shared memory for the payload
@@ -452,15 +474,15 @@ __device__ __forceinline__ void add_columns(uint32_t (&w)[kPayloadWords], int c0
 // Interval payload of one partial entry (tile column j), one warp: lane l
 // forms the 4 words of rows l, l+32, l+64, l+96 from the row's intervals
 // [0, F0), [F1, F2), ... clipped to the tile and to k_len; rows past the
-// sample stay 0.  Returns the OR of the column-half bits over the rows.
-__device__ __forceinline__ uint32_t payload_intervals_entry(const BackParams& p, long long e, int j,
+// sample stay 0.  Returns this lane's quadrant bits (not yet reduced).
+__device__ __forceinline__ QuadBits payload_intervals_entry(const BackParams& p, long long e, int j,
                                                             int q_len, int k_len, int q0, int hm,
                                                             int q_off, const int32_t (*sF)[kTile],
                                                             bool smem) {
   const int lane = threadIdx.x & 31;
   const int c0 = j * kTile;
   const int32_t* Fg = p.mask_func + static_cast<long long>(hm) * p.nfunc * p.total_q + q_off;
-  uint32_t hb = 0;
+  QuadBits qb;
   uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -472,9 +494,9 @@ __device__ __forceinline__ uint32_t payload_intervals_entry(const BackParams& p,
       for (int f = 1; f + 1 < p.nfunc; f += 2) add_columns(w, c0, F(f), min(F(f + 1), k_len));
     }
     dst[t] = make_uint4(w[0], w[1], w[2], w[3]);
-    hb |= ((w[0] | w[1]) ? 1u : 0u) | ((w[2] | w[3]) ? 2u : 0u);
+    qb.add(i, w);
   }
-  return hb;
+  return qb;
 }
 
 // Block payload of one partial entry, one warp.  The rows of a tile that
@@ -483,7 +505,7 @@ __device__ __forceinline__ uint32_t payload_intervals_entry(const BackParams& p,
 // the sample) and forms each segment's 4 words with 4 ballots over the
 // columns; lane l then stores rows l, l+32, l+64, l+96 (16 bytes each,
 // coalesced).
-__device__ __forceinline__ uint32_t payload_blocks_entry(const BackParams& p, long long e, int j,
+__device__ __forceinline__ QuadBits payload_blocks_entry(const BackParams& p, long long e, int j,
                                                          int q_len, int k_len, int q0, int hm) {
   const int lane = threadIdx.x & 31;
   const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
@@ -519,13 +541,13 @@ __device__ __forceinline__ uint32_t payload_blocks_entry(const BackParams& p, lo
     r = seg_end;
   }
   uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + lane;
-  uint32_t hb = 0;
+  QuadBits qb;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
-    hb |= ((mine[i][0] | mine[i][1]) ? 1u : 0u) | ((mine[i][2] | mine[i][3]) ? 2u : 0u);
+    qb.add(i, mine[i]);
   }
-  return hb;
+  return qb;
 }
 
 // One CTA (4 warps) per (Q plan row, mask head).  All CTAs share the
@@ -602,13 +624,16 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
   for (int k = wi; k < np; k += 4) {
     const long long e = pstart + k;
     const int j = p.p_idx[e];
-    uint32_t hb;
+    QuadBits qb;
     if (KIND == MASK_INTERVALS)
-      hb = payload_intervals_entry(p, e, j, q_len, k_len, q0, hm, q_off, sF, smem);
+      qb = payload_intervals_entry(p, e, j, q_len, k_len, q0, hm, q_off, sF, smem);
     else
-      hb = payload_blocks_entry(p, e, j, q_len, k_len, q0, hm);
-    hb = __reduce_or_sync(kFull, hb);
-    if (lane == 0) p.halves[e] = static_cast<uint8_t>(hb);
+      qb = payload_blocks_entry(p, e, j, q_len, k_len, q0, hm);
+    qb.reduce();
+    if (lane == 0) {
+      p.halves[e] = static_cast<uint8_t>(qb.halves());
+      p.quads[e] = static_cast<uint8_t>(qb.quads());
+    }
   }
 }
 
@@ -869,6 +894,7 @@ cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspac
   p.entry_row = plan->entry_row;
   p.payload = plan->payload;
   p.halves = plan->halves;
+  p.quads = plan->quads;
   p.rows = rows;
   p.rows_ub = ws.rows_ub;
   p.nq_max = ws.nq_max;

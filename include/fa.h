@@ -213,7 +213,9 @@ int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream,
  *   per row), payload [P*128*4] (entry e, tile row r, word w: bit l keeps
  *   column 32*w+l), work_desc [T*4] (m_block, head, batch, q_valid_rows) in
  *   execution order, halves [P] (bit s: some element of key columns
- *   64s..64s+63 of the partial tile is visible).  Synchronous.
+ *   64s..64s+63 of the partial tile is visible), quads [P] (quadrant
+ *   (a, s) = tile rows 64a..64a+63 x key columns 64s..64s+63: bit 2a+s set
+ *   if one of its elements is visible, bit 4+2a+s if all are).  Synchronous.
  */
 typedef struct {
   int32_t* cu_q_rows;
@@ -225,6 +227,7 @@ typedef struct {
   uint32_t* payload;
   int32_t* work_desc;
   uint8_t* halves;
+  uint8_t* quads;
 } fa_plan_host_view;
 
 int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);

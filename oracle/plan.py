@@ -17,7 +17,12 @@ Follows "Flex Attention Mask Plan Design":
   uint32 whose bit l is 1 iff element (row r, column 32*w + l) of the tile is
   visible; padding and out-of-sample elements are 0.  With it goes
   halves[e]: bit s is 1 iff some element in columns [s*T_KV/2, (s+1)*T_KV/2)
-  of the tile is visible (the consumer skips an empty half).
+  of the tile is visible (the consumer skips an empty half), and quads[e]
+  for the tile's four quadrants (row half a, column half s, quadrant index
+  2a + s): bit 2a+s is 1 iff some element of the quadrant is visible, bit
+  4+2a+s iff every element of it is (so the quadrant lies inside the sample).
+  A consumer that works on one half-height row block at a time reads which
+  column halves it must visit, and which need no predicate, from it.
 * §4.8 schedule: ``sequence_desc[B, 8]`` = (q_offset, k_offset, q_len, k_len,
   Q-plan-row begin, Q-plan-row count, K tile count, 0) and
   ``work_desc[tasks, 4]`` = (m_block, head, batch, q_valid_rows), one task per
@@ -60,6 +65,7 @@ class Plan:
     full_idx: np.ndarray           # int64 [F]
     payload: np.ndarray            # uint32 [P, T_Q, ceil(T_KV/32)]
     halves: np.ndarray             # uint8 [P]: bit s = some element of column half s is visible
+    quads: np.ndarray              # uint8 [P]: bit 2a+s any / bit 4+2a+s all of quadrant (a, s) visible
     sequence_desc: np.ndarray      # int64 [B, 8]
     work_desc: np.ndarray          # int64 [tasks, 4]
     visible_pairs: int             # |visible (q, k)| summed over mask heads and samples
@@ -84,6 +90,21 @@ def _classify_tile_row(vis_rows: np.ndarray, T_Q: int, T_KV: int, nk: int):
     # elements are False above, so a tile needing tail protection is never full.
     full = tiles.all(axis=(0, 2))
     return visible, full, tiles
+
+
+def _quadrant_bits(tiles: np.ndarray) -> np.ndarray:
+    """bool [T_Q, n, T_KV] -> uint8 [n]: quadrant (a, s) = rows [a*T_Q/2, (a+1)*T_Q/2)
+    x columns [s*T_KV/2, (s+1)*T_KV/2); bit 2a+s = any element visible, bit
+    4+2a+s = all elements visible."""
+    T_Q, n, T_KV = tiles.shape
+    rq, cq = T_Q // 2, T_KV // 2
+    out = np.zeros(n, np.uint8)
+    for a in range(2):
+        for s in range(2):
+            quad = tiles[a * rq:(a + 1) * rq, :, s * cq:(s + 1) * cq]
+            out |= (quad.any(axis=(0, 2)).astype(np.uint8) << (2 * a + s))
+            out |= (quad.all(axis=(0, 2)).astype(np.uint8) << (4 + 2 * a + s))
+    return out
 
 
 def _pack_tiles(tiles: np.ndarray) -> np.ndarray:
@@ -132,7 +153,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
 
     p_cnt = np.zeros((len(heads), rows), np.int64)
     f_cnt = np.zeros((len(heads), rows), np.int64)
-    p_lists, f_lists, payloads, halves = [], [], [], []
+    p_lists, f_lists, payloads, halves, quads = [], [], [], [], []
     visible_pairs = 0
     for slot, hm in enumerate(heads):
         for r in range(rows):
@@ -156,6 +177,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
                 lo = tiles[:, pi, :hcut].any(axis=(0, 2))
                 hi = tiles[:, pi, hcut:].any(axis=(0, 2))
                 halves.append((lo.astype(np.uint8) | (hi.astype(np.uint8) << 1)))
+                quads.append(_quadrant_bits(tiles[:, pi, :]))
 
     def _csr(cnt):
         off = np.zeros(cnt.size + 1, np.int64)
@@ -167,6 +189,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
     nw = -(-T_KV // 32)
     payload = (np.concatenate(payloads) if payloads else np.zeros((0, T_Q, nw), np.uint32))
     halves_arr = np.concatenate(halves) if halves else np.zeros(0, np.uint8)
+    quads_arr = np.concatenate(quads) if quads else np.zeros(0, np.uint8)
 
     seq = np.zeros((B, 8), np.int64)
     for b, (q_off, q_len, k_off, k_len) in enumerate(bounds):
@@ -178,7 +201,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
         work = np.zeros((0, 4), np.int64)
     return Plan(T_Q, T_KV, len(heads), w.Hq, w.Hk, rows, cu_q_rows, k_tiles, row_batch, row_mblock,
                 row_qvalid, p_cnt, f_cnt, _csr(p_cnt), _csr(f_cnt), partial_idx, full_idx,
-                payload, halves_arr, seq, work, visible_pairs)
+                payload, halves_arr, quads_arr, seq, work, visible_pairs)
 
 
 def schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, Hq, Hk, Hmask) -> np.ndarray:
@@ -263,5 +286,6 @@ def build_plan_by_heads(w, T_Q: int = 128, T_KV: int = 128, processes: int = 8) 
                 _csr(f_cnt), np.concatenate([q.partial_idx for q in parts]),
                 np.concatenate([q.full_idx for q in parts]),
                 np.concatenate([q.payload for q in parts]),
-                np.concatenate([q.halves for q in parts]), first.sequence_desc, work,
+                np.concatenate([q.halves for q in parts]),
+                np.concatenate([q.quads for q in parts]), first.sequence_desc, work,
                 sum(q.visible_pairs for q in parts))

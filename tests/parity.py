@@ -33,6 +33,7 @@ def compare_plan(gpu: dict, ref: OP.Plan):
     assert np.array_equal(gpu["full_idx"], ref.full_idx)
     assert np.array_equal(gpu["payload"], ref.payload)
     assert np.array_equal(gpu["halves"], ref.halves)
+    assert np.array_equal(gpu["quads"], ref.quads)
     assert np.array_equal(gpu["work_desc"], ref.work_desc)
 
 
@@ -80,8 +81,14 @@ def sample_rows(w, per_head: int, seed: int = 0, heads=None):
         if q_len == 0:
             continue
         edges = [r for t in range(0, q_len, 128) for r in (t, t + 127) if r < q_len]
-        edges += [q_len - 1, q_len - 2] if q_len > 1 else [0]
+        tail = [q_len - 1, q_len - 2] if q_len > 1 else [0]
         for h in heads:
-            extra = rng.integers(0, q_len, size=max(0, per_head - len(edges)))
-            out[(b, h)] = list(edges[:per_head]) + list(extra)
+            # up to half of the rows are tile-edge rows spread over the whole
+            # sample (a different subset per head), the sample's last rows
+            # always, the rest random
+            n_edge = min(len(edges), per_head // 2)
+            pick = rng.choice(len(edges), size=n_edge, replace=False) if n_edge else []
+            chosen = [edges[i] for i in pick] + tail
+            extra = rng.integers(0, q_len, size=max(0, per_head - len(chosen)))
+            out[(b, h)] = chosen + list(extra)
     return out

@@ -20,17 +20,20 @@ def _built():
     PT.ensure_built()
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("name", ["tiny_causal", "sliding_sink", "varlen_doc_causal",
                                   "prefix_alibi_softcap"])
-def test_plan_parity_interval_workloads(name):
-    w = W.make(name, 0)
+def test_plan_parity_interval_workloads(name, seed):
+    w = W.make(name, seed)
     dp, plan = PT.gpu_plan(w)
     PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w.mask_only()))
     plan.free()
 
 
-def test_plan_parity_video_block_sparse():
-    w = W.make("video_block_sparse", 0)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_plan_parity_video_block_sparse(seed):
+    # the block mask is regenerated per seed
+    w = W.make("video_block_sparse", seed)
     dp, plan = PT.gpu_plan(w)
     ref = OP.build_plan_by_heads(w.mask_only(), processes=16)
     PT.compare_plan(fa.fa_plan_export(plan), ref)

@@ -271,7 +271,7 @@ def _assert_same_plan(a, b):
         assert getattr(a, f) == getattr(b, f), f
     for f in ("cu_q_rows", "k_tiles", "row_batch", "row_mblock", "row_qvalid", "partial_count",
               "full_count", "partial_offset", "full_offset", "partial_idx", "full_idx", "payload",
-              "halves", "sequence_desc", "work_desc"):
+              "halves", "quads", "sequence_desc", "work_desc"):
         x, y = getattr(a, f), getattr(b, f)
         assert x.shape == y.shape and np.array_equal(x, y), f
 
@@ -347,3 +347,50 @@ def test_schedule_gqa_sections(Hmask):
     secs = [(b, h // 2) for (m, h, b, qv) in first]
     assert secs == sorted(secs)
     assert any(h % 2 == 1 for (m, h, b, qv) in first) and any(h % 2 == 0 for (m, h, b, qv) in first)
+
+
+@pytest.mark.parametrize("T", [(128, 128), (64, 32)])
+@pytest.mark.parametrize("kind", ["intervals", "blocks64", "blocks48"])
+def test_quads_brute_force(T, kind):
+    """Quadrant bits of every partial entry by per-element loops: quadrant
+    (a, s) covers tile rows [a*T_Q/2, (a+1)*T_Q/2) and columns
+    [s*T_KV/2, (s+1)*T_KV/2); bit 2a+s says one of its elements is visible,
+    bit 4+2a+s that all are (elements outside the sample are not visible)."""
+    if kind == "intervals":
+        w = _tiny_interval_workload(seed=19, B=0, S=0, nfunc=1, varlen_lens=[300, 129, 70, 257])
+        # causal rows: diagonal tiles have a full lower-left quadrant
+        for b, (qo, ql, _, _) in enumerate(w.sample_bounds()):
+            w.mask_func[0, 0, qo:qo + ql] = np.arange(1, ql + 1)
+    elif kind == "blocks64":
+        w = _small_block_workload(2, 333, 64, 64, seed=7, density=0.3)
+    else:
+        w = _small_block_workload(2, 301, 48, 80, seed=8, density=0.3)
+    T_Q, T_KV = T
+    p = P.build_plan(w, T_Q, T_KV)
+    bounds = w.sample_bounds()
+    seen_full = seen_partial_quad = 0
+    for hm in range(w.Hmask):
+        for r in range(p.rows):
+            b, m = int(p.row_batch[r]), int(p.row_mblock[r])
+            _, ql, _, kl = bounds[b]
+            vis = M.visible_rows(w, hm, b, np.arange(ql))
+            f = hm * p.rows + r
+            for e in range(int(p.partial_offset[f]), int(p.partial_offset[f + 1])):
+                j = int(p.partial_idx[e])
+                want = 0
+                for a in range(2):
+                    for s_ in range(2):
+                        anyv, allv = False, True
+                        for rr in range(a * T_Q // 2, (a + 1) * T_Q // 2):
+                            for cc in range(s_ * T_KV // 2, (s_ + 1) * T_KV // 2):
+                                q, k = m * T_Q + rr, j * T_KV + cc
+                                v = q < ql and k < kl and bool(vis[q, k])
+                                anyv |= v
+                                allv &= v
+                        want |= (int(anyv) << (2 * a + s_)) | (int(allv) << (4 + 2 * a + s_))
+                assert int(p.quads[e]) == want, (hm, r, j)
+                seen_full += bin(want >> 4).count("1")
+                seen_partial_quad += bin((want & 15) & ~(want >> 4)).count("1")
+    assert p.partial_idx.size > 0
+    if T == (128, 128):  # both kinds of quadrant occur at the consumer's tile
+        assert seen_full > 0 and seen_partial_quad > 0
