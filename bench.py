@@ -70,7 +70,7 @@ def load_peaks():
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "attn_fwd_pair.cu", "ptx.cuh", "internal.h"):
+    for f in ("attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu", "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "block_sparse_masked_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -78,8 +78,12 @@ def kernel_hash() -> str:
 
 def fwd_kernel_name(w) -> str:
     """The forward kernel the library launches for this workload."""
-    if w.mask_kind == "intervals" and not (w.softcap and w.softcap > 0) and w.alibi_slopes is None:
+    mods = bool(w.softcap and w.softcap > 0) or w.alibi_slopes is not None
+    if w.mask_kind == "intervals" and not mods:
         return "k_fwd_pair (attention forward, two Q tiles per task)"
+    if (w.mask_kind == "blocks" and not mods and w.d == 128 and w.block_q % 64 == 0
+            and w.block_kv % 64 == 0):
+        return "k_fwd_kt (keys-major attention forward, 64-row halves x pairs of 64x64 quadrants)"
     return "k_fwd (attention forward, one Q tile per task)"
 
 

@@ -1065,6 +1065,9 @@ cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why
 }
 cudaError_t launch_fwd_d128(const FwdLaunch& a, cudaStream_t st, const char** why) {
   if (use_pair(a)) return launch_fwd_pair_d128(a, st, why);
+  // block masks of 64-aligned blocks: one 64-row half of a Q tile against
+  // pairs of its live 64x64 quadrants (attn_fwd_kt.cu)
+  if (fwd_kt_applies(a)) return launch_fwd_kt(a, st, why);
   return launch_d<128>(a, st, why);
 }
 

@@ -232,3 +232,53 @@ def test_full_workload_sampled_rows(name, per_head, seed):
     eo, el = PT.check_rows(w, dp.o, dp.lse, rows)
     print(f"{name} seed {seed}: O max-abs {eo:.3e}, LSE max-abs {el:.3e}")
     plan.free()
+
+
+def _block_problem(seed, B, S, H, Hk, blk_q, blk_kv, density, diagonal=True, Sk=None, d=128):
+    Sk = S if Sk is None else Sk
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, S, H, d, generator=gen).bfloat16()
+    k, v = (torch.randn(B, Sk, Hk, d, generator=gen).bfloat16() for _ in range(2))
+    bm = W.random_block_mask(seed, H, -(-S // blk_q), -(-Sk // blk_kv), density, diagonal=diagonal)
+    return W.Workload("blk", W.LAYOUT_BSHD, B, S, Sk, H, Hk, d, q, k, v, 1 / math.sqrt(d), "blocks",
+                      block_mask=bm, block_q=blk_q, block_kv=blk_kv)
+
+
+@pytest.mark.parametrize("geom", [(128, 64), (64, 192), (128, 128)])
+def test_block_mask_64_multiple_geometries(geom):
+    # logical blocks that are multiples of 64 run one 64-row half of a Q tile
+    # against pairs of its live 64x64 quadrants; ragged tails on both axes
+    w = _block_problem(51, B=1, S=777, H=2, Hk=2, blk_q=geom[0], blk_kv=geom[1], density=0.3, Sk=650)
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+def test_block_mask_empty_block_rows():
+    # whole logical block rows without an active block (no diagonal): the Q
+    # halves see no key at all (O = 0, LSE = -inf), next to halves that do
+    w = _block_problem(52, B=2, S=640, H=2, Hk=1, blk_q=64, blk_kv=64, density=0.2, diagonal=False)
+    w.block_mask[:, 1, :] = 0      # rows 64-127 of tile 0: its second half
+    w.block_mask[:, 2:4, :] = 0    # all of tile 1
+    w.block_mask[0, 7, :] = 0
+    dp, plan = run(w)
+    lse = dp.lse.cpu()
+    assert torch.all(lse[:, 64:128] == -math.inf) and torch.all(lse[:, 640 + 128:640 + 256] == -math.inf)
+    assert torch.all(dp.o.float().cpu()[:, 128:256] == 0)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
+
+
+def test_block_mask_growing_scores_rescale():
+    # key blocks of growing magnitude along each row's list: column maxima
+    # move by far more than 2^8 between steps, so the running sums and O are
+    # rescaled many times inside a task
+    w = _block_problem(53, B=1, S=1024, H=2, Hk=2, blk_q=64, blk_kv=64, density=0.5)
+    k = w.k.float()
+    for j in range(1024 // 64):
+        k[:, 64 * j:64 * (j + 1)] *= 1.0 + 0.45 * j
+    w.k = k.bfloat16()
+    w.q = (w.q.float() * 2.0).bfloat16()
+    dp, plan = run(w)
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    plan.free()
