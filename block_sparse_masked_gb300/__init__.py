@@ -41,6 +41,7 @@ FA_ERR_UNSUPPORTED = -8
 FA_LAYOUT_BSHD = 0
 FA_LAYOUT_THD = 1
 FA_DTYPE_BF16 = 0
+FA_PLAN_BACKWARD = 1
 FA_MOD_SOFTCAP = 1
 FA_MOD_ALIBI = 2
 FA_TILE_Q = 128
@@ -73,6 +74,12 @@ class FaPlanInfo(_c.Structure):
                 ("build_us", _c.c_double)]
 
 
+class FaPlanBwdHostView(_c.Structure):
+    _fields_ = [("cu_k_rows", _vp), ("partial_offset", _vp), ("partial_idx", _vp),
+                ("full_offset", _vp), ("full_idx", _vp), ("payload", _vp), ("dq_write_order", _vp),
+                ("dq_write_order_full", _vp)]
+
+
 class FaPlanHostView(_c.Structure):
     _fields_ = [("cu_q_rows", _vp), ("sequence_desc", _vp), ("partial_offset", _vp),
                 ("partial_idx", _vp), ("full_offset", _vp), ("full_idx", _vp), ("payload", _vp),
@@ -100,6 +107,11 @@ def lib():
                                               P(_vp)]
         L.fa_plan_build_blocks.argtypes = [P(FaGeometry), _vp, _i32, _i32, _i32, P(FaAllocator),
                                            _vp, P(_vp)]
+        L.fa_plan_build_intervals_ex.argtypes = [P(FaGeometry), _vp, _i32, _i32, _u32, P(FaAllocator),
+                                                 _vp, P(_vp)]
+        L.fa_plan_build_blocks_ex.argtypes = [P(FaGeometry), _vp, _i32, _i32, _i32, _u32,
+                                              P(FaAllocator), _vp, P(_vp)]
+        L.fa_plan_export_backward.argtypes = [_vp, P(FaPlanBwdHostView)]
         L.fa_plan_free.argtypes = [_vp, _vp]
         L.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, P(FaGeometry), _c.c_float, P(FaMods), _vp]
         L.fa_plan_info_get.argtypes = [_vp, _i32, _vp, P(FaPlanInfo)]
@@ -109,7 +121,8 @@ def lib():
         L.fa_selftest_wait_timeout.argtypes = [_u64, _vp]
         L.fa_last_error.restype = _c.c_char_p
         L.fa_version.restype = _c.c_char_p
-        for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_free", "fa_fwd",
+        for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_build_intervals_ex",
+                  "fa_plan_build_blocks_ex", "fa_plan_export_backward", "fa_plan_free", "fa_fwd",
                   "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags",
                   "fa_plan_header_noalloc", "fa_selftest_wait_timeout"):
             getattr(L, f).restype = _c.c_int
@@ -210,20 +223,34 @@ def _alloc_arg(allocator: Optional[Allocator]):
 
 
 def fa_plan_build_intervals(geom: FaGeometry, mask_func, Hmask: int, nfunc: int,
-                            stream=None, allocator: Optional[Allocator] = None) -> Plan:
+                            stream=None, allocator: Optional[Allocator] = None,
+                            backward: bool = False) -> Plan:
+    """fa_plan_build_intervals, or fa_plan_build_intervals_ex with FA_PLAN_BACKWARD."""
     out = _vp()
-    _check(lib().fa_plan_build_intervals(_c.byref(geom), _ptr(mask_func), Hmask, nfunc,
-                                         _alloc_arg(allocator), _stream_handle(stream),
-                                         _c.byref(out)))
+    if backward:
+        _check(lib().fa_plan_build_intervals_ex(_c.byref(geom), _ptr(mask_func), Hmask, nfunc,
+                                                FA_PLAN_BACKWARD, _alloc_arg(allocator),
+                                                _stream_handle(stream), _c.byref(out)))
+    else:
+        _check(lib().fa_plan_build_intervals(_c.byref(geom), _ptr(mask_func), Hmask, nfunc,
+                                             _alloc_arg(allocator), _stream_handle(stream),
+                                             _c.byref(out)))
     return Plan(out.value, allocator)
 
 
 def fa_plan_build_blocks(geom: FaGeometry, block_mask, Hmask: int, block_q: int, block_kv: int,
-                         stream=None, allocator: Optional[Allocator] = None) -> Plan:
+                         stream=None, allocator: Optional[Allocator] = None,
+                         backward: bool = False) -> Plan:
+    """fa_plan_build_blocks, or fa_plan_build_blocks_ex with FA_PLAN_BACKWARD."""
     out = _vp()
-    _check(lib().fa_plan_build_blocks(_c.byref(geom), _ptr(block_mask), Hmask, block_q, block_kv,
-                                      _alloc_arg(allocator), _stream_handle(stream),
-                                      _c.byref(out)))
+    if backward:
+        _check(lib().fa_plan_build_blocks_ex(_c.byref(geom), _ptr(block_mask), Hmask, block_q,
+                                             block_kv, FA_PLAN_BACKWARD, _alloc_arg(allocator),
+                                             _stream_handle(stream), _c.byref(out)))
+    else:
+        _check(lib().fa_plan_build_blocks(_c.byref(geom), _ptr(block_mask), Hmask, block_q, block_kv,
+                                          _alloc_arg(allocator), _stream_handle(stream),
+                                          _c.byref(out)))
     return Plan(out.value, allocator)
 
 
@@ -257,6 +284,27 @@ def fa_plan_info_get(plan: Plan, count_visible: bool = False, stream=None) -> di
     d = {f: getattr(info, f) for f, _ in FaPlanInfo._fields_}
     d["header"] = list(info.header)
     return d
+
+
+def fa_plan_export_backward(plan: Plan) -> dict:
+    """Debug snapshot of the backward views (K2Q lists, key-major payload, dQ order)."""
+    info = fa_plan_info_get(plan)
+    KR, KP, KF = info["header"][4], info["header"][5], info["header"][6]
+    B, Hm = info["batch"], info["mask_heads"]
+    arrs = {
+        "cu_k_rows": np.zeros(B + 1, np.int32),
+        "partial_offset": np.zeros(Hm * KR + 1, np.int32),
+        "partial_idx": np.zeros(KP, np.int32),
+        "full_offset": np.zeros(Hm * KR + 1, np.int32),
+        "full_idx": np.zeros(KF, np.int32),
+        "payload": np.zeros((KP, FA_TILE_K, FA_PAYLOAD_WORDS), np.uint32),
+        "dq_write_order": np.zeros(KP, np.int32),
+        "dq_write_order_full": np.zeros(KF, np.int32),
+    }
+    view = FaPlanBwdHostView(*[a.ctypes.data if a.size else None for a in arrs.values()])
+    _check(lib().fa_plan_export_backward(plan.handle, _c.byref(view)))
+    arrs["header"] = np.array(info["header"], np.int64)
+    return arrs
 
 
 def fa_plan_export(plan: Plan) -> dict:

@@ -76,8 +76,8 @@ constexpr int kHalf = 64;                       // Q rows per sub-task, keys per
 constexpr int kCols = 32;                       // query columns per softmax warpgroup
 constexpr int kHalfBytes = kHalf * D * 2;       // 16 KB
 constexpr int kSlotBytes = 2 * kHalfBytes;      // ring slot: two positions
-constexpr int kKSlots = 2, kVSlots = 3;
-constexpr int kSBuf = 4;                        // TMEM S^T buffers, 64 columns each
+constexpr int kKSlots = 3, kVSlots = 2;
+constexpr int kSBuf = 2;                        // TMEM S^T buffers, 64 columns each
 constexpr int kPBuf = 2;                        // shared-memory P^T buffers
 constexpr int kDescRing = 8;                    // step descriptors ahead of the consumers
 constexpr int kSubRing = 2;                     // sub-task records

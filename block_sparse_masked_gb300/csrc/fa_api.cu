@@ -222,10 +222,12 @@ void free_plan_mem(fa_plan* p, cudaStream_t st) {
   Alloc al{p->custom_alloc ? &p->alloc : nullptr, p->device, st};
   al.put(p->mem.ptr, p->mem.bytes);
   p->mem.ptr = nullptr;
+  al.put(p->bmem.ptr, p->bmem.bytes);
+  p->bmem.ptr = nullptr;
 }
 
-int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_allocator* allocator,
-                 void* stream, fa_plan** out) {
+int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t flags,
+                 const fa_allocator* allocator, void* stream, fa_plan** out) {
   const auto t0 = std::chrono::steady_clock::now();
   if (!out) return fail(FA_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
@@ -264,6 +266,12 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
                o_po = c1.take(4ull * (nflat_ub + 1)), o_fo = c1.take(4ull * (nflat_ub + 1)),
                o_hist = c1.take(4ull * NS * (C + 1)), o_cursor = c1.take(4ull * NS * (C + 1)),
                o_work = c1.take(16ull * rows_ub * g.heads_q);
+  // backward K2Q view: padded K rows (mask head, sample, K tile)
+  const bool bwd = (flags & FA_PLAN_BACKWARD) != 0;
+  const long long kflat_ub = bwd ? static_cast<long long>(Hmask) * B * kt_ub : 0;
+  const size_t o_kpc = c1.take(4ull * kflat_ub), o_kfc = c1.take(4ull * kflat_ub),
+               o_ckr = c1.take(bwd ? 4ull * (B + 1) : 0), o_krb = c1.take(bwd ? 4ull * B * kt_ub : 0),
+               o_kpo = c1.take(bwd ? 4ull * (kflat_ub + 1) : 0), o_kfo = c1.take(bwd ? 4ull * (kflat_ub + 1) : 0);
   Alloc al{allocator, dev, st};
   uint8_t* w1 = static_cast<uint8_t*>(al.get(c1.off));
   if (!w1) return fail(FA_ERR_ALLOC, "workspace allocation of %zu bytes failed", c1.off);
@@ -280,6 +288,14 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   ws.hist = reinterpret_cast<int32_t*>(w1 + o_hist);
   ws.cursors = reinterpret_cast<int32_t*>(w1 + o_cursor);
   ws.work = reinterpret_cast<int32_t*>(w1 + o_work);
+  if (bwd) {
+    ws.kp_cnt = reinterpret_cast<int32_t*>(w1 + o_kpc);
+    ws.kf_cnt = reinterpret_cast<int32_t*>(w1 + o_kfc);
+    ws.cu_krows = reinterpret_cast<int32_t*>(w1 + o_ckr);
+    ws.krow_batch = reinterpret_cast<int32_t*>(w1 + o_krb);
+    ws.kp_off = reinterpret_cast<int32_t*>(w1 + o_kpo);
+    ws.kf_off = reinterpret_cast<int32_t*>(w1 + o_kfo);
+  }
 
   auto bail = [&](int code) {
     al.put(w1, c1.off);
@@ -296,7 +312,9 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   const long long ticket = ++t_ticket;
   // front stage, then the schedule, which the GPU runs while this thread
   // waits for the header, sizes the plan and allocates it
-  cudaError_t e = bsm::launch_front(g, margs, ws, gi->cu_seqlens_q, gi->cu_seqlens_k, hh, ticket, st);
+  // the K2Q counts start at zero (two adjacent sub-arrays)
+  cudaError_t e = bwd ? cudaMemsetAsync(ws.kp_cnt, 0, o_ckr - o_kpc, st) : cudaSuccess;
+  if (!e) e = bsm::launch_front(g, margs, ws, gi->cu_seqlens_q, gi->cu_seqlens_k, hh, ticket, st);
   if (!e) e = cudaEventRecord(ev, st);
   if (!e) e = bsm::launch_schedule(g, ws, Hmask, NS, C, st);
   if (!e) e = wait_header(hh, ticket, ev);  // the one host/device synchronisation of a build
@@ -313,6 +331,8 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
     return bail(fail(FA_ERR_INVALID_MASK, "mask endpoints out of range or out of order "
                                           "(need 0 <= F0 <= ... <= F(n-1) <= k_len)"));
   if (err & bsm::PLANERR_OVERFLOW) return bail(fail(FA_ERR_UNSUPPORTED, "more than 2^30 plan entries"));
+  if (bwd && (hdr[5] != hdr[1] || hdr[6] != hdr[2]))
+    return bail(fail(FA_ERR_CUDA, "planner inconsistency: K2Q and Q2K entry counts differ"));
 
   fa_plan* plan = new (std::nothrow) fa_plan();
   if (!plan) return bail(fail(FA_ERR_ALLOC, "host allocation"));
@@ -363,9 +383,40 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, const fa_all
   plan->quads = pm + q_qd;
   plan->block_q = margs.block_q;
   plan->block_kv = margs.block_kv;
+  if (bwd) {
+    plan->backward = true;
+    plan->k_rows = hdr[4];
+    plan->kP = hdr[5];
+    plan->kF = hdr[6];
+    const long long kflat = static_cast<long long>(Hmask) * plan->k_rows;
+    Carver c3;
+    const size_t r_ckr = c3.take(4ull * (B + 1)), r_krb = c3.take(4ull * plan->k_rows),
+                 r_kpo = c3.take(4ull * (kflat + 1)), r_kfo = c3.take(4ull * (kflat + 1)),
+                 r_kpi = c3.take(4ull * plan->kP), r_kfi = c3.take(4ull * plan->kF),
+                 r_dq = c3.take(4ull * plan->kP), r_dqf = c3.take(4ull * plan->kF),
+                 r_kpay = c3.take(16ull * bsm::kTile * plan->kP);
+    uint8_t* bm = static_cast<uint8_t*>(al.get(c3.off));
+    if (!bm) {
+      free_plan_mem(plan, st);
+      delete plan;
+      return bail(fail(FA_ERR_ALLOC, "backward view allocation of %zu bytes failed", c3.off));
+    }
+    plan->bmem.ptr = bm;
+    plan->bmem.bytes = c3.off;
+    plan->cu_krows = reinterpret_cast<int32_t*>(bm + r_ckr);
+    plan->krow_batch = reinterpret_cast<int32_t*>(bm + r_krb);
+    plan->kp_off = reinterpret_cast<int32_t*>(bm + r_kpo);
+    plan->kf_off = reinterpret_cast<int32_t*>(bm + r_kfo);
+    plan->kp_idx = reinterpret_cast<int32_t*>(bm + r_kpi);
+    plan->kf_idx = reinterpret_cast<int32_t*>(bm + r_kfi);
+    plan->dq_order = reinterpret_cast<int32_t*>(bm + r_dq);
+    plan->dq_order_full = reinterpret_cast<int32_t*>(bm + r_dqf);
+    plan->kpayload = reinterpret_cast<uint32_t*>(bm + r_kpay);
+  }
 
   // exact-size copies (the schedule included), CSR lists, payloads: one launch
   e = bsm::launch_back(g, margs, ws, plan, gi->cu_seqlens_q, gi->cu_seqlens_k, st);
+  if (!e && bwd) e = bsm::launch_back_k2q(g, ws, plan, st);
   if (e) {
     free_plan_mem(plan, st);
     delete plan;
@@ -408,6 +459,12 @@ extern "C" {
 
 int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func, int32_t Hmask,
                             int32_t nfunc, const fa_allocator* allocator, void* stream, fa_plan** out) {
+  return fa_plan_build_intervals_ex(geom, mask_func, Hmask, nfunc, 0u, allocator, stream, out);
+}
+
+int fa_plan_build_intervals_ex(const fa_geometry* geom, const int32_t* mask_func, int32_t Hmask,
+                               int32_t nfunc, uint32_t flags, const fa_allocator* allocator, void* stream,
+                               fa_plan** out) {
   t_err.clear();
   if (out) *out = nullptr;
   if (int e = check_geometry(geom)) return e;
@@ -420,12 +477,19 @@ int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func, i
   m.mask_func = mask_func;
   m.nfunc = nfunc;
   m.Hmask = Hmask;
-  return build_common(geom, m, allocator, stream, out);
+  if (flags & ~static_cast<uint32_t>(FA_PLAN_BACKWARD)) return fail(FA_ERR_INVALID_ARG, "unknown plan flags");
+  return build_common(geom, m, flags, allocator, stream, out);
 }
 
 int fa_plan_build_blocks(const fa_geometry* geom, const uint8_t* block_mask, int32_t Hmask,
                          int32_t block_q, int32_t block_kv, const fa_allocator* allocator, void* stream,
                          fa_plan** out) {
+  return fa_plan_build_blocks_ex(geom, block_mask, Hmask, block_q, block_kv, 0u, allocator, stream, out);
+}
+
+int fa_plan_build_blocks_ex(const fa_geometry* geom, const uint8_t* block_mask, int32_t Hmask,
+                            int32_t block_q, int32_t block_kv, uint32_t flags, const fa_allocator* allocator,
+                            void* stream, fa_plan** out) {
   t_err.clear();
   if (out) *out = nullptr;
   if (int e = check_geometry(geom)) return e;
@@ -442,7 +506,8 @@ int fa_plan_build_blocks(const fa_geometry* geom, const uint8_t* block_mask, int
   m.nbq = cdiv(geom->seqlen_q, block_q);
   m.nbk = cdiv(geom->seqlen_k, block_kv);
   m.Hmask = Hmask;
-  return build_common(geom, m, allocator, stream, out);
+  if (flags & ~static_cast<uint32_t>(FA_PLAN_BACKWARD)) return fail(FA_ERR_INVALID_ARG, "unknown plan flags");
+  return build_common(geom, m, flags, allocator, stream, out);
 }
 
 int fa_plan_free(fa_plan* plan, void* stream) {
@@ -515,7 +580,7 @@ int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream, f
   info->layout = plan->geom.layout;
   info->num_tasks = plan->tasks;
   info->payload_bytes = plan->P * bsm::kTile * bsm::kPayloadWords * 4;
-  info->plan_bytes = static_cast<int64_t>(plan->mem.bytes);
+  info->plan_bytes = static_cast<int64_t>(plan->mem.bytes + plan->bmem.bytes);
   info->signature = plan->signature;
   info->build_us = plan->build_us;
   info->visible_pairs = -1;
@@ -559,6 +624,33 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst) {
     if (!it.d || it.n == 0) continue;
     cudaError_t e = cudaMemcpy(it.d, it.s, it.n, cudaMemcpyDeviceToHost);
     if (e) return cuda_fail(e, "plan export");
+  }
+  return FA_OK;
+}
+
+int fa_plan_export_backward(const fa_plan* plan, fa_plan_bwd_host_view* dst) {
+  t_err.clear();
+  if (!plan || !dst) return fail(FA_ERR_INVALID_ARG, "plan and dst must be non-NULL");
+  if (!plan->backward) return fail(FA_ERR_INVALID_ARG, "the plan was built without FA_PLAN_BACKWARD");
+  const long long B = plan->geom.batch, nflat = static_cast<long long>(plan->Hmask) * plan->k_rows;
+  struct Item {
+    void* d;
+    const void* s;
+    size_t n;
+  } items[] = {
+      {dst->cu_k_rows, plan->cu_krows, 4ull * (B + 1)},
+      {dst->partial_offset, plan->kp_off, 4ull * (nflat + 1)},
+      {dst->partial_idx, plan->kp_idx, 4ull * plan->kP},
+      {dst->full_offset, plan->kf_off, 4ull * (nflat + 1)},
+      {dst->full_idx, plan->kf_idx, 4ull * plan->kF},
+      {dst->payload, plan->kpayload, 16ull * bsm::kTile * plan->kP},
+      {dst->dq_write_order, plan->dq_order, 4ull * plan->kP},
+      {dst->dq_write_order_full, plan->dq_order_full, 4ull * plan->kF},
+  };
+  for (auto& it : items) {
+    if (!it.d || it.n == 0) continue;
+    cudaError_t e = cudaMemcpy(it.d, it.s, it.n, cudaMemcpyDeviceToHost);
+    if (e) return cuda_fail(e, "backward view export");
   }
   return FA_OK;
 }

@@ -102,7 +102,23 @@ struct FrontParams {
   long long* host_header;  // host memory, 8 values then the ticket; may be null
   long long ticket;
   unsigned* ctl;       // [0] CTAs arrived, [1] error bits; zero at launch, zero again at exit
+  // backward K2Q view (§4.4); kp_cnt is null when it is not built
+  int32_t* kp_cnt;     // [Hmask*B*kt_ub] per padded K row (hm, b, K tile): zero at launch
+  int32_t* kf_cnt;
+  int kt_ub;
+  int32_t* cu_krows;   // [B+1], written by the last CTA
+  int32_t* krow_batch; // [k_rows]
+  int32_t* kp_off;     // [Hmask*k_rows+1], compact order (hm, K row)
+  int32_t* kf_off;
 };
+
+// K2Q counts (§4.4): the tile (Q row, K tile j) of sample b adds one
+// partial or full Q contributor to K row (hm, b, j).
+__device__ __forceinline__ void count_k2q(const FrontParams& p, int hm, int b, int j, bool partial, bool full) {
+  const long long r = (static_cast<long long>(hm) * p.B + b) * p.kt_ub + j;
+  if (partial) atomicAdd(p.kp_cnt + r, 1);
+  if (full) atomicAdd(p.kf_cnt + r, 1);
+}
 
 struct SampleGeo {
   int q_off, k_off, q_len, k_len;
@@ -143,7 +159,7 @@ __device__ __forceinline__ SampleGeo sample_geo(const FrontParams& p, int b) {
 // "covered" if one maximal run of merged intervals contains the whole tile;
 // visible = OR over valid rows of touched, full = AND over all 128 rows of
 // covered (rows past the sample's q_len cover nothing, so a Q tail is never full).
-__device__ __forceinline__ void classify_intervals(const FrontParams& p, const SampleGeo& sg,
+__device__ __forceinline__ void classify_intervals(const FrontParams& p, const SampleGeo& sg, int b,
                                                    int lr, int hm, long long ws_row) {
   const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   __shared__ uint32_t s_v[4], s_f[4];
@@ -204,6 +220,12 @@ __device__ __forceinline__ void classify_intervals(const FrontParams& p, const S
       p.full_bits[ws_row * p.words + w] = f;
       pc += __popc(v & ~f);
       fc += __popc(f);
+      if (p.kp_cnt) {
+        for (uint32_t x = v; x; x &= x - 1) {
+          const int bit = __ffs(x) - 1;
+          count_k2q(p, hm, b, 32 * w + bit, !((f >> bit) & 1u), (f >> bit) & 1u);
+        }
+      }
     }
     __syncthreads();
   }
@@ -217,7 +239,7 @@ __device__ __forceinline__ void classify_intervals(const FrontParams& p, const S
 // touches the logical blocks [r0, r1] x [c0, c1] that overlap its in-bounds
 // part; it is visible if any is active and full if all are and the tile has
 // no Q/K tail.  Words are bit-packed with warp ballots.
-__device__ __forceinline__ void classify_blocks(const FrontParams& p, const SampleGeo& sg, int lr,
+__device__ __forceinline__ void classify_blocks(const FrontParams& p, const SampleGeo& sg, int b, int lr,
                                                 int hm, long long ws_row) {
   const int t = threadIdx.x, lane = t & 31;
   __shared__ int s_pc, s_fc;
@@ -250,6 +272,7 @@ __device__ __forceinline__ void classify_blocks(const FrontParams& p, const Samp
       }
       vis = any;
       full = any && all && !qtail && !ktail;
+      if (p.kp_cnt && vis) count_k2q(p, hm, b, j, !full, full);
     }
     const uint32_t vb = __ballot_sync(kFull, vis);
     const uint32_t fb = __ballot_sync(kFull, full);
@@ -272,6 +295,52 @@ __device__ __forceinline__ void classify_blocks(const FrontParams& p, const Samp
 // prefixes and the row -> sample map; exclusive scans of the per-row counts
 // in compact (mask head, row) order; the header; reset of the control words.
 constexpr int kScanItems = 8;
+
+// Exclusive scans, by the whole CTA, of two per-row counts read by
+// counts(i, a, c) for compact rows i in [0, n): offsets to off_a/off_c
+// [n + 1]; totals added to tot_a/tot_c.
+template <class Counts>
+__device__ void scan_pair(long long n, int32_t* off_a, int32_t* off_c, long long& tot_a, long long& tot_c,
+                          Counts counts) {
+  const int nt = blockDim.x;
+  long long ca = 0, cc = 0;
+  for (long long base = 0; base < n; base += static_cast<long long>(nt) * kScanItems) {
+    const long long i0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
+    int va[kScanItems], vc[kScanItems];
+    long long sa = 0, sc = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+      const long long i = i0 + k;
+      va[k] = 0;
+      vc[k] = 0;
+      if (i < n) counts(i, va[k], vc[k]);
+      sa += va[k];
+      sc += vc[k];
+    }
+    long long ta, tc;
+    long long ea = ca + block_excl_scan(sa, &ta);
+    long long ec = cc + block_excl_scan(sc, &tc);
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+      const long long i = i0 + k;
+      if (i < n) {
+        off_a[i] = static_cast<int32_t>(ea);
+        off_c[i] = static_cast<int32_t>(ec);
+      }
+      ea += va[k];
+      ec += vc[k];
+    }
+    ca += ta;
+    cc += tc;
+  }
+  if (threadIdx.x == 0) {
+    off_a[n] = static_cast<int32_t>(ca);
+    off_c[n] = static_cast<int32_t>(cc);
+  }
+  __syncthreads();
+  tot_a += ca;
+  tot_c += cc;
+}
 
 __device__ void front_finish(const FrontParams& p) {
   const int nt = blockDim.x;
@@ -319,48 +388,53 @@ __device__ void front_finish(const FrontParams& p) {
   __syncthreads();
   const long long n = static_cast<long long>(p.Hmask) * rows;
   long long cp = 0, cf = 0;
-  for (long long base = 0; base < n; base += static_cast<long long>(nt) * kScanItems) {
-    const long long i0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
-    int vp[kScanItems], vf[kScanItems];
-    long long sp = 0, sf = 0;
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) {
-      const long long i = i0 + k;
-      vp[k] = 0;
-      vf[k] = 0;
-      if (i < n) {
-        const int hm = static_cast<int>(i / rows), r = static_cast<int>(i % rows);
-        const int b = p.row_batch[r];
-        const long long ws_row = static_cast<long long>(hm) * p.rows_ub +
-                                 static_cast<long long>(b) * p.nq_max + (r - p.cu_rows[b]);
-        vp[k] = __ldcg(p.p_cnt + ws_row);
-        vf[k] = __ldcg(p.f_cnt + ws_row);
-      }
-      sp += vp[k];
-      sf += vf[k];
+  scan_pair(n, p.p_off, p.f_off, cp, cf, [&](long long i, int& a, int& c) {
+    const int hm = static_cast<int>(i / rows), r = static_cast<int>(i % rows);
+    const int b = p.row_batch[r];
+    const long long ws_row = static_cast<long long>(hm) * p.rows_ub +
+                             static_cast<long long>(b) * p.nq_max + (r - p.cu_rows[b]);
+    a = __ldcg(p.p_cnt + ws_row);
+    c = __ldcg(p.f_cnt + ws_row);
+  });
+  // backward K2Q view (§4.2 backward prefix, §4.4 counts, §4.5 scan): K plan
+  // rows per sample, K row -> sample, and the K2Q offsets
+  long long k_rows = 0, kp = 0, kf = 0;
+  if (p.kp_cnt) {
+    for (int base = 0; base < p.B; base += nt) {
+      const int b = base + threadIdx.x;
+      const int nk = (b < p.B) ? cdiv(sample_geo(p, b).k_len, kTile) : 0;
+      long long tot;
+      const long long begin = k_rows + block_excl_scan(nk, &tot);
+      if (b < p.B) p.cu_krows[b] = static_cast<int32_t>(begin);
+      k_rows += tot;
     }
-    long long tp, tf;
-    long long ep = cp + block_excl_scan(sp, &tp);
-    long long ef = cf + block_excl_scan(sf, &tf);
-#pragma unroll
-    for (int k = 0; k < kScanItems; ++k) {
-      const long long i = i0 + k;
-      if (i < n) {
-        p.p_off[i] = static_cast<int32_t>(ep);
-        p.f_off[i] = static_cast<int32_t>(ef);
+    if (threadIdx.x == 0) p.cu_krows[p.B] = static_cast<int32_t>(k_rows);
+    __syncthreads();
+    for (long long r = threadIdx.x; r < k_rows; r += nt) {
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cu_krows[mid] <= r) lo = mid; else hi = mid - 1;
       }
-      ep += vp[k];
-      ef += vf[k];
+      p.krow_batch[r] = lo;
     }
-    cp += tp;
-    cf += tf;
+    __syncthreads();
+    const long long nk_flat = static_cast<long long>(p.Hmask) * k_rows;
+    scan_pair(nk_flat, p.kp_off, p.kf_off, kp, kf, [&](long long i, int& a, int& c) {
+      const int hm = static_cast<int>(i / k_rows), r = static_cast<int>(i % k_rows);
+      const int b = p.krow_batch[r];
+      const long long ws = (static_cast<long long>(hm) * p.B + b) * p.kt_ub + (r - p.cu_krows[b]);
+      a = __ldcg(p.kp_cnt + ws);
+      c = __ldcg(p.kf_cnt + ws);
+    });
   }
   if (threadIdx.x == 0) {
-    p.p_off[n] = static_cast<int32_t>(cp);
-    p.f_off[n] = static_cast<int32_t>(cf);
     uint32_t e = atomicExch(&p.ctl[1], 0u);  // read and reset the error bits
-    if (cp > 0x3fffffffLL || cf > 0x3fffffffLL) e |= PLANERR_OVERFLOW;
-    const long long h[8] = {rows, cp, cf, 0, 0, 0, 0, static_cast<long long>(e)};
+    if (cp > 0x3fffffffLL || cf > 0x3fffffffLL || kp > 0x3fffffffLL || kf > 0x3fffffffLL) e |= PLANERR_OVERFLOW;
+    // {fwd Q rows, fwd partial, fwd full, bwd Q rows, bwd K rows, bwd partial,
+    // bwd full, error}: the dQ consumer reads the forward Q2K view, which has
+    // the backward geometry, so bwd Q rows = fwd Q rows
+    const long long h[8] = {rows, cp, cf, p.kp_cnt ? rows : 0, k_rows, kp, kf, static_cast<long long>(e)};
 #pragma unroll
     for (int k = 0; k < 8; ++k) p.header[k] = h[k];
     p.ctl[0] = 0u;  // every CTA has arrived: the control words are free again
@@ -386,9 +460,9 @@ __global__ void __launch_bounds__(KIND == MASK_INTERVALS ? 128 : 256) k_front(Fr
     if (lr < cdiv(sg.q_len, kTile)) {
       const long long ws_row = static_cast<long long>(hm) * p.rows_ub + x;
       if (KIND == MASK_INTERVALS)
-        classify_intervals(p, sg, lr, hm, ws_row);
+        classify_intervals(p, sg, b, lr, hm, ws_row);
       else
-        classify_blocks(p, sg, lr, hm, ws_row);
+        classify_blocks(p, sg, b, lr, hm, ws_row);
     }
   }
   __shared__ unsigned s_last;
@@ -637,6 +711,128 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
   }
 }
 
+// ------------------------------------------------------------ K2Q view
+// §4.7 K2Q materialisation, one CTA (4 warps) per (K row, mask head), after
+// the Q2K back stage: warp 0 reads the row's K tile bit out of the Q-major
+// bitsets of every Q row of the sample, 32 Q rows per ballot, and writes the
+// ascending partial and full Q tile lists with each entry's dQ write rank
+// (the K tile's rank among the Q row's non-empty tiles: ascending K order);
+// then the 4 warps transpose each partial entry's Q2K predicate words into
+// the key-major layout of the K-major consumer (one word per key and 32
+// queries, 32 ballots per 32x32 bit block).
+struct K2QParams {
+  // exact-size copies into the plan
+  const int32_t* src[4];
+  int32_t* dst[4];
+  long long count[4];
+  // workspace
+  const uint32_t* vis_bits;
+  const uint32_t* full_bits;
+  const int32_t* seq;
+  const int32_t* cu_krows;
+  const int32_t* krow_batch;
+  const int32_t* kp_off;
+  const int32_t* kf_off;
+  int rows_ub, nq_max, words;
+  // plan
+  const int32_t* p_off;      // Q2K partial offsets [Hmask*rows+1]
+  const uint32_t* payload;   // Q2K payload [P*128*4]
+  int32_t* kp_idx;
+  int32_t* kf_idx;
+  int32_t* dq_order;
+  int32_t* dq_order_full;
+  uint32_t* kpayload;        // [P'*128*4]: key c, word w, bit l = (query 32w+l, key c) visible
+  int rows, k_rows;
+};
+
+__device__ __forceinline__ int popc_below(const uint32_t* wv, int j) {
+  int n = 0;
+  for (int w = 0; w < (j >> 5); ++w) n += __popc(__ldg(wv + w));
+  return n + __popc(__ldg(wv + (j >> 5)) & ((1u << (j & 31)) - 1u));
+}
+__device__ __forceinline__ int popc_partial_below(const uint32_t* wv, const uint32_t* wf, int j) {
+  int n = 0;
+  for (int w = 0; w < (j >> 5); ++w) n += __popc(__ldg(wv + w) & ~__ldg(wf + w));
+  return n + __popc((__ldg(wv + (j >> 5)) & ~__ldg(wf + (j >> 5))) & ((1u << (j & 31)) - 1u));
+}
+
+__global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
+  {
+    const long long tid = (static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nthreads = static_cast<long long>(gridDim.x) * gridDim.y * blockDim.x;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+      for (long long i = tid; i < p.count[a]; i += nthreads) p.dst[a][i] = __ldg(p.src[a] + i);
+  }
+  const int krow = blockIdx.x, hm = blockIdx.y;
+  if (krow >= p.k_rows) return;
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int b = __ldg(p.krow_batch + krow);
+  const int j = krow - __ldg(p.cu_krows + b);  // sample-local K tile
+  const int nq = __ldg(p.seq + 8 * b + 5), row_begin = __ldg(p.seq + 8 * b + 4);
+  const long long flat = static_cast<long long>(hm) * p.k_rows + krow;
+  const int pstart = __ldg(p.kp_off + flat), np = __ldg(p.kp_off + flat + 1) - pstart;
+  const long long qrow0 = static_cast<long long>(hm) * p.rows_ub + static_cast<long long>(b) * p.nq_max;
+  if (wi == 0) {
+    int pb = pstart, fb = __ldg(p.kf_off + flat);
+    for (int i0 = 0; i0 < nq; i0 += 32) {
+      const int i = i0 + lane;
+      bool isp = false, isf = false;
+      int rank = 0;
+      if (i < nq) {
+        const uint32_t* wv = p.vis_bits + (qrow0 + i) * p.words;
+        const uint32_t* wf = p.full_bits + (qrow0 + i) * p.words;
+        const bool v = (__ldg(wv + (j >> 5)) >> (j & 31)) & 1u;
+        isf = (__ldg(wf + (j >> 5)) >> (j & 31)) & 1u;
+        isp = v && !isf;
+        if (v) rank = popc_below(wv, j);
+      }
+      const uint32_t bp = __ballot_sync(kFull, isp), bf = __ballot_sync(kFull, isf);
+      const uint32_t below = (1u << lane) - 1u;
+      if (isp) {
+        const int e = pb + __popc(bp & below);
+        p.kp_idx[e] = i;
+        p.dq_order[e] = rank;
+      }
+      if (isf) {
+        const int e = fb + __popc(bf & below);
+        p.kf_idx[e] = i;
+        p.dq_order_full[e] = rank;
+      }
+      pb += __popc(bp);
+      fb += __popc(bf);
+    }
+  }
+  __syncthreads();  // warp 0's Q tile lists are visible to the CTA
+  for (int k = wi; k < np; k += 4) {
+    const long long e = pstart + k;
+    const int i = p.kp_idx[e];
+    const uint32_t* wv = p.vis_bits + (qrow0 + i) * p.words;
+    const uint32_t* wf = p.full_bits + (qrow0 + i) * p.words;
+    const long long eq = __ldg(p.p_off + static_cast<long long>(hm) * p.rows + row_begin + i) +
+                         popc_partial_below(wv, wf, j);
+    const uint32_t* src = p.payload + eq * (kTile * kPayloadWords);
+    uint32_t mine[kPayloadWords][kPayloadWords];  // [key chunk][query word] for key 32 chunk + lane
+#pragma unroll
+    for (int wq = 0; wq < kPayloadWords; ++wq)
+#pragma unroll
+      for (int kc = 0; kc < kPayloadWords; ++kc) {
+        const uint32_t v = __ldg(src + (32 * wq + lane) * kPayloadWords + kc);  // query 32 wq + lane, keys 32 kc..
+        uint32_t got = 0;
+#pragma unroll
+        for (int bit = 0; bit < 32; ++bit) {
+          const uint32_t word = __ballot_sync(kFull, (v >> bit) & 1u);  // key 32 kc + bit, queries 32 wq..
+          if (lane == bit) got = word;
+        }
+        mine[kc][wq] = got;
+      }
+    uint4* dst = reinterpret_cast<uint4*>(p.kpayload + e * (kTile * kPayloadWords));
+#pragma unroll
+    for (int kc = 0; kc < kPayloadWords; ++kc)
+      dst[32 * kc + lane] = make_uint4(mine[kc][0], mine[kc][1], mine[kc][2], mine[kc][3]);
+  }
+}
+
 // ------------------------------------------------------------ schedule
 // Reads the front stage's outputs in the workspace (the number of rows
 // included) and writes work_desc there; the back stage copies it into the plan.
@@ -830,6 +1026,13 @@ cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspa
   p.host_header = host_header;
   p.ticket = ticket;
   p.ctl = ws.ctl;
+  p.kp_cnt = ws.kp_cnt;
+  p.kf_cnt = ws.kf_cnt;
+  p.kt_ub = ws.kt_ub;
+  p.cu_krows = ws.cu_krows;
+  p.krow_batch = ws.krow_batch;
+  p.kp_off = ws.kp_off;
+  p.kf_off = ws.kf_off;
   // at least one CTA, so that the last-CTA stage also runs without rows
   const dim3 grid(ws.rows_ub > 0 ? ws.rows_ub : 1, m.Hmask);
   if (m.kind == MASK_INTERVALS)
@@ -912,6 +1115,37 @@ cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspac
     k_back<MASK_INTERVALS><<<grid, 128, 0, st>>>(p);
   else
     k_back<MASK_BLOCKS><<<grid, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_back_k2q(const Geometry& g, const PlanWorkspace& ws, fa_plan* plan, cudaStream_t st) {
+  K2QParams p{};
+  const long long nflat = static_cast<long long>(plan->Hmask) * plan->k_rows + 1;
+  p.src[0] = ws.cu_krows;   p.dst[0] = plan->cu_krows;   p.count[0] = g.batch + 1;
+  p.src[1] = ws.krow_batch; p.dst[1] = plan->krow_batch; p.count[1] = plan->k_rows;
+  p.src[2] = ws.kp_off;     p.dst[2] = plan->kp_off;     p.count[2] = nflat;
+  p.src[3] = ws.kf_off;     p.dst[3] = plan->kf_off;     p.count[3] = nflat;
+  p.vis_bits = ws.vis_bits;
+  p.full_bits = ws.full_bits;
+  p.seq = ws.seq;
+  p.cu_krows = ws.cu_krows;
+  p.krow_batch = ws.krow_batch;
+  p.kp_off = ws.kp_off;
+  p.kf_off = ws.kf_off;
+  p.rows_ub = ws.rows_ub;
+  p.nq_max = ws.nq_max;
+  p.words = ws.words;
+  p.p_off = plan->p_off;
+  p.payload = plan->payload;
+  p.kp_idx = plan->kp_idx;
+  p.kf_idx = plan->kf_idx;
+  p.dq_order = plan->dq_order;
+  p.dq_order_full = plan->dq_order_full;
+  p.kpayload = plan->kpayload;
+  p.rows = static_cast<int>(plan->rows);
+  p.k_rows = static_cast<int>(plan->k_rows);
+  const dim3 grid(plan->k_rows > 0 ? static_cast<unsigned>(plan->k_rows) : 1u, plan->Hmask);
+  k_back_k2q<<<grid, 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -122,6 +122,23 @@ int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func,
                             void* stream, fa_plan** out);
 
 /*
+ * Same as fa_plan_build_intervals with build flags.  FA_PLAN_BACKWARD also
+ * builds the backward views of "Flex Attention Mask Plan Design" §4.4 and
+ * §4.7 for the training consumers (§6.3): the K2Q view (for every K plan
+ * row, i.e. mask head x sample x 128-key tile, independent ascending CSR
+ * lists of the partial and full 128-row Q tiles), its key-major packed
+ * predicate, and the dQ write order.  The backward consumers use the
+ * forward's tile geometry, so the dQ consumer reads the forward Q2K view.
+ * The header then reads {fwd Q rows, fwd partial nnz, fwd full nnz, bwd Q
+ * rows, bwd K rows, bwd partial nnz, bwd full nnz, error}.  Unknown flags
+ * return FA_ERR_INVALID_ARG.
+ */
+#define FA_PLAN_BACKWARD 1u
+int fa_plan_build_intervals_ex(const fa_geometry* geom, const int32_t* mask_func, int32_t Hmask,
+                               int32_t nfunc, uint32_t flags, const fa_allocator* allocator, void* stream,
+                               fa_plan** out);
+
+/*
  * Build a plan from a logical block-pair mask ("Decoupling Logical Masks
  * from GPU Execution for Dynamic Block-Sparse Attention" §2: mask M with
  * logical geometry B = (block_q, block_kv), effective set E(M); physical
@@ -136,6 +153,10 @@ int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func,
 int fa_plan_build_blocks(const fa_geometry* geom, const uint8_t* block_mask, int32_t Hmask,
                          int32_t block_q, int32_t block_kv, const fa_allocator* allocator,
                          void* stream, fa_plan** out);
+/* Same with build flags (FA_PLAN_BACKWARD: see fa_plan_build_intervals_ex). */
+int fa_plan_build_blocks_ex(const fa_geometry* geom, const uint8_t* block_mask, int32_t Hmask,
+                            int32_t block_q, int32_t block_kv, uint32_t flags, const fa_allocator* allocator,
+                            void* stream, fa_plan** out);
 
 /*
  * Release a plan ("Flex Attention Mask Plan Design" §8 Ownership: the plan
@@ -231,6 +252,32 @@ typedef struct {
 } fa_plan_host_view;
 
 int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);
+
+/*
+ * Debug snapshot of the backward views ("Flex Attention Mask Plan Design"
+ * §4.7) of a plan built with FA_PLAN_BACKWARD (FA_ERR_INVALID_ARG
+ * otherwise).  Sizes, with KR = header[4], KP = header[5], KF = header[6]:
+ *   cu_k_rows [batch+1] (K plan rows per sample: ceil(k_len / 128)),
+ *   partial_offset / full_offset [Hm*KR+1] (row-major over (mask head,
+ *   K row)), partial_idx [KP], full_idx [KF] (sample-local Q tiles,
+ *   ascending per K row), payload [KP*128*4] (entry e, key column c, word w:
+ *   bit l = query row 32*w+l of the tile is visible for key c),
+ *   dq_write_order [KP], dq_write_order_full [KF] (parallel to the lists:
+ *   rank of the entry's K tile among its Q tile's non-empty K tiles in
+ *   ascending order, a legal order for accumulating dQ).  Synchronous.
+ */
+typedef struct {
+  int32_t* cu_k_rows;
+  int32_t* partial_offset;
+  int32_t* partial_idx;
+  int32_t* full_offset;
+  int32_t* full_idx;
+  uint32_t* payload;
+  int32_t* dq_write_order;
+  int32_t* dq_write_order_full;
+} fa_plan_bwd_host_view;
+
+int fa_plan_export_backward(const fa_plan* plan, fa_plan_bwd_host_view* dst);
 
 /*
  * Error bits written by the forward kernels on the current device (bit 0:

@@ -64,23 +64,15 @@ class BackwardView:
         return [self.k_rows, int(self.partial_idx.size), int(self.full_idx.size)]
 
 
-def _tile_classes(vis: np.ndarray, T_Q: int, T_KV: int, nq: int, nk: int):
-    """Dense visibility [q_len, k_len] -> (tiles bool [nq, T_Q, nk, T_KV], class [nq, nk])
-    with class 0 empty, 1 partial, 2 full."""
-    q_len, k_len = vis.shape
-    d = np.zeros((nq * T_Q, nk * T_KV), dtype=bool)
-    d[:q_len, :k_len] = vis
-    tiles = d.reshape(nq, T_Q, nk, T_KV)
-    anyv = tiles.any(axis=(1, 3))
-    allv = tiles.all(axis=(1, 3))
-    cls = np.where(allv, 2, np.where(anyv, 1, 0))
-    return tiles, cls
+def build_backward_view(w, T_Q: int = 128, T_KV: int = 128, mask_heads=None) -> BackwardView:
+    """K2Q view, its payload and the dQ write order, by dense expansion of the
+    mask one Q tile strip at a time (every element of every tile is tested).
 
-
-def build_backward_view(w, T_Q: int = 128, T_KV: int = 128) -> BackwardView:
-    """K2Q view, its payload and the dQ write order, by dense expansion of the mask."""
+    ``mask_heads`` restricts the build to those heads, in that order (for
+    building large views one head per process)."""
     bounds = w.sample_bounds()
     B = len(bounds)
+    heads = list(range(w.Hmask)) if mask_heads is None else list(mask_heads)
     k_rows_b = np.array([-(-kl // T_KV) for (_, _, _, kl) in bounds], dtype=np.int64)
     q_rows_b = np.array([-(-ql // T_Q) for (_, ql, _, _) in bounds], dtype=np.int64)
     cu_k_rows = np.concatenate([[0], np.cumsum(k_rows_b)]).astype(np.int64)
@@ -88,46 +80,74 @@ def build_backward_view(w, T_Q: int = 128, T_KV: int = 128) -> BackwardView:
     krow_batch = np.repeat(np.arange(B), k_rows_b)
     krow_nblock = np.concatenate([np.arange(n) for n in k_rows_b]) if k_rows else np.zeros(0, np.int64)
     nw = -(-T_Q // 32)
-    p_cnt = np.zeros((w.Hmask, k_rows), np.int64)
-    f_cnt = np.zeros((w.Hmask, k_rows), np.int64)
-    p_lists, f_lists, pays, p_ord, f_ord = [], [], [], [], []
-    for hm in range(w.Hmask):
+    # per (head slot, K row): lists of (Q tile, rank, payload or None) in ascending Q tile order
+    plist = [[[] for _ in range(k_rows)] for _ in heads]
+    flist = [[[] for _ in range(k_rows)] for _ in heads]
+    for slot, hm in enumerate(heads):
         for b, (q_off, q_len, k_off, k_len) in enumerate(bounds):
             nq, nk = int(q_rows_b[b]), int(k_rows_b[b])
-            if nk == 0:
-                continue
-            vis = M.visible_rows(w, hm, b, np.arange(q_len)) if q_len else np.zeros((0, k_len), bool)
-            tiles, cls = _tile_classes(vis, T_Q, T_KV, nq, nk)
-            # rank of K tile j among the non-empty K tiles of Q tile i (ascending K)
-            nonempty = cls > 0
-            rank = np.cumsum(nonempty, axis=1) - 1
-            for j in range(nk):
-                r = int(cu_k_rows[b]) + j
-                pi = np.nonzero(cls[:, j] == 1)[0]
-                fi = np.nonzero(cls[:, j] == 2)[0]
-                p_cnt[hm, r], f_cnt[hm, r] = pi.size, fi.size
-                p_lists.append(pi)
-                f_lists.append(fi)
-                p_ord.append(rank[pi, j])
-                f_ord.append(rank[fi, j])
-                for i in pi:
-                    t = tiles[i, :, j, :]                       # [T_Q rows, T_KV keys]
-                    padded = np.zeros((T_KV, nw * 32), dtype=bool)
-                    padded[:, :T_Q] = t.T                       # key-major
-                    words = np.packbits(padded, axis=1, bitorder="little").view("<u4")
-                    pays.append(words.reshape(T_KV, nw).astype(np.uint32))
+            for i in range(nq):
+                rows = np.arange(i * T_Q, min((i + 1) * T_Q, q_len))
+                vis = M.visible_rows(w, hm, b, rows)
+                strip = np.zeros((T_Q, nk * T_KV), dtype=bool)
+                strip[:rows.size, :k_len] = vis
+                tiles = strip.reshape(T_Q, nk, T_KV)
+                anyv = tiles.any(axis=(0, 2))
+                allv = tiles.all(axis=(0, 2))
+                rank = np.cumsum(anyv) - 1         # rank among the strip's non-empty K tiles
+                for j in np.nonzero(anyv)[0]:
+                    r = int(cu_k_rows[b]) + int(j)
+                    if allv[j]:
+                        flist[slot][r].append((i, int(rank[j])))
+                    else:
+                        padded = np.zeros((T_KV, nw * 32), dtype=bool)
+                        padded[:, :T_Q] = tiles[:, j, :].T      # key-major
+                        words = np.packbits(padded, axis=1, bitorder="little").view("<u4")
+                        plist[slot][r].append((i, int(rank[j]), words.reshape(T_KV, nw).astype(np.uint32)))
 
-    def _csr(cnt):
+    def _csr(lists):
+        cnt = np.array([[len(x) for x in per] for per in lists], np.int64).reshape(-1)
         off = np.zeros(cnt.size + 1, np.int64)
-        off[1:] = np.cumsum(cnt.reshape(-1))
+        off[1:] = np.cumsum(cnt)
         return off
 
-    cat = lambda xs: np.concatenate(xs).astype(np.int64) if xs else np.zeros(0, np.int64)
-    payload = np.stack(pays) if pays else np.zeros((0, T_KV, nw), np.uint32)
-    fwd_rows = int(q_rows_b.sum())
-    return BackwardView(T_Q, T_KV, w.Hmask, k_rows, cu_k_rows, krow_batch, krow_nblock, _csr(p_cnt),
-                        _csr(f_cnt), cat(p_lists), cat(f_lists), payload, cat(p_ord), cat(f_ord),
-                        fwd_rows)
+    flat_p = [e for per in plist for row in per for e in row]
+    flat_f = [e for per in flist for row in per for e in row]
+    payload = (np.stack([e[2] for e in flat_p]) if flat_p else np.zeros((0, T_KV, nw), np.uint32))
+    return BackwardView(T_Q, T_KV, len(heads), k_rows, cu_k_rows, krow_batch, krow_nblock, _csr(plist),
+                        _csr(flist), np.array([e[0] for e in flat_p], np.int64),
+                        np.array([e[0] for e in flat_f], np.int64), payload,
+                        np.array([e[1] for e in flat_p], np.int64), np.array([e[1] for e in flat_f], np.int64),
+                        int(q_rows_b.sum()))
+
+
+def _one_head(args):
+    w, T_Q, T_KV, hm = args
+    return build_backward_view(w, T_Q, T_KV, mask_heads=[hm])
+
+
+def build_backward_view_by_heads(w, T_Q: int = 128, T_KV: int = 128, processes: int = 8) -> BackwardView:
+    """Same result as build_backward_view(w), one mask head per spawned worker
+    (``w`` mask-only); per-head parts concatenate in head order, the layout
+    of the row-major (mask head, K row) CSR."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(processes) as pool:
+        parts = pool.map(_one_head, [(w, T_Q, T_KV, hm) for hm in range(w.Hmask)])
+    first = parts[0]
+
+    def _merge(offs):
+        out, base = [np.zeros(1, np.int64)], 0
+        for o in offs:
+            out.append(o[1:] + base)
+            base += int(o[-1])
+        return np.concatenate(out)
+
+    cat = lambda f: np.concatenate([getattr(q, f) for q in parts])
+    return BackwardView(T_Q, T_KV, w.Hmask, first.k_rows, first.cu_k_rows, first.krow_batch,
+                        first.krow_nblock, _merge([q.partial_offset for q in parts]),
+                        _merge([q.full_offset for q in parts]), cat("partial_idx"), cat("full_idx"),
+                        cat("payload"), cat("dq_write_order"), cat("dq_write_order_full"), first.fwd_rows)
 
 
 def visible_from_k2q(v: BackwardView, hm: int, b: int, q_len: int, k_len: int) -> np.ndarray:

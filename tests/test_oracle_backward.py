@@ -174,3 +174,13 @@ def test_k2q_payload_single_element():
     want[70, 0] = 1 << 5
     assert np.array_equal(v.payload[0], want)
     assert v.dq_write_order.tolist() == [0]
+
+
+def test_backward_view_by_heads_equals_single_pass():
+    w = _interval_case()
+    one = OB.build_backward_view(w)
+    merged = OB.build_backward_view_by_heads(w.mask_only(), processes=2)
+    for f in ("partial_offset", "full_offset", "partial_idx", "full_idx", "payload", "dq_write_order",
+              "dq_write_order_full", "cu_k_rows"):
+        assert np.array_equal(getattr(one, f), getattr(merged, f)), f
+    assert one.k_rows == merged.k_rows
