@@ -113,6 +113,8 @@ def lib():
                                               P(FaAllocator), _vp, P(_vp)]
         L.fa_plan_export_backward.argtypes = [_vp, P(FaPlanBwdHostView)]
         L.fa_plan_free.argtypes = [_vp, _vp]
+        L.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, P(FaGeometry), _c.c_float,
+                             P(FaMods), _vp]
         L.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, P(FaGeometry), _c.c_float, P(FaMods), _vp]
         L.fa_plan_info_get.argtypes = [_vp, _i32, _vp, P(FaPlanInfo)]
         L.fa_plan_export.argtypes = [_vp, P(FaPlanHostView)]
@@ -122,7 +124,7 @@ def lib():
         L.fa_last_error.restype = _c.c_char_p
         L.fa_version.restype = _c.c_char_p
         for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_build_intervals_ex",
-                  "fa_plan_build_blocks_ex", "fa_plan_export_backward", "fa_plan_free", "fa_fwd",
+                  "fa_plan_build_blocks_ex", "fa_plan_export_backward", "fa_plan_free", "fa_fwd", "fa_bwd",
                   "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags",
                   "fa_plan_header_noalloc", "fa_selftest_wait_timeout"):
             getattr(L, f).restype = _c.c_int
@@ -275,6 +277,29 @@ def fa_fwd(plan: Plan, q, k, v, o, lse, geom: FaGeometry, scale: float, softcap:
     _check(lib().fa_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                         _c.byref(geom), float(scale), _c.byref(mods) if mods else None,
                         _stream_handle(stream)))
+
+
+def _mods(softcap, alibi_slopes):
+    flags = 0
+    keep = None
+    if softcap and softcap > 0:
+        flags |= FA_MOD_SOFTCAP
+    if alibi_slopes is not None:
+        flags |= FA_MOD_ALIBI
+        keep = np.ascontiguousarray(alibi_slopes, dtype=np.float32)
+    if not flags:
+        return None, None
+    return FaMods(flags, float(softcap or 0.0), keep.ctypes.data if keep is not None else None), keep
+
+
+def fa_bwd(plan: Plan, q, k, v, o, dout, lse, dq, dk, dv, geom: FaGeometry, scale: float,
+           softcap: float = 0.0, alibi_slopes=None, stream=None):
+    """Launch the backward (plan built with backward=True); dq, dk, dv are written."""
+    mods, keep = _mods(softcap, alibi_slopes)
+    _check(lib().fa_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                        _ptr(dq), _ptr(dk), _ptr(dv), _c.byref(geom), float(scale),
+                        _c.byref(mods) if mods else None, _stream_handle(stream)))
+    del keep
 
 
 def fa_plan_info_get(plan: Plan, count_visible: bool = False, stream=None) -> dict:

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libbsm_fa.so")
 BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
-SOURCES = ["fa_api.cu", "planner.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu"]
+SOURCES = ["fa_api.cu", "planner.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu", "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

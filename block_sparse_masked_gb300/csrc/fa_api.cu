@@ -565,6 +565,69 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
   return FA_OK;
 }
 
+int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, const fa_geometry* geom, float scale,
+           const fa_mods* mods, void* stream) {
+  t_err.clear();
+  if (!plan) return fail(FA_ERR_INVALID_ARG, "plan is NULL");
+  if (!plan->backward) return fail(FA_ERR_PLAN_MISMATCH, "the plan was built without FA_PLAN_BACKWARD");
+  if (int e = check_geometry(geom)) return e;
+  const bsm::Geometry g = to_geom(geom);
+  const bsm::Geometry& pg = plan->geom;
+  if (g.layout != pg.layout || g.batch != pg.batch || g.seqlen_q != pg.seqlen_q || g.seqlen_k != pg.seqlen_k ||
+      g.total_q != pg.total_q || g.total_k != pg.total_k || g.heads_q != pg.heads_q ||
+      g.heads_k != pg.heads_k || g.head_dim != pg.head_dim || g.dtype != pg.dtype)
+    return fail(FA_ERR_PLAN_MISMATCH, "geometry differs from the plan's");
+  if (plan->signature != bsm::Signature{}.hash())
+    return fail(FA_ERR_PLAN_MISMATCH, "plan signature differs from this consumer's");
+  if (g.head_dim != 128) return fail(FA_ERR_UNSUPPORTED, "the backward supports head_dim 128");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != plan->device) return fail(FA_ERR_PLAN_MISMATCH, "plan was built on device %d", plan->device);
+  if (!(scale > 0.0f) || !std::isfinite(scale))
+    return fail(FA_ERR_INVALID_ARG, "scale must be positive and finite");
+  const long long rows_q = (g.layout == FA_LAYOUT_BSHD) ? static_cast<long long>(g.batch) * g.seqlen_q : g.total_q;
+  const long long rows_k = (g.layout == FA_LAYOUT_BSHD) ? static_cast<long long>(g.batch) * g.seqlen_k : g.total_k;
+  if (rows_q == 0 && rows_k == 0) return FA_OK;
+  for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv)}) {
+    if (!ptr) return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk and dv must be non-NULL");
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return fail(FA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  }
+  bsm::BwdLaunch a{};
+  a.plan = plan;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.scale = scale;
+  if (mods) {
+    a.flags = mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI);
+    a.softcap = mods->softcap;
+    a.slopes = mods->alibi_slopes;
+    if ((a.flags & FA_MOD_SOFTCAP) && !(mods->softcap > 0.0f))
+      return fail(FA_ERR_INVALID_ARG, "softcap must be > 0 when FA_MOD_SOFTCAP is set");
+    if ((a.flags & FA_MOD_ALIBI) && !mods->alibi_slopes)
+      return fail(FA_ERR_INVALID_ARG, "FA_MOD_ALIBI needs alibi_slopes");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Delta workspace [heads_q, total_q], stream-ordered, from the plan's allocator
+  Alloc al{plan->custom_alloc ? &plan->alloc : nullptr, plan->device, st};
+  const size_t dbytes = 4ull * static_cast<size_t>(g.heads_q) * static_cast<size_t>(rows_q > 0 ? rows_q : 1);
+  a.delta = static_cast<float*>(al.get(dbytes));
+  if (!a.delta) return fail(FA_ERR_ALLOC, "backward workspace of %zu bytes", dbytes);
+  const char* why = "";
+  const cudaError_t e = bsm::launch_bwd(a, st, &why);
+  al.put(a.delta, dbytes);
+  if (e) return fail(FA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
+  return FA_OK;
+}
+
 int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream, fa_plan_info* info) {
   t_err.clear();
   if (!plan || !info) return fail(FA_ERR_INVALID_ARG, "plan and info must be non-NULL");

@@ -55,6 +55,7 @@ struct fa_plan {
   fa_allocator alloc{};
   bool custom_alloc = false;
   bsm::DeviceMem mem;
+  bsm::DeviceMem bmem;  // backward view (FA_PLAN_BACKWARD)
   // views into mem
   int32_t* cu_q_rows = nullptr;     // [B+1]
   int32_t* seq_desc = nullptr;      // [B*8]
@@ -71,6 +72,19 @@ struct fa_plan {
   // [P] quadrant (a, s) = rows 64a.. x key columns 64s..: bit 2a+s any element visible, bit 4+2a+s all
   uint8_t* quads = nullptr;
   int32_t block_q = 0, block_kv = 0;  // logical block geometry of a block-mask plan
+  // backward K2Q view ("Flex Attention Mask Plan Design" §4.4, §4.7); absent
+  // (k_rows = 0, null pointers) unless the plan was built with FA_PLAN_BACKWARD
+  bool backward = false;
+  int64_t k_rows = 0, kP = 0, kF = 0;
+  int32_t* cu_krows = nullptr;       // [B+1] K plan row prefix
+  int32_t* krow_batch = nullptr;     // [k_rows] sample of each K row
+  int32_t* kp_off = nullptr;         // [Hmask*k_rows+1]
+  int32_t* kf_off = nullptr;
+  int32_t* kp_idx = nullptr;         // [kP] sample-local Q tiles, ascending per K row
+  int32_t* kf_idx = nullptr;         // [kF]
+  int32_t* dq_order = nullptr;       // [kP] dQ write rank (ascending K order within the Q tile)
+  int32_t* dq_order_full = nullptr;  // [kF]
+  uint32_t* kpayload = nullptr;      // [kP*128*4] key c, word w, bit l = (query 32w+l, key c) visible
 };
 
 namespace bsm {
@@ -94,6 +108,13 @@ struct PlanWorkspace {
   int32_t* cursors;
   int32_t* work;          // schedule output [rows_ub*heads_q*4]
   int rows_ub, nq_max, kt_ub, words;
+  // backward K2Q view; kp_cnt null when not built
+  int32_t* kp_cnt = nullptr;  // [Hmask*B*kt_ub], zero before the front stage
+  int32_t* kf_cnt = nullptr;
+  int32_t* cu_krows = nullptr;    // [B+1]
+  int32_t* krow_batch = nullptr;  // [B*kt_ub]
+  int32_t* kp_off = nullptr;      // [Hmask*B*kt_ub+1]
+  int32_t* kf_off = nullptr;
 };
 
 struct MaskArgs {
@@ -119,6 +140,9 @@ cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmas
 // exact-size copies into the plan, CSR lists, the entry->row map, payloads.
 cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspace& ws, fa_plan* plan,
                         const int32_t* cu_q_src, const int32_t* cu_k_src, cudaStream_t st);
+// K2Q view (FA_PLAN_BACKWARD plans), after launch_back: exact-size copies,
+// Q tile lists with dQ write ranks, key-major payload.
+cudaError_t launch_back_k2q(const Geometry& g, const PlanWorkspace& ws, fa_plan* plan, cudaStream_t st);
 cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, cudaStream_t st);
 
 // ---- forward (attn_fwd*.cu) ---------------------------------------------
@@ -143,6 +167,26 @@ cudaError_t launch_fwd_pair_d128(const FwdLaunch& a, cudaStream_t st, const char
 // d = 128, no score mods (attn_fwd_kt.cu)
 bool fwd_kt_applies(const FwdLaunch& a);
 cudaError_t launch_fwd_kt(const FwdLaunch& a, cudaStream_t st, const char** why);
+// ---- backward (attn_bwd.cu), FA_PLAN_BACKWARD plans, head_dim 128 -----------
+struct BwdLaunch {
+  const fa_plan* plan;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* delta;  // workspace [heads_q, total_q]
+  void* dq;
+  void* dk;
+  void* dv;
+  float scale;
+  int flags;
+  float softcap;
+  const float* slopes;  // host, heads_q
+};
+// Delta, then the dQ kernel (forward Q2K view), then the dK/dV kernel (K2Q view).
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st, const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
 

@@ -11,7 +11,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (FA_LAYOUT_BSHD, FaGeometry, Plan, fa_fwd, fa_plan_build_blocks,
+from . import (FA_LAYOUT_BSHD, FaGeometry, Plan, fa_bwd, fa_fwd, fa_plan_build_blocks,
                fa_plan_build_intervals, geometry)
 from .workloads import Workload
 
@@ -63,3 +63,12 @@ def forward(dp: DeviceProblem, plan: Plan, stream=None):
     fa_fwd(plan, dp.q, dp.k, dp.v, dp.o, dp.lse, dp.geom, w.scale, softcap=w.softcap,
            alibi_slopes=w.alibi_slopes, stream=stream)
     return dp.o, dp.lse
+
+
+def backward(dp: DeviceProblem, plan: Plan, dout: torch.Tensor, stream=None):
+    """Gradients for the forward outputs dp.o / dp.lse: returns (dq, dk, dv)."""
+    w = dp.w
+    dq, dk, dv = torch.empty_like(dp.q), torch.empty_like(dp.k), torch.empty_like(dp.v)
+    fa_bwd(plan, dp.q, dp.k, dp.v, dp.o, dout, dp.lse, dq, dk, dv, dp.geom, w.scale, softcap=w.softcap,
+           alibi_slopes=w.alibi_slopes, stream=stream)
+    return dq, dk, dv

@@ -200,6 +200,28 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
            float* lse, const fa_geometry* geom, float scale, const fa_mods* mods,
            void* stream);
 
+/*
+ * Masked attention backward ("Flex Attention Mask Plan Design" §6.3) for a
+ * plan built with FA_PLAN_BACKWARD (FA_ERR_PLAN_MISMATCH otherwise): the
+ * gradients of FlexAttention Eq. 1 with the same mods as the forward.  A
+ * Q-major kernel walks the forward Q2K view and writes dQ; a K-major kernel
+ * walks the K2Q view and writes dK and dV, summing the Q heads of each K/V
+ * head's group; partial tiles use their packed predicate, full tiles none.
+ * Scores are recomputed from q and k; P = exp(mod(scale QK^T) - lse).
+ *   q, k, v, o, dout: device bf16 in the geometry's layout (o and lse are
+ *   the forward's outputs for these q, k, v); lse: device float32
+ *   [heads_q, total_q]; dq (like q), dk, dv (like k): device bf16, written
+ *   in full (rows and keys without a visible pair get 0).
+ * head_dim 128 only (FA_ERR_UNSUPPORTED otherwise).  A [heads_q, total_q]
+ * float32 workspace comes from the plan's allocator (or the library's
+ * pool) and is returned in stream order.  Asynchronous on `stream`: three
+ * kernel launches (Delta = rowsum(dout * o), dQ, dK/dV).  Pointers must be
+ * 16-byte aligned.
+ */
+int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, const void* o,
+           const void* dout, const float* lse, void* dq, void* dk, void* dv, const fa_geometry* geom,
+           float scale, const fa_mods* mods, void* stream);
+
 /* Plan statistics and layout sizes (Tessera-style mask statistics). */
 typedef struct {
   int64_t header[8];      /* fwd Q rows, partial nnz, full nnz, 0, 0, 0, 0, error flags */
