@@ -184,14 +184,22 @@ def visible_flops(info: dict, Hq: int, d: int) -> float:
 
 def algorithmic_bytes(w, info: dict) -> float:
     """Bytes one forward launch must move at least once: Q, K, V read, O and
-    LSE written, and the plan it reads (CSR offsets and lists, task list and
-    the packed predicate payload of the partial entries)."""
+    LSE written, and the plan it reads (CSR offsets and lists, task list, and
+    the packed predicate payload of the partial entries; the keys-major
+    kernel reads the per-entry quadrant bytes instead and the predicate words
+    only of quadrants that are not fully visible, none for 64-aligned block
+    masks over lengths that are multiples of 64)."""
     qkv = sum(t.numel() * t.element_size() for t in (w.q, w.k, w.v))
     o = w.q.numel() * w.q.element_size()
     lse = 4 * w.Hq * w.total_q
     hdr = info["header"]
     plan_meta = 4 * (2 * (info["mask_heads"] * hdr[0] + 1) + hdr[1] + hdr[2]) + 16 * info["num_tasks"]
-    return float(qkv + o + lse + plan_meta + info["payload_bytes"])
+    if fwd_kernel_name(w).startswith("k_fwd_kt"):
+        aligned = w.Sq % 64 == 0 and w.Sk % 64 == 0
+        payload = hdr[1] + (0 if aligned else info["payload_bytes"])
+    else:
+        payload = info["payload_bytes"]
+    return float(qkv + o + lse + plan_meta + payload)
 
 
 def roofline(flops: float, alg_bytes: float, ms: float, peaks: dict, peak_src: str, traffic):
@@ -250,6 +258,36 @@ def time_plan_builds(fa, runner, dp, flush, stream, reps: int):
     return statistics.median(host_us), statistics.median(gpu_ms)
 
 
+def time_backward(fa, runner, dp, flush, stream, reps: int, fwd_flops: float, peaks: dict):
+    """fa_bwd (Delta, dQ, dK/dV launches) timed alone; TFLOPS on visible pairs
+    with the usual 2.5x-forward count (five d-deep products per pair)."""
+    import torch
+    w = dp.w
+    if w.d != 128:
+        return {"skipped": "the backward supports head_dim 128"}
+    plan = runner.build_plan(dp, backward=True)
+    runner.forward(dp, plan)
+    dout = torch.randn(dp.q.shape, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    for _ in range(2):
+        runner.backward(dp, plan, dout)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for i in range(reps):
+        flush.zero_()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        ev[i][0].record(stream)
+        runner.backward(dp, plan, dout)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    b_us = fa.fa_plan_info_get(plan)["build_us"]
+    plan.free()
+    tf = 2.5 * fwd_flops / (ms * 1e-3) / 1e12
+    return {"bwd_ms": ms, "tflops": tf, "frac_bf16_peak": tf / float(peaks["bf16_tflops"]),
+            "flops_convention": "2.5 x forward visible FLOPs (10 d per visible pair)",
+            "plan_build_us_with_backward_view": b_us, "launches": 3}
+
+
 def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, seed: int):
     """Forward alone, plan build and roofline of every workload (one seed)."""
     import torch
@@ -267,12 +305,13 @@ def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, s
         plan.free()
         b_us, b_ms = time_plan_builds(fa, runner, dp, flush, stream, max(10, reps // 2))
         rf = roofline(flops, algorithmic_bytes(w, info), ms, peaks, peak_src, known_traffic(name))
+        bwd = time_backward(fa, runner, dp, flush, stream, max(5, reps // 2), flops, peaks)
         out[name] = {"workload": WORKLOAD_DESC[name], "fwd_ms": ms, "tflops": rf["tflops"],
                      "frac_bf16_peak": rf["tflops"] / float(peaks["bf16_tflops"]),
                      "bound": rf["bound"], "frac": rf["frac"], "alg_bytes": rf["alg_bytes"],
                      "traffic": rf["traffic"], "plan_build_us": b_us, "plan_gpu_ms": b_ms,
                      "visible_pairs": info["visible_pairs"] * (w.Hq if info["mask_heads"] == 1 else 1),
-                     "kernel": fwd_kernel_name(w)}
+                     "kernel": fwd_kernel_name(w), "backward": bwd}
         del dp, plan, w
         torch.cuda.empty_cache()
     return out

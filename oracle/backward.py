@@ -233,3 +233,19 @@ def attention_grad_full(w, dout):
                 dk[k_off:k_off + k_len, hk, :] += gk
                 dv[k_off:k_off + k_len, hk, :] += gv
     return dq, dk, dv
+
+
+def dq_rows(w, b: int, h: int, rows, dout):
+    """dQ of sample b, Q head h at sample-local rows only (fp64): a row's dQ
+    depends on its own visible keys and its own softmax, so full-size
+    workloads can be checked row by row."""
+    qh, kh, vh = head_slice(w, b, h)
+    rows = np.asarray(rows, np.int64)
+    hm = 0 if w.Hmask == 1 else h
+    vis = M.visible_rows(w, hm, b, rows)
+    q_off = w.sample_bounds()[b][0]
+    do_all = as_f64(dout)
+    do = do_all[b, rows, h, :] if w.layout == 0 else do_all[q_off + rows, h, :]
+    slope = None if w.alibi_slopes is None else float(w.alibi_slopes[h])
+    gq, _, _, _, _ = attention_grad_dense(qh[rows], kh, vh, do, vis, rows, w.scale, w.softcap, slope)
+    return gq

@@ -184,3 +184,17 @@ def test_backward_view_by_heads_equals_single_pass():
               "dq_write_order_full", "cu_k_rows"):
         assert np.array_equal(getattr(one, f), getattr(merged, f)), f
     assert one.k_rows == merged.k_rows
+
+
+def test_dq_rows_equals_full_gradient_rows():
+    n, d = 70, 16
+    g = torch.Generator().manual_seed(3)
+    q, k, v = (torch.randn(1, n, 2, d, generator=g).bfloat16() for _ in range(3))
+    mf = W.random_intervals(4, 1, n, n, 3, 1)
+    w = W.Workload("t", W.LAYOUT_BSHD, 1, n, n, 2, 2, d, q, k, v, 0.25, "intervals", mask_func=mf)
+    w.softcap = 3.0
+    w.alibi_slopes = W.alibi_slopes(2)
+    dout = torch.randn(1, n, 2, d, generator=g).bfloat16()
+    fq, _, _ = OB.attention_grad_full(w, dout)
+    rows = np.array([0, 5, 33, 69])
+    assert np.allclose(OB.dq_rows(w, 0, 1, rows, dout), fq[0, rows, 1, :], atol=1e-12)
