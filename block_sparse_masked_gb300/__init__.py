@@ -14,6 +14,7 @@ Names follow the C entry points:
     fa_plan_info_get(plan, count_visible=False) -> dict
     fa_plan_export(plan) -> dict of numpy arrays
     fa_last_error(), fa_device_error_flags(), fa_version()
+    fa_debug_set_work_desc(plan, task, field, value)   (bounds-checked build only)
 """
 from __future__ import annotations
 
@@ -25,7 +26,10 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libbsm_fa.so")
+# BSM_FA_CHECKED=1 selects the bounds-checked debug build of the same library
+# (build(checked=True)); it must be chosen before the first call.
+LIB_PATH = os.path.join(_HERE, "libbsm_fa_checked.so" if os.environ.get("BSM_FA_CHECKED") == "1"
+                        else "libbsm_fa.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "fa.h")
 
 FA_OK = 0
@@ -100,7 +104,8 @@ def lib():
     global _LIB
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: run `python -m block_sparse_masked_gb300.build`")
+            raise RuntimeError(f"{LIB_PATH} is missing: run `python -m block_sparse_masked_gb300.build`"
+                               + (" --checked" if LIB_PATH.endswith("_checked.so") else ""))
         L = _c.CDLL(LIB_PATH)
         P = _c.POINTER
         L.fa_plan_build_intervals.argtypes = [P(FaGeometry), _vp, _i32, _i32, P(FaAllocator), _vp,
@@ -121,12 +126,13 @@ def lib():
         L.fa_device_error_flags.argtypes = [_vp, P(_u32)]
         L.fa_plan_header_noalloc.argtypes = [P(FaGeometry), _vp, _i32, _i32, _vp, _vp]
         L.fa_selftest_wait_timeout.argtypes = [_u64, _vp]
+        L.fa_debug_set_work_desc.argtypes = [_vp, _c.c_int64, _i32, _i32, _vp]
         L.fa_last_error.restype = _c.c_char_p
         L.fa_version.restype = _c.c_char_p
         for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_build_intervals_ex",
                   "fa_plan_build_blocks_ex", "fa_plan_export_backward", "fa_plan_free", "fa_fwd", "fa_bwd",
                   "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags",
-                  "fa_plan_header_noalloc", "fa_selftest_wait_timeout"):
+                  "fa_plan_header_noalloc", "fa_selftest_wait_timeout", "fa_debug_set_work_desc"):
             getattr(L, f).restype = _c.c_int
         _LIB = L
     return _LIB
@@ -358,6 +364,16 @@ def fa_plan_export(plan: Plan) -> dict:
 def fa_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None):
     """Launch the never-completing bounded wait (see fa.h); read the result with fa_device_error_flags."""
     _check(lib().fa_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)))
+
+
+def fa_debug_set_work_desc(plan: "Plan", task: int, field: int, value: int, stream=None):
+    """Debug build only (see fa.h): overwrite one work_desc field of a plan."""
+    _check(lib().fa_debug_set_work_desc(plan.handle, int(task), int(field), int(value), _stream_handle(stream)))
+
+
+def checked_build() -> bool:
+    """True when the bounds-checked debug library is the one loaded."""
+    return b"bounds-checked" in lib().fa_version()
 
 
 def fa_device_error_flags(stream=None) -> int:

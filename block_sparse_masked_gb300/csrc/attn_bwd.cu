@@ -73,6 +73,8 @@ struct BwdParams {
   __nv_bfloat16* dv;
   uint32_t* err;
   int Hq, Hk, Hmask, rows, k_rows, total_q, ntasks;
+  int B, total_k;                  // samples, K rows of the tensors
+  long long nP, nF, kP, kF;        // Q2K and K2Q entries (bounds of the checked build)
   int flags;
   float scale, scale_log2;
   float y_scale, cap;  // softcap: z = cap * tanh(y_scale * s)
@@ -136,8 +138,8 @@ __device__ __forceinline__ DqTask dq_task(const BwdParams& p, int t) {
   DqTask k;
   const int* wd = p.work + 4LL * t;
   k.m_block = __ldg(wd + 0);
-  k.h = __ldg(wd + 1);
-  k.b = __ldg(wd + 2);
+  k.h = static_cast<int>(bsm_idx(__ldg(wd + 1), p.Hq, p.err));
+  k.b = static_cast<int>(bsm_idx(__ldg(wd + 2), p.B, p.err));
   k.qv = __ldg(wd + 3);
   const int* sq = p.seq + 8 * k.b;
   k.q_off = __ldg(sq + 0);
@@ -145,7 +147,8 @@ __device__ __forceinline__ DqTask dq_task(const BwdParams& p, int t) {
   const int row_begin = __ldg(sq + 4);
   const int hm = (p.Hmask == 1) ? 0 : k.h;
   k.hk = k.h / (p.Hq / p.Hk);
-  const long long flat = static_cast<long long>(hm) * p.rows + row_begin + k.m_block;
+  const long long flat = bsm_idx(static_cast<long long>(hm) * p.rows + row_begin + k.m_block,
+                                 static_cast<long long>(p.Hmask) * p.rows, p.err);
   k.p0 = __ldg(p.p_off + flat);
   k.np = __ldg(p.p_off + flat + 1) - k.p0;
   k.f0 = __ldg(p.f_off + flat);
@@ -266,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j0 = 0; j0 < k.n; j0 += 32) {
         int my_kt = 0;
         if (j0 + lane < k.n)
-          my_kt = (j0 + lane < k.np) ? __ldg(p.p_idx + k.p0 + j0 + lane) : __ldg(p.f_idx + k.f0 + j0 + lane - k.np);
+          my_kt = (j0 + lane < k.np) ? __ldg(p.p_idx + bsm_idx(k.p0 + j0 + lane, p.nP, p.err))
+                                     : __ldg(p.f_idx + bsm_idx(k.f0 + j0 + lane - k.np, p.nF, p.err));
         const int cnt = min(32, k.n - j0);
         for (int jj = 0; jj < cnt; ++jj) {
           const int kt = __shfl_sync(0xffffffffu, my_kt, jj);
@@ -401,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const DqTask k = *tdec;
       named_bar_sync(1, 256);
       if (k.n < 0) break;
-      const bool row_ok = r < k.qv;
       const long long grow = static_cast<long long>(k.q_off) + k.m_block * 128 + r;
+      const bool row_ok = r < k.qv && bsm_ok(grow, p.total_q, p.err);
       __nv_bfloat16* dqrow = p.dq + (grow * p.Hq + k.h) * D + wg * 64;
       if (k.n == 0) {
         if (row_ok) {
@@ -422,9 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool partial = j < k.np;
         uint2 pw = make_uint2(~0u, ~0u);
         if (partial)
-          pw = __ldg(reinterpret_cast<const uint2*>(p.payload + static_cast<long long>(k.p0 + j) * 512 + r * 4) + wg);
+          pw = __ldg(reinterpret_cast<const uint2*>(p.payload + bsm_idx(k.p0 + j, p.nP, p.err) * 512 + r * 4) + wg);
         const int kt = (MODS && (p.flags & FA_MOD_ALIBI))
-                           ? (partial ? __ldg(p.p_idx + k.p0 + j) : __ldg(p.f_idx + k.f0 + j - k.np))
+                           ? (partial ? __ldg(p.p_idx + bsm_idx(k.p0 + j, p.nP, p.err))
+                                      : __ldg(p.f_idx + bsm_idx(k.f0 + j - k.np, p.nF, p.err)))
                            : 0;
         mbar_wait(b_sfull + 8 * sb, (g >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
         tc_fence_after();
@@ -503,7 +508,8 @@ struct KvWalk {
   __device__ __forceinline__ void load(const BwdParams& p, int hk, int krow) {
     const int h = hk * (p.Hq / p.Hk) + g;
     const int hm = (p.Hmask == 1) ? 0 : h;
-    const long long flat = static_cast<long long>(hm) * p.k_rows + krow;
+    const long long flat = bsm_idx(static_cast<long long>(hm) * p.k_rows + krow,
+                                   static_cast<long long>(p.Hmask) * p.k_rows, p.err);
     p0 = __ldg(p.kp_off + flat);
     np_g = __ldg(p.kp_off + flat + 1) - p0;
     f0 = __ldg(p.kf_off + flat);
@@ -530,9 +536,12 @@ struct KvWalk {
   __device__ __forceinline__ int head(const BwdParams& p, int hk) const { return hk * (p.Hq / p.Hk) + g; }
   __device__ __forceinline__ bool partial() const { return e < np_g; }
   __device__ __forceinline__ int qtile(const BwdParams& p) const {
-    return partial() ? __ldg(p.kp_idx + p0 + e) : __ldg(p.kf_idx + f0 + e - np_g);
+    return partial() ? __ldg(p.kp_idx + bsm_idx(p0 + e, p.kP, p.err))
+                     : __ldg(p.kf_idx + bsm_idx(f0 + e - np_g, p.kF, p.err));
   }
-  __device__ __forceinline__ long long entry() const { return static_cast<long long>(p0) + e; }
+  __device__ __forceinline__ long long entry(const BwdParams& p) const {
+    return bsm_idx(static_cast<long long>(p0) + e, p.kP, p.err);
+  }
 };
 
 template <bool MODS>
@@ -565,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // read the same heads' Q and dO
   const int hk = static_cast<int>(blockIdx.x / p.k_rows);
   const int krow = static_cast<int>(blockIdx.x % p.k_rows);
-  const int b = __ldg(p.krow_batch + krow);
+  const int b = static_cast<int>(bsm_idx(__ldg(p.krow_batch + krow), p.B, p.err));
   const int kt = krow - __ldg(p.cu_krows + b);
   const int* sq = p.seq + 8 * b;
   const int q_off = __ldg(sq + 0), k_off = __ldg(sq + 1), q_len = __ldg(sq + 2), k_len = __ldg(sq + 3);
@@ -623,8 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 4; ++i) {
         const int rr = lane + 32 * i;
         const long long idx = static_cast<long long>(h) * p.total_q + q0 + rr;
-        lse_s[rr] = rr < qv ? __ldg(p.lse + idx) * kLog2e : INFINITY;
-        del_s[rr] = rr < qv ? __ldg(p.delta + idx) : 0.0f;
+        const bool in = rr < qv && bsm_ok(q0 + rr, p.total_q, p.err);
+        lse_s[rr] = in ? __ldg(p.lse + idx) * kLog2e : INFINITY;
+        del_s[rr] = in ? __ldg(p.delta + idx) : 0.0f;
       }
       __syncwarp();
       if (leader && !*abort_flag) {
@@ -711,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float slope_l2 = (MODS && (p.flags & FA_MOD_ALIBI)) ? p.slopes[h] * kLog2e : 0.0f;
       uint2 pw = make_uint2(~0u, ~0u);
       if (partial)
-        pw = __ldg(reinterpret_cast<const uint2*>(p.kpayload + wk.entry() * 512 + t * 4) + wg);
+        pw = __ldg(reinterpret_cast<const uint2*>(p.kpayload + wk.entry(p) * 512 + t * 4) + wg);
       const float* lse_s = reinterpret_cast<const float*>(gbase + kKvOffRing + st * kKvStageBytes + 2 * kTileBytes);
       const float* del_s = lse_s + 128;
       mbar_wait(b_full + 8 * st, (s / kKvStages) & 1, abort_flag, p.err, kWaitTimeoutNs);  // LSE, Delta
@@ -748,8 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(b_accdone, (s - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
       tc_fence_after();
     }
-    const bool key_ok = t < kv;
     const long long krow_g = static_cast<long long>(k_off) + kt * 128 + t;
+    const bool key_ok = t < kv && bsm_ok(krow_g, p.total_k, p.err);
     __nv_bfloat16* dkrow = p.dk + (krow_g * p.Hk + hk) * D + wg * 64;
     __nv_bfloat16* dvrow = p.dv + (krow_g * p.Hk + hk) * D + wg * 64;
 #pragma unroll
@@ -890,6 +900,12 @@ cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st, const char** why) {
   p.k_rows = static_cast<int>(pl->k_rows);
   p.total_q = static_cast<int>(rows_q);
   p.ntasks = static_cast<int>(pl->tasks);
+  p.B = g.batch;
+  p.total_k = static_cast<int>(rows_k);
+  p.nP = pl->P;
+  p.nF = pl->F;
+  p.kP = pl->kP;
+  p.kF = pl->kF;
   p.flags = a.flags;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;

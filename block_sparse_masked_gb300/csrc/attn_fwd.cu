@@ -96,6 +96,8 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int Hq, Hk, Hmask, rows, total_q, ntasks;
+  int B;             // samples
+  long long nP, nF;  // partial and full entries of the plan (bounds of the checked build)
   int flags;
   float scale;       // multiplies Q K^T
   float scale_log2;  // scale * log2(e)
@@ -116,8 +118,8 @@ __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
   Task k;
   const int* wd = p.work + 4LL * t;
   k.m_block = wd[0];
-  k.h = wd[1];
-  k.b = wd[2];
+  k.h = static_cast<int>(bsm_idx(wd[1], p.Hq, &g_fwd_err));
+  k.b = static_cast<int>(bsm_idx(wd[2], p.B, &g_fwd_err));
   k.qv = wd[3];
   const int* sq = p.seq + 8 * k.b;
   k.q_off = sq[0];
@@ -125,7 +127,9 @@ __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
   const int row_begin = sq[4];
   const int hm = (p.Hmask == 1) ? 0 : k.h;
   k.hk = k.h / (p.Hq / p.Hk);
-  const long long flat = static_cast<long long>(hm) * p.rows + row_begin + k.m_block;
+  const long long flat =
+      bsm_idx(static_cast<long long>(hm) * p.rows + row_begin + k.m_block, static_cast<long long>(p.Hmask) * p.rows,
+              &g_fwd_err);
   k.p0 = p.p_off[flat];
   k.np = p.p_off[flat + 1] - k.p0;
   k.f0 = p.f_off[flat];
@@ -134,13 +138,14 @@ __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
 }
 
 __device__ __forceinline__ int tile_index(const FwdParams& p, const Task& k, int j) {
-  return (j < k.np) ? __ldg(p.p_idx + k.p0 + j) : __ldg(p.f_idx + k.f0 + (j - k.np));
+  return (j < k.np) ? __ldg(p.p_idx + bsm_idx(k.p0 + j, p.nP, &g_fwd_err))
+                    : __ldg(p.f_idx + bsm_idx(k.f0 + (j - k.np), p.nF, &g_fwd_err));
 }
 // Key halves of tile j that hold a visible element (bit s: keys 64s..64s+63);
 // full tiles use both.  A tile with one empty half loads, multiplies and
 // exponentiates only the other half.
 __device__ __forceinline__ int tile_halves(const FwdParams& p, const Task& k, int j) {
-  return (j < k.np) ? static_cast<int>(__ldg(p.halves + k.p0 + j)) : 3;
+  return (j < k.np) ? static_cast<int>(__ldg(p.halves + bsm_idx(k.p0 + j, p.nP, &g_fwd_err))) : 3;
 }
 
 // Block-mask plans (HALVES): one ring slot, score buffer and P V step
@@ -605,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       group_sync();
       const Task k = tdec[ti & 1];
       if (k.n < 0) break;
-      const bool row_ok = r < k.qv;
       const long long grow = static_cast<long long>(k.q_off) + k.m_block * kTile + r;
+      const bool row_ok = r < k.qv && bsm_ok(grow, p.total_q, &g_fwd_err);
       __nv_bfloat16* orow = p.o + (grow * p.Hq + k.h) * D + wg * OC;
       if (k.n == 0) {
         if (row_ok) {
@@ -797,7 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             q.h = (wg ? hb : ha) >> 1;
           }
           q.pw = make_uint2(~0u, ~0u);
-          if (q.e >= 0 && q.e < k.np) q.pw = __ldg(pay - wg + static_cast<long long>(q.e) * kTile * 2 + q.h);
+          if (q.e >= 0 && q.e < k.np) {
+            const long long e = bsm_idx(k.p0 + q.e, p.nP, &g_fwd_err) - k.p0;
+            q.pw = __ldg(pay - wg + e * kTile * 2 + q.h);
+          }
           q.kt = (MODS && q.e >= 0) ? tile_index(p, k, q.e) : 0;
           return true;
         };
@@ -826,13 +834,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         g += j;
       } else {
         // interval masks: predicate words and K tile fetched one tile ahead
-        uint2 pw_next = (k.np > 0) ? __ldg(pay) : make_uint2(~0u, ~0u);
+        uint2 pw_next = (k.np > 0) ? __ldg(pay + (bsm_idx(k.p0, p.nP, &g_fwd_err) - k.p0) * kTile * 2)
+                                   : make_uint2(~0u, ~0u);
         int kt_next = MODS ? tile_index(p, k, 0) : 0;
         for (int j = 0; j < k.n; ++j) {
           const bool partial = j < k.np;
           const uint2 pw = partial ? pw_next : make_uint2(~0u, ~0u);
           const int kt = kt_next;
-          if (j + 1 < k.np) pw_next = __ldg(pay + static_cast<long long>(j + 1) * kTile * 2);
+          if (j + 1 < k.np) pw_next = __ldg(pay + (bsm_idx(k.p0 + j + 1, p.nP, &g_fwd_err) - k.p0) * kTile * 2);
           if (MODS && j + 1 < k.n) kt_next = tile_index(p, k, j + 1);
           step(j, j, wg, partial, pw, kt);
         }
@@ -973,6 +982,9 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   p.Hmask = pl->Hmask;
   p.rows = static_cast<int>(pl->rows);
   p.total_q = static_cast<int>(rows_q);
+  p.B = g.batch;
+  p.nP = pl->P;
+  p.nF = pl->F;
   p.flags = a.flags;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;

@@ -124,6 +124,8 @@ struct KtParams {
   float* lse;
   uint32_t* err;
   int Hq, Hk, Hmask, rows, total_q, rows_k, ntasks;
+  int B;             // samples
+  long long nP, nF;  // partial and full entries of the plan (bounds of the checked build)
   float scale_log2;
 };
 
@@ -143,10 +145,11 @@ static_assert(sizeof(StepDesc) == 32, "descriptor size");
 constexpr int kFullPos = -1, kEmptyPos = -2;
 
 __device__ __forceinline__ int tile_of(const KtParams& p, int p0, int np, int f0, int j) {
-  return (j < np) ? __ldg(p.p_idx + p0 + j) : __ldg(p.f_idx + f0 + (j - np));
+  return (j < np) ? __ldg(p.p_idx + bsm_idx(p0 + j, p.nP, p.err))
+                  : __ldg(p.f_idx + bsm_idx(f0 + (j - np), p.nF, p.err));
 }
 __device__ __forceinline__ int quads_of(const KtParams& p, int p0, int np, int j) {
-  return (j < np) ? static_cast<int>(__ldg(p.quads + p0 + j)) : 0xFF;  // full tiles: every quadrant full
+  return (j < np) ? static_cast<int>(__ldg(p.quads + bsm_idx(p0 + j, p.nP, p.err))) : 0xFF;  // full tiles: every quadrant full
 }
 
 // Instruction descriptor, kind::f16 with A and B both MN-major (the P V step:
@@ -341,12 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       t = __shfl_sync(0xffffffffu, t, 0);
       if (t < 0 || t >= p.ntasks || *abort_flag) break;
       const int* wd = p.work + 4LL * t;
-      const int m_block = __ldg(wd + 0), h = __ldg(wd + 1), b = __ldg(wd + 2), qv = __ldg(wd + 3);
+      const int m_block = __ldg(wd + 0), qv = __ldg(wd + 3);
+      const int h = static_cast<int>(bsm_idx(__ldg(wd + 1), p.Hq, p.err));
+      const int b = static_cast<int>(bsm_idx(__ldg(wd + 2), p.B, p.err));
       const int* sq = p.seq + 8 * b;
       const int q_off = __ldg(sq + 0), k_off = __ldg(sq + 1), row_begin = __ldg(sq + 4);
       const int hm = (p.Hmask == 1) ? 0 : h;
       const int hk = h / (p.Hq / p.Hk);
-      const long long flat = static_cast<long long>(hm) * p.rows + row_begin + m_block;
+      const long long flat = bsm_idx(static_cast<long long>(hm) * p.rows + row_begin + m_block,
+                                     static_cast<long long>(p.Hmask) * p.rows, p.err);
       const int p0 = __ldg(p.p_off + flat), np = __ldg(p.p_off + flat + 1) - p0;
       const int f0 = __ldg(p.f_off + flat), n = np + (__ldg(p.f_off + flat + 1) - f0);
       for (int qh = 0; qh < 2; ++qh) {
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s.nsteps == 0) {
         // no visible key for any row of this half: O = 0, LSE = -inf
         const int row = cb + t;
-        if (t < kCols && row < s.qv) {
+        if (t < kCols && row < s.qv && bsm_ok(s.q0 + row, p.total_q, p.err)) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<long long>(s.q0 + row) * p.Hq + s.h) * D);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -603,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (e >= 0) {
           const int kc = kHalf * (e & 1) + (t & 63);
           const uint32_t* pw =
-              p.payload + static_cast<long long>(e >> 1) * 512 + (kHalf * s.qh + cb) * 4 + (kc >> 5);
+              p.payload + bsm_idx(e >> 1, p.nP, p.err) * 512 + (kHalf * s.qh + cb) * 4 + (kc >> 5);
           uint32_t bits = 0u;
 #pragma unroll 8
           for (int r = 0; r < kCols; ++r) bits |= ((__ldg(pw + 4 * r) >> (kc & 31)) & 1u) << r;
@@ -704,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float l = (xch[t] + xch[kCols + t]) + (xch[2 * kCols + t] + xch[3 * kCols + t]);
           const bool have = l > 0.0f;
           mnew[cb + t] = have ? 1.0f / l : 0.0f;
-          if (cb + t < s.qv && p.lse != nullptr)
+          if (cb + t < s.qv && p.lse != nullptr && bsm_ok(s.q0 + cb + t, p.total_q, p.err))
             p.lse[static_cast<long long>(s.h) * p.total_q + s.q0 + cb + t] =
                 have ? (mref[cb + t] + __log2f(l)) * kLn2 : -INFINITY;
         }
@@ -738,9 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         group_sync();
         if (t == 0) {
+          if (bsm_ok(s.q0 + cb + kCols - 1, p.total_q, p.err))
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
-            tma_store_2d(&tmOq, sQ + qb * kHalfBytes + ch * 8192 + cb * 128, s.h * D + ch * 64, s.q0 + cb);
+            for (int ch = 0; ch < 2; ++ch)
+              tma_store_2d(&tmOq, sQ + qb * kHalfBytes + ch * 8192 + cb * 128, s.h * D + ch * 64, s.q0 + cb);
           bulk_commit_group();
           store_pending = true;
           pend_qb = qb;
@@ -751,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* orow = p.o + static_cast<long long>(s.q0 + cb) * p.Hq * D + s.h * D + t;
 #pragma unroll
         for (int c = 0; c < kCols; ++c)
-          if (cb + c < s.qv) orow[static_cast<long long>(c) * p.Hq * D] = __float2bfloat16_rn(o[c]);
+          if (cb + c < s.qv && bsm_ok(s.q0 + cb + c, p.total_q, p.err))
+            orow[static_cast<long long>(c) * p.Hq * D] = __float2bfloat16_rn(o[c]);
         group_sync();
         if (t == 0) mbar_arrive(b_qempty + 8 * qb);
       }
@@ -834,6 +842,9 @@ cudaError_t launch_fwd_kt(const FwdLaunch& a, cudaStream_t st, const char** why)
   p.total_q = static_cast<int>(rows_q);
   p.rows_k = static_cast<int>(rows_k);
   p.ntasks = static_cast<int>(pl->tasks);
+  p.B = g.batch;
+  p.nP = pl->P;
+  p.nF = pl->F;
   p.scale_log2 = a.scale * kLog2e;
   if (p.err == nullptr) {
     *why = "forward error word not found";

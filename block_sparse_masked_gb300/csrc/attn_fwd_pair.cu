@@ -100,6 +100,8 @@ struct PairParams {
   float* lse;
   uint32_t* err;     // the forward kernels' error word
   int Hq, Hk, Hmask, rows, total_q, ntasks;
+  int B;             // samples
+  long long nP, nF;  // partial and full entries of the plan (bounds of the checked build)
   float scale_log2;  // scale * log2(e)
 };
 
@@ -124,8 +126,8 @@ __device__ __forceinline__ PairTask load_pair(const PairParams& p, int t) {
     k.skip = 1;
     return k;
   }
-  k.h = wd[1];
-  k.b = wd[2];
+  k.h = static_cast<int>(bsm_idx(wd[1], p.Hq, p.err));
+  k.b = static_cast<int>(bsm_idx(wd[2], p.B, p.err));
   const int* sq = p.seq + 8 * k.b;
   k.q_off = sq[0];
   k.k_off = sq[1];
@@ -137,13 +139,21 @@ __device__ __forceinline__ PairTask load_pair(const PairParams& p, int t) {
     s.m = m + x;
     if (s.m >= nrows) continue;  // no B tile (qv stays 0, lists empty)
     s.qv = min(128, q_len - s.m * 128);
-    const long long flat = static_cast<long long>(hm) * p.rows + row_begin + s.m;
+    const long long flat = bsm_idx(static_cast<long long>(hm) * p.rows + row_begin + s.m,
+                                   static_cast<long long>(p.Hmask) * p.rows, p.err);
     s.p0 = p.p_off[flat];
     s.np = p.p_off[flat + 1] - s.p0;
     s.f0 = p.f_off[flat];
     s.nf = p.f_off[flat + 1] - s.f0;
   }
   return k;
+}
+
+__device__ __forceinline__ int p_entry(const PairParams& p, long long i) {
+  return __ldg(p.p_idx + bsm_idx(i, p.nP, p.err));
+}
+__device__ __forceinline__ int f_entry(const PairParams& p, long long i) {
+  return __ldg(p.f_idx + bsm_idx(i, p.nF, p.err));
 }
 
 // Ascending walk over one tile's K tiles: a merge of its partial list and
@@ -156,10 +166,10 @@ struct OwnWalk {
   __device__ __forceinline__ void init(const PairParams& p, const Half& s) {
     ip = 0;
     jf = 0;
-    kp = (s.np > 0) ? __ldg(p.p_idx + s.p0) : INT_MAX;
-    kf = (s.nf > 0) ? __ldg(p.f_idx + s.f0) : INT_MAX;
-    kp_nx = (s.np > 1) ? __ldg(p.p_idx + s.p0 + 1) : INT_MAX;
-    kf_nx = (s.nf > 1) ? __ldg(p.f_idx + s.f0 + 1) : INT_MAX;
+    kp = (s.np > 0) ? p_entry(p, s.p0) : INT_MAX;
+    kf = (s.nf > 0) ? f_entry(p, s.f0) : INT_MAX;
+    kp_nx = (s.np > 1) ? p_entry(p, s.p0 + 1) : INT_MAX;
+    kf_nx = (s.nf > 1) ? f_entry(p, s.f0 + 1) : INT_MAX;
   }
   __device__ __forceinline__ int head() const { return min(kp, kf); }
   // Takes the head: returns its K tile; *partial_entry = its payload entry or -1
@@ -169,14 +179,14 @@ struct OwnWalk {
       *partial_entry = s.p0 + ip;
       ++ip;
       kp = kp_nx;
-      kp_nx = (ip + 1 < s.np) ? __ldg(p.p_idx + s.p0 + ip + 1) : INT_MAX;
+      kp_nx = (ip + 1 < s.np) ? p_entry(p, s.p0 + ip + 1) : INT_MAX;
       return kt;
     }
     const int kt = kf;
     *partial_entry = -1;
     ++jf;
     kf = kf_nx;
-    kf_nx = (jf + 1 < s.nf) ? __ldg(p.f_idx + s.f0 + jf + 1) : INT_MAX;
+    kf_nx = (jf + 1 < s.nf) ? f_entry(p, s.f0 + jf + 1) : INT_MAX;
     return kt;
   }
 };
@@ -442,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Half& hx = k.t[x];
       if (hx.qv <= 0) continue;  // no B tile in this pair
       const int n = hx.np + hx.nf;
-      const bool row_ok = r < hx.qv;
       const long long grow = static_cast<long long>(k.q_off) + hx.m * 128 + r;
+      const bool row_ok = r < hx.qv && bsm_ok(grow, p.total_q, p.err);
       __nv_bfloat16* orow = p.o + (grow * p.Hq + k.h) * D;
       if (n == 0) {
         if (row_ok) {
@@ -460,14 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint4* pay = reinterpret_cast<const uint4*>(p.payload) + r;  // + entry * 128
       int e_next;
       walk.take(p, hx, &e_next);
-      uint4 pw_next = (e_next >= 0) ? __ldg(pay + static_cast<long long>(e_next) * 128)
+      uint4 pw_next = (e_next >= 0) ? __ldg(pay + bsm_idx(e_next, p.nP, p.err) * 128)
                                     : make_uint4(~0u, ~0u, ~0u, ~0u);
       for (int j = 0; j < n; ++j) {
         const bool partial = e_next >= 0;
         const uint4 pw = pw_next;
         if (j + 1 < n) {  // next own tile, fetched one step ahead
           walk.take(p, hx, &e_next);
-          pw_next = (e_next >= 0) ? __ldg(pay + static_cast<long long>(e_next) * 128)
+          pw_next = (e_next >= 0) ? __ldg(pay + bsm_idx(e_next, p.nP, p.err) * 128)
                                   : make_uint4(~0u, ~0u, ~0u, ~0u);
         }
         mbar_wait(b_sfull + 8 * x, g & 1, abort_flag, p.err, kWaitTimeoutNs);
@@ -642,6 +652,9 @@ cudaError_t launch_pair_impl(const FwdLaunch& a, cudaStream_t st, const char** w
   p.rows = static_cast<int>(pl->rows);
   p.total_q = static_cast<int>(rows_q);
   p.ntasks = static_cast<int>(pl->tasks);
+  p.B = g.batch;
+  p.nP = pl->P;
+  p.nF = pl->F;
   p.scale_log2 = a.scale * kLog2e;
   if (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) {
     *why = "score mods are not supported by the two-tile forward";

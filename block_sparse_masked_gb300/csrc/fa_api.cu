@@ -741,8 +741,35 @@ int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
   return FA_OK;
 }
 
+int fa_debug_set_work_desc(fa_plan* plan, int64_t task, int32_t field, int32_t value, void* stream) {
+  t_err.clear();
+#ifdef BSM_CHECKED
+  if (plan == nullptr || task < 0 || task >= plan->tasks || field < 0 || field > 3)
+    return fail(FA_ERR_INVALID_ARG, "task or field out of range");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(plan->work_desc + 4 * task + field, &value, sizeof(value),
+                                  cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e) return cuda_fail(e, "work_desc write");
+  return FA_OK;
+#else
+  (void)plan;
+  (void)task;
+  (void)field;
+  (void)value;
+  (void)stream;
+  return fail(FA_ERR_UNSUPPORTED, "fa_debug_set_work_desc exists only in the bounds-checked build");
+#endif
+}
+
 const char* fa_last_error(void) { return t_err.c_str(); }
 
-const char* fa_version(void) { return "block_sparse_masked_gb300 0.1 (sm_103a)"; }
+const char* fa_version(void) {
+#ifdef BSM_CHECKED
+  return "block_sparse_masked_gb300 0.1 (sm_103a, bounds-checked)";
+#else
+  return "block_sparse_masked_gb300 0.1 (sm_103a)";
+#endif
+}
 
 }  // extern "C"

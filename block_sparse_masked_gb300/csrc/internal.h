@@ -18,6 +18,30 @@ constexpr int kMaxHeads = 256;        // heads_q limit of the forward kernel par
 enum PlanErr : uint32_t { PLANERR_MASK = 1u, PLANERR_SEQLENS = 2u, PLANERR_OVERFLOW = 4u };
 enum MaskKind : int { MASK_INTERVALS = 0, MASK_BLOCKS = 1 };
 
+// Error bits reported by kernels (the device error word).
+enum : uint32_t { DEVERR_TIMEOUT = 1u, DEVERR_SMEM_ALIGN = 2u, DEVERR_BOUNDS = 4u };
+
+// Debug builds (-DBSM_CHECKED): every plan-derived global index goes through
+// bsm_idx(i, n, err), which returns i when 0 <= i < n and otherwise records
+// DEVERR_BOUNDS in *err and returns 0, so that a read stays in bounds and a
+// guarded write (bsm_ok) is skipped; nothing traps.  Release builds compile
+// both to the plain index.
+#if defined(__CUDACC__) && defined(BSM_CHECKED)
+__device__ __forceinline__ long long bsm_idx(long long i, long long n, uint32_t* err) {
+  if (i >= 0 && i < n) return i;
+  atomicOr(err, DEVERR_BOUNDS);
+  return 0;
+}
+__device__ __forceinline__ bool bsm_ok(long long i, long long n, uint32_t* err) {
+  if (i >= 0 && i < n) return true;
+  atomicOr(err, DEVERR_BOUNDS);
+  return false;
+}
+#elif defined(__CUDACC__)
+__device__ __forceinline__ long long bsm_idx(long long i, long long, uint32_t*) { return i; }
+__device__ __forceinline__ bool bsm_ok(long long, long long, uint32_t*) { return true; }
+#endif
+
 // Consumer signature ("Flex Attention Mask Plan Design" §7): every field
 // that fixes how the plan's topology and payload are laid out for the one
 // consumer this library ships.
@@ -188,6 +212,15 @@ struct BwdLaunch {
 // Delta, then the dQ kernel (forward Q2K view), then the dK/dV kernel (K2Q view).
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st, const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
+// The error word the bounds checks of a checked build (-DBSM_CHECKED)
+// report into; nullptr in a release build, whose checks compile away.
+inline uint32_t* checked_error_word() {
+#ifdef BSM_CHECKED
+  return fwd_error_word();
+#else
+  return nullptr;
+#endif
+}
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t st);
 
 // ---- error reporting and argument checks shared with fa_plan_header_noalloc

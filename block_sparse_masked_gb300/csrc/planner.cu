@@ -505,6 +505,9 @@ struct BackParams {
   // blocks
   const uint8_t* block_mask;
   int block_q, block_kv, nbq, nbk;
+  // bounds of the checked build: plan entries, and the device error word
+  long long nP, nF;
+  uint32_t* err;
 };
 
 // Quadrant bits of one partial entry, per lane and then reduced over the
@@ -672,14 +675,15 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
       while (pb) {
         const int bit = __ffs(pb) - 1;
         pb &= pb - 1;
-        p.p_idx[pp] = w * 32 + bit;
-        p.entry_row[pp] = static_cast<int32_t>(flat);
+        const long long at = bsm_idx(pp, p.nP, p.err);
+        p.p_idx[at] = w * 32 + bit;
+        p.entry_row[at] = static_cast<int32_t>(flat);
         ++pp;
       }
       while (fb) {
         const int bit = __ffs(fb) - 1;
         fb &= fb - 1;
-        p.f_idx[pf++] = w * 32 + bit;
+        p.f_idx[bsm_idx(pf++, p.nF, p.err)] = w * 32 + bit;
       }
       pbase += __shfl_sync(kFull, xp, 31);
       fbase += __shfl_sync(kFull, xf, 31);
@@ -696,7 +700,7 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
   }
   __syncthreads();  // the row's p_idx (written by warp 0) and sF are visible to the CTA
   for (int k = wi; k < np; k += 4) {
-    const long long e = pstart + k;
+    const long long e = bsm_idx(pstart + k, p.nP, p.err);
     const int j = p.p_idx[e];
     QuadBits qb;
     if (KIND == MASK_INTERVALS)
@@ -743,6 +747,10 @@ struct K2QParams {
   int32_t* dq_order_full;
   uint32_t* kpayload;        // [P'*128*4]: key c, word w, bit l = (query 32w+l, key c) visible
   int rows, k_rows;
+  // bounds of the checked build: Q2K partial entries, K2Q partial and full
+  // entries, and the device error word
+  long long nP, kP, kF;
+  uint32_t* err;
 };
 
 __device__ __forceinline__ int popc_below(const uint32_t* wv, int j) {
@@ -790,12 +798,12 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
       const uint32_t bp = __ballot_sync(kFull, isp), bf = __ballot_sync(kFull, isf);
       const uint32_t below = (1u << lane) - 1u;
       if (isp) {
-        const int e = pb + __popc(bp & below);
+        const long long e = bsm_idx(pb + __popc(bp & below), p.kP, p.err);
         p.kp_idx[e] = i;
         p.dq_order[e] = rank;
       }
       if (isf) {
-        const int e = fb + __popc(bf & below);
+        const long long e = bsm_idx(fb + __popc(bf & below), p.kF, p.err);
         p.kf_idx[e] = i;
         p.dq_order_full[e] = rank;
       }
@@ -805,12 +813,13 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
   }
   __syncthreads();  // warp 0's Q tile lists are visible to the CTA
   for (int k = wi; k < np; k += 4) {
-    const long long e = pstart + k;
+    const long long e = bsm_idx(pstart + k, p.kP, p.err);
     const int i = p.kp_idx[e];
     const uint32_t* wv = p.vis_bits + (qrow0 + i) * p.words;
     const uint32_t* wf = p.full_bits + (qrow0 + i) * p.words;
-    const long long eq = __ldg(p.p_off + static_cast<long long>(hm) * p.rows + row_begin + i) +
-                         popc_partial_below(wv, wf, j);
+    const long long eq = bsm_idx(__ldg(p.p_off + static_cast<long long>(hm) * p.rows + row_begin + i) +
+                                     popc_partial_below(wv, wf, j),
+                                 p.nP, p.err);
     const uint32_t* src = p.payload + eq * (kTile * kPayloadWords);
     uint32_t mine[kPayloadWords][kPayloadWords];  // [key chunk][query word] for key 32 chunk + lane
 #pragma unroll
@@ -846,6 +855,7 @@ struct SchedParams {
   int32_t* work;     // [tasks*4]
   int B, Hq, Hk, Hmask, C, NS;
   int in_smem;       // 1: histogram and cursors live in dynamic shared memory (2*NS*(C+1) ints)
+  uint32_t* err;     // device error word (checked build)
 };
 
 __device__ __forceinline__ int task_cost(const SchedParams& p, int rows, int h, int row) {
@@ -961,7 +971,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
         const unsigned same = __match_any_sync(amask, bucket);
         const int rank = __popc(same & ((1u << lane) - 1));
         const int pos = cur[bucket] + rank;
-        int32_t* wd = p.work + 4LL * pos;
+        int32_t* wd = p.work + 4LL * bsm_idx(pos, static_cast<long long>(p.Hq) * rows, p.err);
         wd[0] = m;
         wd[1] = h;
         wd[2] = b;
@@ -1046,7 +1056,7 @@ cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmas
                             int max_cost, cudaStream_t st) {
   if (ws.rows_ub == 0) return cudaSuccess;
   SchedParams p{ws.seq, ws.cu_rows, ws.p_off, ws.f_off, ws.hist, ws.cursors, ws.work,
-                g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections, 0};
+                g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections, 0, checked_error_word()};
   // histogram and cursors in shared memory when they fit (shared-memory
   // atomics and the single CTA's scans then stay on chip)
   constexpr size_t kSchedSmemMax = 160 * 1024;
@@ -1110,6 +1120,9 @@ cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspac
   p.block_kv = m.block_kv;
   p.nbq = m.nbq;
   p.nbk = m.nbk;
+  p.nP = plan->P;
+  p.nF = plan->F;
+  p.err = checked_error_word();
   const dim3 grid(rows > 0 ? rows : 1, rows > 0 ? m.Hmask : 1);
   if (m.kind == MASK_INTERVALS)
     k_back<MASK_INTERVALS><<<grid, 128, 0, st>>>(p);
@@ -1144,6 +1157,10 @@ cudaError_t launch_back_k2q(const Geometry& g, const PlanWorkspace& ws, fa_plan*
   p.kpayload = plan->kpayload;
   p.rows = static_cast<int>(plan->rows);
   p.k_rows = static_cast<int>(plan->k_rows);
+  p.nP = plan->P;
+  p.kP = plan->kP;
+  p.kF = plan->kF;
+  p.err = checked_error_word();
   const dim3 grid(plan->k_rows > 0 ? static_cast<unsigned>(plan->k_rows) : 1u, plan->Hmask);
   k_back_k2q<<<grid, 128, 0, st>>>(p);
   return cudaGetLastError();

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "internal.h"
+
 namespace bsm {
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
@@ -84,8 +86,7 @@ __device__ __forceinline__ int clc_response(uint32_t resp) {
   return ok ? static_cast<int>(x) : -1;
 }
 
-// Error bits reported by kernels.
-enum : uint32_t { DEVERR_TIMEOUT = 1u, DEVERR_SMEM_ALIGN = 2u };
+// Error bits (DEVERR_*) and the checked-build index helpers are in internal.h.
 
 // A wait that always ends: it gives up once `*abort` is set by another
 // role of the CTA, or after `timeout_ns` of global time, in which case it

@@ -302,11 +302,14 @@ typedef struct {
 int fa_plan_export_backward(const fa_plan* plan, fa_plan_bwd_host_view* dst);
 
 /*
- * Error bits written by the forward kernels on the current device (bit 0:
+ * Error bits written by the library's kernels on the current device (bit 0:
  * a bounded in-kernel wait ran out and the kernel stopped early, so its
  * output is incomplete; bit 1: dynamic shared memory was not aligned as
- * the kernel requires, so it did no work).  Synchronises `stream`, returns the bits in
- * *flags and clears them.
+ * the kernel requires, so it did no work; bit 2, only in the bounds-checked
+ * debug build libbsm_fa_checked.so: a planner, forward or backward kernel
+ * computed a plan-derived global index outside the plan's exact sizes, and
+ * the access was redirected or skipped).  Synchronises `stream`, returns
+ * the bits in *flags and clears them.
  */
 int fa_device_error_flags(void* stream, uint32_t* flags);
 
@@ -318,6 +321,18 @@ int fa_device_error_flags(void* stream, uint32_t* flags);
  * with fa_device_error_flags.  Nothing faults, traps or hangs.
  */
 int fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/*
+ * Debug only (the bounds-checked build libbsm_fa_checked.so; the release
+ * build returns FA_ERR_UNSUPPORTED and changes nothing): overwrites field
+ * `field` (0 Q tile, 1 head, 2 sample, 3 valid rows) of task `task` of the
+ * plan's work_desc with `value`, synchronously on `stream`.  It breaks the
+ * plan's immutability on purpose, so that tests can check that an
+ * out-of-range head or sample is caught by the kernels' index checks (bit
+ * 2 of the device error flags) instead of being used.  FA_ERR_INVALID_ARG
+ * when the task or field is out of range.
+ */
+int fa_debug_set_work_desc(fa_plan* plan, int64_t task, int32_t field, int32_t value, void* stream);
 
 /*
  * Allocation-free sizing of an interval plan.  The paper has no counterpart

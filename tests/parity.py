@@ -16,7 +16,8 @@ LSE_ATOL = 1e-3
 
 
 def ensure_built():
-    fb.build()
+    # the bounds-checked debug library when BSM_FA_CHECKED=1 selected it
+    fb.build(checked=fa.LIB_PATH.endswith("_checked.so"))
     fa.lib()
     assert torch.cuda.is_available(), "GPU tests need CUDA"
 
