@@ -22,6 +22,11 @@ Workloads (all bf16, head dimension d, physical tiles 128x128 on the GPU):
                         P ~ U[1024, 4096], F0 = max(P, q+1); score_mod is a
                         tanh softcap of 50 followed by ALiBi with slope
                         2^(-8(h+1)/32) times (k - q).
+* ``decode_paged``      decoding (one query per sequence) over a paged KV
+                        cache: B=32 sequences of k_len ~ U[2048, 32768],
+                        Hq=32, Hk=8, d=128, 64-token pages in a random
+                        permutation of the page pool, causal at the
+                        query's absolute position (``decode_paged`` below).
 
 Q/K/V are N(0, 1) draws from a seeded CPU ``torch.Generator`` rounded to
 bf16; whoever consumes them (GPU path or oracle) sees the rounded values.
@@ -118,15 +123,27 @@ def tiny_causal(seed: int = 0) -> Workload:
                     1.0 / math.sqrt(d), "intervals", mask_func=mf)
 
 
+def causal_rows(qpos) -> np.ndarray:
+    """Endpoints [1, n] of causal rows at positions qpos: F0 = q + 1."""
+    return (np.asarray(qpos, np.int64) + 1).reshape(1, -1)
+
+
+def sliding_sink_rows(qpos, window: int, sink: int) -> np.ndarray:
+    """Endpoints [3, n] of rows at positions qpos that see a sink of `sink`
+    keys and a window of `window` keys ending at q."""
+    qpos = np.asarray(qpos, np.int64)
+    f0 = np.minimum(sink, qpos + 1)
+    f1 = np.maximum(f0, qpos - (window - 1))
+    f2 = qpos + 1
+    return np.stack([f0, f1, f2])
+
+
 def sliding_sink(seed: int = 0, B: int = 4, H: int = 16, S: int = 4096, d: int = 128,
                  window: int = 1024, sink: int = 4) -> Workload:
     gen = torch.Generator().manual_seed(seed)
     q, k, v = _qkv(gen, (B, S, H, d), (B, S, H, d))
     qpos = _local_positions(B, S)
-    f0 = np.minimum(sink, qpos + 1)
-    f1 = np.maximum(f0, qpos - (window - 1))
-    f2 = qpos + 1
-    mf = np.stack([f0, f1, f2]).astype(np.int32).reshape(1, 3, B * S)
+    mf = sliding_sink_rows(qpos, window, sink).astype(np.int32).reshape(1, 3, B * S)
     return Workload("sliding_sink", LAYOUT_BSHD, B, S, S, H, H, d, q, k, v,
                     1.0 / math.sqrt(d), "intervals", mask_func=mf)
 
@@ -206,6 +223,91 @@ WORKLOADS = {
 
 def make(name: str, seed: int = 0, **kw) -> Workload:
     return WORKLOADS[name](seed=seed, **kw)
+
+
+@dataclasses.dataclass
+class DecodeWorkload:
+    """Decoding over a paged KV cache: q_len query rows per sequence (the
+    newest tokens, at absolute positions offset_b + i with offset_b = k_len_b
+    - q_len), K/V in pages of ``page_size`` tokens.  Logical key j of
+    sequence b lives in page ``page_table[b, j // page_size]`` at row
+    ``j % page_size``; table entries past a sequence's last page hold -1.
+    Rows of a sequence's last page past k_len, and pages no sequence uses,
+    hold NaN: nothing may read them.  ``mask_func`` holds the endpoints of
+    each query row evaluated at its absolute position (the mask converted
+    for inference)."""
+
+    name: str
+    B: int
+    q_len: int
+    Hq: int
+    Hk: int
+    d: int
+    q: torch.Tensor                 # bf16 [B*q_len, Hq, d] (THD, q_len rows per sequence)
+    k_cache: torch.Tensor           # bf16 [num_pages, page_size, Hk, d]
+    v_cache: torch.Tensor
+    page_table: np.ndarray          # int32 [B, pages_per_seq]
+    page_size: int
+    k_lens: np.ndarray              # int64 [B]
+    mask_func: np.ndarray           # int32 [1, nfunc, B*q_len]
+    scale: float
+    mask_name: str = "causal"
+
+    @property
+    def offsets(self) -> np.ndarray:
+        return self.k_lens - self.q_len
+
+    @property
+    def cu_seqlens_q(self) -> np.ndarray:
+        return (np.arange(self.B + 1) * self.q_len).astype(np.int32)
+
+    @property
+    def cu_seqlens_k(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.k_lens)]).astype(np.int32)
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+
+def decode_paged(seed: int = 0, B: int = 32, Hq: int = 32, Hk: int = 8, d: int = 128,
+                 page_size: int = 64, kmin: int = 2048, kmax: int = 32768, q_len: int = 1,
+                 mask: str = "causal", window: int = 8192, sink: int = 4, spare_pages: int = 8,
+                 k_lens=None) -> DecodeWorkload:
+    rng = np.random.default_rng(seed)
+    if k_lens is None:
+        k_lens = rng.integers(kmin, kmax, size=B, endpoint=True)
+    k_lens = np.asarray(k_lens, np.int64)
+    assert np.all(k_lens >= q_len)
+    npg = -(-k_lens // page_size)
+    pages_per_seq = max(1, int(npg.max()))
+    num_pages = int(npg.sum()) + spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.full((B, pages_per_seq), -1, np.int32)
+    at = 0
+    for b in range(B):
+        table[b, :npg[b]] = perm[at:at + npg[b]]
+        at += int(npg[b])
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn((B * q_len, Hq, d), generator=gen).to(torch.bfloat16)
+    kc = torch.randn((num_pages, page_size, Hk, d), generator=gen).to(torch.bfloat16)
+    vc = torch.randn((num_pages, page_size, Hk, d), generator=gen).to(torch.bfloat16)
+    used = np.zeros((num_pages, page_size), bool)
+    for b in range(B):
+        j = np.arange(k_lens[b])
+        used[table[b, j // page_size], j % page_size] = True
+    nan_rows = torch.from_numpy(~used)
+    kc[nan_rows] = float("nan")
+    vc[nan_rows] = float("nan")
+    qpos = (np.repeat(k_lens - q_len, q_len) + np.tile(np.arange(q_len), B))
+    if mask == "causal":
+        mf = causal_rows(qpos)
+    elif mask == "sliding":
+        mf = sliding_sink_rows(qpos, window, sink)
+    else:
+        raise ValueError(mask)
+    return DecodeWorkload("decode_paged", B, q_len, Hq, Hk, d, q, kc, vc, table, page_size, k_lens,
+                          mf.astype(np.int32)[None], 1.0 / math.sqrt(d), mask)
 
 
 def random_intervals(seed: int, B: int, Sq: int, Sk: int, nfunc: int, Hmask: int = 1,

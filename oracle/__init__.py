@@ -21,9 +21,14 @@ Modules
   attention  fp64 masked attention with score_mods: softmax(mod(QK^T*scale))V
              and its log-sum-exp (FlexAttention Eq. 1; "Flex Attention Mask
              Plan Design" §6.1 for rows without visible keys).
+  backward   fp64 gradients dQ, dK, dV and the K2Q backward view.
+  decode     fp64 decoding rows over a paged KV cache: logical keys gathered
+             through the page table, the mask evaluated at the query's
+             absolute position (FlexAttention summary, §3.4 Paged Attention
+             Integration and Modification Conversion for Inference).
 
 Every function is pinned by tests under ``tests/test_oracle_*.py`` against
 the pages' worked example, closed forms, library routines on special cases,
 invariants and brute force.
 """
-from . import mask, plan, attention  # noqa: F401
+from . import mask, plan, attention, decode  # noqa: F401
