@@ -11,6 +11,8 @@ Names follow the C entry points:
     fa_plan_build_blocks(geom, block_mask, Hmask, block_q, block_kv) -> Plan
     fa_plan_free(plan)
     fa_fwd(plan, q, k, v, o, lse, geom, scale, mods=None)
+    fa_bwd(plan, q, k, v, o, dout, lse, dq, dk, dv, geom, scale, mods=None)
+    fa_decode_paged(plan, q, k_cache, v_cache, page_table, page_size, o, lse, geom, scale)
     fa_plan_info_get(plan, count_visible=False) -> dict
     fa_plan_export(plan) -> dict of numpy arrays
     fa_last_error(), fa_device_error_flags(), fa_version()
@@ -121,6 +123,8 @@ def lib():
         L.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, P(FaGeometry), _c.c_float,
                              P(FaMods), _vp]
         L.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, P(FaGeometry), _c.c_float, P(FaMods), _vp]
+        L.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _c.c_int64, _vp, _vp,
+                                      P(FaGeometry), _c.c_float, P(FaMods), _vp]
         L.fa_plan_info_get.argtypes = [_vp, _i32, _vp, P(FaPlanInfo)]
         L.fa_plan_export.argtypes = [_vp, P(FaPlanHostView)]
         L.fa_device_error_flags.argtypes = [_vp, P(_u32)]
@@ -132,7 +136,8 @@ def lib():
         for f in ("fa_plan_build_intervals", "fa_plan_build_blocks", "fa_plan_build_intervals_ex",
                   "fa_plan_build_blocks_ex", "fa_plan_export_backward", "fa_plan_free", "fa_fwd", "fa_bwd",
                   "fa_plan_info_get", "fa_plan_export", "fa_device_error_flags",
-                  "fa_plan_header_noalloc", "fa_selftest_wait_timeout", "fa_debug_set_work_desc"):
+                  "fa_plan_header_noalloc", "fa_selftest_wait_timeout", "fa_debug_set_work_desc",
+                  "fa_decode_paged"):
             getattr(L, f).restype = _c.c_int
         _LIB = L
     return _LIB
@@ -283,6 +288,17 @@ def fa_fwd(plan: Plan, q, k, v, o, lse, geom: FaGeometry, scale: float, softcap:
     _check(lib().fa_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                         _c.byref(geom), float(scale), _c.byref(mods) if mods else None,
                         _stream_handle(stream)))
+
+
+def fa_decode_paged(plan: Plan, q, k_cache, v_cache, page_table, page_size: int, o, lse,
+                    geom: FaGeometry, scale: float, stream=None):
+    """Decoding over a paged KV cache (see fa.h): q [batch, heads_q, d],
+    k_cache / v_cache [num_pages, page_size, heads_k, d], page_table
+    [batch, pages_per_seq] int32, all on the device."""
+    _check(lib().fa_decode_paged(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                 int(page_table.shape[1]), int(page_size), int(k_cache.shape[0]),
+                                 _ptr(o), _ptr(lse), _c.byref(geom), float(scale), None,
+                                 _stream_handle(stream)))
 
 
 def _mods(softcap, alibi_slopes):

@@ -23,7 +23,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libbsm_fa.so")
 OUT_CHECKED = os.path.join(HERE, "libbsm_fa_checked.so")
 BUILD_DIR = os.path.join(os.path.dirname(HERE), "_build")
-SOURCES = ["fa_api.cu", "planner.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu", "attn_bwd.cu"]
+SOURCES = ["fa_api.cu", "planner.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu", "attn_bwd.cu",
+           "attn_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

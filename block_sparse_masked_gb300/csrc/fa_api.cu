@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <chrono>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -624,6 +625,74 @@ int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, con
   const char* why = "";
   const cudaError_t e = bsm::launch_bwd(a, st, &why);
   al.put(a.delta, dbytes);
+  if (e) return fail(FA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
+  return FA_OK;
+}
+
+int fa_decode_paged(const fa_plan* plan, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* page_table, int32_t pages_per_seq, int32_t page_size, int64_t num_pages,
+                    void* o, float* lse, const fa_geometry* geom, float scale, const fa_mods* mods,
+                    void* stream) {
+  t_err.clear();
+  if (!plan) return fail(FA_ERR_INVALID_ARG, "plan is NULL");
+  if (int e = check_geometry(geom)) return e;
+  const bsm::Geometry g = to_geom(geom);
+  const bsm::Geometry& pg = plan->geom;
+  if (g.layout != pg.layout || g.batch != pg.batch || g.seqlen_q != pg.seqlen_q || g.seqlen_k != pg.seqlen_k ||
+      g.total_q != pg.total_q || g.total_k != pg.total_k || g.heads_q != pg.heads_q ||
+      g.heads_k != pg.heads_k || g.head_dim != pg.head_dim || g.dtype != pg.dtype)
+    return fail(FA_ERR_PLAN_MISMATCH, "geometry differs from the plan's");
+  if (plan->signature != bsm::Signature{}.hash())
+    return fail(FA_ERR_PLAN_MISMATCH, "plan signature differs from this consumer's");
+  if (plan->mask_kind != bsm::MASK_INTERVALS)
+    return fail(FA_ERR_UNSUPPORTED, "decoding takes interval-mask plans");
+  if (g.layout != FA_LAYOUT_THD || g.seqlen_q != 1 || g.total_q != g.batch)
+    return fail(FA_ERR_UNSUPPORTED, "decoding takes one query row per sequence (THD, max_seqlen_q = 1, total_q = batch)");
+  if (g.head_dim != 128) return fail(FA_ERR_UNSUPPORTED, "decoding supports head_dim 128");
+  const int G = g.heads_q / g.heads_k;
+  if (!(plan->Hmask == 1 || (plan->Hmask == g.heads_q && G == 1)))
+    return fail(FA_ERR_UNSUPPORTED, "decoding takes one mask for every head, or per-head masks without GQA");
+  if (G > 64) return fail(FA_ERR_UNSUPPORTED, "decoding supports at most 64 query heads per K/V head");
+  if (mods && (mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)))
+    return fail(FA_ERR_UNSUPPORTED, "decoding takes no score mods");
+  if (page_size < 16 || (page_size & (page_size - 1)) != 0)
+    return fail(FA_ERR_INVALID_ARG, "page_size must be a power of two >= 16");
+  if (pages_per_seq < 1 || num_pages < 1 || num_pages * static_cast<int64_t>(page_size) + 128 > INT32_MAX)
+    return fail(FA_ERR_INVALID_ARG, "pages_per_seq and num_pages must be >= 1 and num_pages * page_size < 2^31");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != plan->device) return fail(FA_ERR_PLAN_MISMATCH, "plan was built on device %d", plan->device);
+  if (!(scale > 0.0f) || !std::isfinite(scale))
+    return fail(FA_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (g.total_q == 0) return FA_OK;
+  for (const void* ptr : {q, k_cache, v_cache, static_cast<const void*>(o), static_cast<const void*>(page_table)})
+    if (!ptr) return fail(FA_ERR_INVALID_ARG, "q, k_cache, v_cache, o and page_table must be non-NULL");
+  for (const void* ptr : {q, k_cache, v_cache, static_cast<const void*>(o), static_cast<const void*>(lse)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return fail(FA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) sms = 1;
+  bsm::DecodeLaunch a{};
+  a.plan = plan;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.page_table = page_table;
+  a.pages_per_seq = pages_per_seq;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.o = o;
+  a.lse = lse;
+  a.scale = scale;
+  a.num_sms = sms;
+  bsm::DecodeSizes z{};
+  const size_t bytes = bsm::decode_workspace_bytes(a, &z);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Alloc al{plan->custom_alloc ? &plan->alloc : nullptr, plan->device, st};
+  void* ws = al.get(bytes);
+  if (!ws) return fail(FA_ERR_ALLOC, "decode workspace of %zu bytes", bytes);
+  const char* why = "";
+  const cudaError_t e = bsm::launch_decode(a, z, ws, st, &why);
+  al.put(ws, bytes);
   if (e) return fail(FA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   return FA_OK;
 }

@@ -19,7 +19,7 @@ enum PlanErr : uint32_t { PLANERR_MASK = 1u, PLANERR_SEQLENS = 2u, PLANERR_OVERF
 enum MaskKind : int { MASK_INTERVALS = 0, MASK_BLOCKS = 1 };
 
 // Error bits reported by kernels (the device error word).
-enum : uint32_t { DEVERR_TIMEOUT = 1u, DEVERR_SMEM_ALIGN = 2u, DEVERR_BOUNDS = 4u };
+enum : uint32_t { DEVERR_TIMEOUT = 1u, DEVERR_SMEM_ALIGN = 2u, DEVERR_BOUNDS = 4u, DEVERR_PAGE = 8u };
 
 // Debug builds (-DBSM_CHECKED): every plan-derived global index goes through
 // bsm_idx(i, n, err), which returns i when 0 <= i < n and otherwise records
@@ -211,6 +211,31 @@ struct BwdLaunch {
 };
 // Delta, then the dQ kernel (forward Q2K view), then the dK/dV kernel (K2Q view).
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st, const char** why);
+
+// Decoding over a paged KV cache (attn_decode.cu).
+struct DecodeLaunch {
+  const fa_plan* plan;
+  const void* q;          // [total_q, heads_q, 128]
+  const void* k_cache;    // [num_pages, page_size, heads_k, 128]
+  const void* v_cache;
+  const int32_t* page_table;  // device [batch, pages_per_seq]
+  int pages_per_seq, page_size;
+  int64_t num_pages;
+  void* o;
+  float* lse;
+  float scale;
+  int num_sms;
+};
+struct DecodeSizes {
+  int G, gy, chunks, chunk_rows, T;
+  long long max_units;
+  size_t off_remap, off_units, off_cu, off_part_o, off_part_ml, bytes;
+};
+// Workspace layout of one decode call; returns its size in bytes.
+size_t decode_workspace_bytes(const DecodeLaunch& a, DecodeSizes* s);
+// Page conversion and unit split, the decode kernel, the unit merge.
+cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws, cudaStream_t st,
+                          const char** why);
 uint32_t* fwd_error_word();  // device address of the forward kernels' error word
 // The error word the bounds checks of a checked build (-DBSM_CHECKED)
 // report into; nullptr in a release build, whose checks compile away.

@@ -222,6 +222,42 @@ int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, con
            const void* dout, const float* lse, void* dq, void* dk, void* dv, const fa_geometry* geom,
            float scale, const fa_mods* mods, void* stream);
 
+/*
+ * Decoding over a paged KV cache ("FlexAttention: A Programming Model for
+ * Generating Optimized Attention Kernels", summary page, §3.4 Paged
+ * Attention Integration and Modification Conversion for Inference).
+ *
+ * The plan is an interval plan whose geometry is THD with one query row per
+ * sequence (max_seqlen_q = 1, total_q = batch) and the sequences' logical
+ * key counts (cu_seqlens_k); the endpoints of each query row are those of
+ * its absolute position offset = k_len - 1 (the mask converted for
+ * inference).  Key j of sequence b is read from page page_table[b][j /
+ * page_size], row j % page_size: before the attention kernel, one small
+ * kernel converts every K tile of the plan's lists into the physical rows
+ * of its pages (the page table becomes part of the index lists; the
+ * attention loop sees physical rows only), and splits each sequence's list
+ * into units of a few K tiles (Split-K).  The attention kernel runs one
+ * persistent CTA per SM over the units; a last kernel merges the units of
+ * each query row.
+ *   q: device bf16 [batch, heads_q, 128]; k_cache, v_cache: device bf16
+ *   [num_pages, page_size, heads_k, 128]; page_table: device int32
+ *   [batch, pages_per_seq] (entries for pages past a sequence's k_len are
+ *   never read); o: device bf16 like q; lse: device float32 [heads_q, batch]
+ *   (natural log), may be NULL.  page_size: a power of two >= 16.
+ * A page number outside [0, num_pages) for a key that is needed sets bit 3
+ * of the device error flags (fa_device_error_flags) and reads zeros.
+ * One mask for every head (Hmask = 1, any GQA group up to 64 query heads
+ * per K/V head), or per-head masks without GQA; no score mods
+ * (FA_ERR_UNSUPPORTED otherwise).  A workspace (index conversion, units,
+ * per-unit O, max and sum) comes from the plan's allocator or the
+ * library's pool and is returned in stream order.  Asynchronous on
+ * `stream`: three kernel launches.  Pointers must be 16-byte aligned.
+ */
+int fa_decode_paged(const fa_plan* plan, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* page_table, int32_t pages_per_seq, int32_t page_size,
+                    int64_t num_pages, void* o, float* lse, const fa_geometry* geom, float scale,
+                    const fa_mods* mods, void* stream);
+
 /* Plan statistics and layout sizes (Tessera-style mask statistics). */
 typedef struct {
   int64_t header[8];      /* fwd Q rows, partial nnz, full nnz, 0, 0, 0, 0, error flags */
@@ -308,7 +344,8 @@ int fa_plan_export_backward(const fa_plan* plan, fa_plan_bwd_host_view* dst);
  * the kernel requires, so it did no work; bit 2, only in the bounds-checked
  * debug build libbsm_fa_checked.so: a planner, forward or backward kernel
  * computed a plan-derived global index outside the plan's exact sizes, and
- * the access was redirected or skipped).  Synchronises `stream`, returns
+ * the access was redirected or skipped; bit 3: fa_decode_paged met a page
+ * number outside the cache for a key it needed, and read zeros instead).  Synchronises `stream`, returns
  * the bits in *flags and clears them.
  */
 int fa_device_error_flags(void* stream, uint32_t* flags);

@@ -34,18 +34,33 @@ def gather_logical(cache: torch.Tensor, table_row: np.ndarray, k_len: int, page_
     return A.as_f64(rows)
 
 
+def _rows(w, b: int, h: int, k: np.ndarray, v: np.ndarray):
+    """O [q_len, d], LSE [q_len] of sequence b, Q head h, from its logical
+    K/V [k_len, Hk, d].  Mask head: 0 for a mask shared by the heads, else h."""
+    k_len = int(w.k_lens[b])
+    hk = h // (w.Hq // w.Hk)
+    hm = 0 if w.mask_func.shape[0] == 1 else h
+    rows = np.arange(b * w.q_len, (b + 1) * w.q_len)
+    q = A.as_f64(w.q[torch.from_numpy(rows), h])
+    vis = M.interval_visible(w.mask_func[hm][:, rows], k_len)
+    q_abs = (k_len - w.q_len) + np.arange(w.q_len)  # absolute positions (used by position-dependent mods)
+    return A.attention_dense(q, k[:, hk], v[:, hk], vis, q_abs, w.scale)
+
+
 def decode_rows(w, b: int, h: int):
     """O [q_len, d] and LSE [q_len] (fp64) of the query rows of sequence b, Q head h."""
     k_len = int(w.k_lens[b])
-    group = w.Hq // w.Hk
-    hk = h // group
-    rows = np.arange(b * w.q_len, (b + 1) * w.q_len)
-    q = A.as_f64(w.q[torch.from_numpy(rows), h])
-    k = gather_logical(w.k_cache, w.page_table[b], k_len, w.page_size)[:, hk]
-    v = gather_logical(w.v_cache, w.page_table[b], k_len, w.page_size)[:, hk]
-    vis = M.interval_visible(w.mask_func[0][:, rows], k_len)
-    q_abs = (k_len - w.q_len) + np.arange(w.q_len)
-    return A.attention_dense(q, k, v, vis, q_abs, w.scale)
+    k = gather_logical(w.k_cache, w.page_table[b], k_len, w.page_size)
+    v = gather_logical(w.v_cache, w.page_table[b], k_len, w.page_size)
+    return _rows(w, b, h, k, v)
+
+
+def decode_sequence(w, b: int, heads=None):
+    """{h: (O [q_len, d], LSE [q_len])} of sequence b for the given Q heads (all by default)."""
+    k_len = int(w.k_lens[b])
+    k = gather_logical(w.k_cache, w.page_table[b], k_len, w.page_size)
+    v = gather_logical(w.v_cache, w.page_table[b], k_len, w.page_size)
+    return {h: _rows(w, b, h, k, v) for h in (range(w.Hq) if heads is None else heads)}
 
 
 def decode_full(w):
@@ -53,8 +68,7 @@ def decode_full(w):
     o = np.zeros((w.B * w.q_len, w.Hq, w.d))
     lse = np.full((w.Hq, w.B * w.q_len), -np.inf)
     for b in range(w.B):
-        for h in range(w.Hq):
-            ob, lb = decode_rows(w, b, h)
+        for h, (ob, lb) in decode_sequence(w, b).items():
             o[b * w.q_len:(b + 1) * w.q_len, h] = ob
             lse[h, b * w.q_len:(b + 1) * w.q_len] = lb
     return o, lse

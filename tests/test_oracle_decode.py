@@ -155,3 +155,20 @@ def test_generator_hides_unused_rows_behind_nan():
         assert np.isfinite(D.gather_logical(w.k_cache, w.page_table[b], n, 64)).all()
     o, lse = D.decode_full(w)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+def test_per_head_masks_follow_their_own_rows():
+    # mask heads = Q heads (no GQA): head h sees a window of 8 + 24 h keys
+    w, logical = _contiguous(8, B=2, Hq=3, Hk=3, d=8, k_lens=[150, 61], page_size=16)
+    windows = [8 + 24 * h for h in range(w.Hq)]
+    pos = w.k_lens - 1
+    w.mask_func = np.stack([W.sliding_sink_rows(pos, win, 0) for win in windows]).astype(np.int32)
+    for b in range(w.B):
+        n = int(w.k_lens[b])
+        kb, vb = (A.as_f64(t) for t in logical[b])
+        j = np.arange(n)
+        for h in range(w.Hq):
+            vis = ((j > n - 1 - windows[h]) & (j <= n - 1))[None, :]
+            o, _ = D.decode_rows(w, b, h)
+            ref = _sdpa(A.as_f64(w.q[b:b + 1, h]), kb[:, h], vb[:, h], w.scale, vis)
+            np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
