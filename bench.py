@@ -68,9 +68,13 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
+FWD_SOURCES = ("attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu", "ptx.cuh", "internal.h")
+DECODE_SOURCES = ("attn_decode.cu", "ptx.cuh", "internal.h")
+
+
+def kernel_hash(files=FWD_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "attn_fwd_pair.cu", "attn_fwd_kt.cu", "ptx.cuh", "internal.h"):
+    for f in files:
         with open(os.path.join(ROOT, "block_sparse_masked_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -92,7 +96,7 @@ def known_traffic(workload: str):
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    kh = kernel_hash()
+    kh = kernel_hash(DECODE_SOURCES if workload == "decode_paged" else FWD_SOURCES)
     with open(p) as f:
         for line in f:
             parts = line.split()
@@ -314,7 +318,47 @@ def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, s
                      "kernel": fwd_kernel_name(w), "backward": bwd}
         del dp, plan, w
         torch.cuda.empty_cache()
+    out["decode_paged"] = time_decode(fa, runner, W, flush, stream, peaks, peak_src, reps, seed)
+    torch.cuda.empty_cache()
     return out
+
+
+DECODE_DESC = ("decode over a paged KV cache: B=32 sequences, k_len ~ U[2048, 32768], Hq=32 Hk=8 d=128, "
+               "64-token pages, causal at the query's absolute position")
+
+
+def time_decode(fa, runner, W, flush, stream, peaks, peak_src, reps: int, seed: int):
+    """fa_decode_paged (page conversion + unit split, decode kernel, unit
+    merge) timed alone, L2 flushed before each call.  Algorithmic bytes: the
+    K and V rows of every visible key once per K/V head, Q read, O and LSE
+    written; the bound is HBM."""
+    import torch
+    w = W.decode_paged(seed)
+    dp = runner.decode_to_device(w)
+    plan = runner.decode_plan(dp)
+    info = fa.fa_plan_info_get(plan, count_visible=True)
+    vis_keys = info["visible_pairs"]  # summed over the mask heads' rows
+    kv_heads = w.Hk if info["mask_heads"] == 1 else 1
+    alg = float(vis_keys * kv_heads * w.d * 2 * 2 + 2 * w.q.numel() * 2 + 4 * w.Hq * w.B)
+    for _ in range(3):
+        runner.decode(dp, plan)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+    for i in range(reps):
+        flush.zero_()
+        torch.cuda._sleep(SLEEP_CYCLES)
+        ev[i][0].record(stream)
+        runner.decode(dp, plan)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flops = 4.0 * w.d * vis_keys * w.Hq
+    rf = roofline(flops, alg, ms, peaks, peak_src, known_traffic("decode_paged"))
+    plan.free()
+    return {"workload": DECODE_DESC, "decode_ms": ms, "bound": rf["bound"], "frac": rf["frac"],
+            "alg_bytes": alg, "alg_gbs": rf["alg_gbs"], "tflops": rf["tflops"], "traffic": rf["traffic"],
+            "visible_keys_per_kv_head": vis_keys, "launches": 3,
+            "kernel": "k_decode<16> (persistent keys-major decode; prep and merge kernels beside it)"}
 
 
 def cpu_baseline(w, budget_s: float):

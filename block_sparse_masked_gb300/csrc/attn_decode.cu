@@ -61,8 +61,8 @@ constexpr float kNoMax = -1.0e30f;    // reference max of a column before its fi
 constexpr int D = 128;
 constexpr int kTileBytes = kTile * D * 2;       // 32 KB: one K or V tile, [2 halves][128 rows][128 B]
 constexpr int kStageBytes = 2 * kTileBytes;     // K then V
-constexpr int kThreads = 192;                   // warps 0-3 softmax, 4 producer, 5 MMA issuer
-constexpr int kWarpProducer = 4, kWarpMma = 5;
+constexpr int kThreads = 224;  // warps 0-3 softmax, 4 producer, 5 S^T issuer, 6 P V issuer
+constexpr int kWarpProducer = 4, kWarpMma = 5, kWarpPV = 6;
 
 struct DecParams {
   // plan
@@ -94,7 +94,7 @@ struct DecLayout {
   static constexpr int kQBytes = 2 * N * 128;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;          // P: [2 key halves][N rows][128 B]
   static constexpr int kOffSmall = kOffP + kQBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 1;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2;
   static constexpr int kSmTmem = 8 * kNumBars;
   static constexpr int kSmAbort = kSmTmem + 4;
   static constexpr int kSmRed = (kSmAbort + 4 + 15) & ~15;  // [4 warps][N] floats
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_qfull = b_empty + 8 * L::kStages, b_qempty = b_qfull + 16;
   const uint32_t b_sfull = b_qempty + 16, b_sfree = b_sfull + 16;
   const uint32_t b_pfull = b_sfree + 16, b_pvdone = b_pfull + 8;
-  const uint32_t b_ofree = b_pvdone + 8, b_drain = b_ofree + 16;
+  const uint32_t b_ofree = b_pvdone + 8, b_drain = b_ofree + 16, b_drain2 = b_drain + 8;
   static_assert(8 * L::kNumBars == L::kSmTmem, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + L::kSmTmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(small + L::kSmAbort);
@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_pfull, 4);
     mbar_init(b_pvdone, 1);
     mbar_init(b_drain, 1);
+    mbar_init(b_drain2, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -315,75 +316,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    // Step order: S(g + 1) is issued before P V(g), across unit boundaries.
+    // ------------------------------------------------------------ S^T issuer
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, N, 0);              // K (128 keys) x Q (N), both K-major
-      constexpr uint32_t idO = idesc_bf16_f32(128, N, 0) | (1u << 15);  // V^T (MN-major) x P (K-major)
+      constexpr uint32_t idS = idesc_bf16_f32(128, N, 0);  // K (128 keys) x Q (N), both K-major
       const uint64_t dK0 = sdesc_sw128(sRing, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(sRing + kTileBytes, 16384, 1024);
       const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
-      const uint64_t dP0 = sdesc_sw128(sP, 16, 1024);
-      // the steps of this CTA, in order: (unit ordinal, entry within the unit)
-      long long u_s = blockIdx.x, u_p = blockIdx.x;  // units of the next S and the next P V
-      int ui_s = 0, j_s = 0, n_s = (u_s < total) ? load_unit(p, u_s).n : 0;
-      int ui_p = 0, j_p = 0, n_p = n_s;
-      int gs = 0, gp = 0;
-      auto issue_s = [&]() -> bool {  // S of the next step, if any
-        if (u_s >= total) return false;
-        const int st = gs % L::kStages, sb = gs & 1, qb = ui_s & 1;
-        if (j_s == 0) mbar_wait(b_qfull + 8 * qb, (ui_s >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
-        mbar_wait(b_full + 8 * st, (gs / L::kStages) & 1, abort_flag, p.err, kWaitTimeoutNs);
-        if (gs >= 2) mbar_wait(b_sfree + 8 * sb, ((gs >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
-        if (*abort_flag) return false;
-        tc_fence_after();
-        const uint64_t dK = dK0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+      int g = 0, ui = 0;
+      for (long long u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++ui) {
+        const int n = load_unit(p, u).n, qb = ui & 1;
+        mbar_wait(b_qfull + 8 * qb, (ui >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
         const uint64_t dQ = dQ0 + static_cast<uint64_t>((qb * L::kQBytes) >> 4);
+        for (int j = 0; j < n; ++j, ++g) {
+          const int st = g % L::kStages, sb = g & 1;
+          mbar_wait(b_full + 8 * st, (g / L::kStages) & 1, abort_flag, p.err, kWaitTimeoutNs);
+          if (g >= 2) mbar_wait(b_sfree + 8 * sb, ((g >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
+          if (*abort_flag) break;
+          tc_fence_after();
+          const uint64_t dK = dK0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offK = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          const uint32_t offQ = ((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + N * sb, dK + offK, dQ + offQ, idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t offK = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            const uint32_t offQ = ((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + N * sb, dK + offK, dQ + offQ, idS, kk > 0);
+          }
+          umma_commit(b_sfull + 8 * sb);
         }
-        umma_commit(b_sfull + 8 * sb);
-        ++gs;
-        if (++j_s == n_s) {  // the unit's Q buffer is free once its last S completes
-          umma_commit(b_qempty + 8 * qb);
-          j_s = 0;
-          ++ui_s;
-          u_s += gridDim.x;
-          n_s = (u_s < total) ? load_unit(p, u_s).n : 0;
-        }
-        return true;
-      };
-      issue_s();
-      while (u_p < total && !*abort_flag) {
-        issue_s();
-        const int st = gp % L::kStages, ob = ui_p & 1;
-        if (j_p == 0 && ui_p >= 2) mbar_wait(b_ofree + 8 * ob, ((ui_p >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
-        mbar_wait(b_pfull, gp & 1, abort_flag, p.err, kWaitTimeoutNs);
-        if (*abort_flag) break;
-        tc_fence_after();
-        const uint64_t dV = dV0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t offP = ((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4;
-          umma_bf16_ss(tmem + 2 * N + N * ob, dV + static_cast<uint64_t>((kk * 2048) >> 4), dP0 + offP, idO,
-                       (j_p > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(b_empty + 8 * st);
-        umma_commit(b_pvdone);
-        ++gp;
-        if (++j_p == n_p) {
-          j_p = 0;
-          ++ui_p;
-          u_p += gridDim.x;
-          n_p = (u_p < total) ? load_unit(p, u_p).n : 0;
-        }
+        // the unit's Q buffer is free once its last S^T completes
+        umma_commit(b_qempty + 8 * qb);
       }
       // every MMA issued above completes before TMEM is released
       umma_commit(b_drain);
       mbar_wait_drain(b_drain, 0, kWaitTimeoutNs);
+    }
+  } else if (warp == kWarpPV) {
+    // ------------------------------------------------------------ P V issuer
+    // Issued as soon as P lands: it does not wait for the next K tile.
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16_f32(128, N, 0) | (1u << 15);  // V^T (MN-major) x P (K-major)
+      const uint64_t dV0 = sdesc_sw128(sRing + kTileBytes, 16384, 1024);
+      const uint64_t dP0 = sdesc_sw128(sP, 16, 1024);
+      int g = 0, ui = 0;
+      for (long long u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++ui) {
+        const int n = load_unit(p, u).n, ob = ui & 1;
+        // the unit's first P V overwrites its O^T buffer: the epilogue of the
+        // unit two before must have read it
+        if (ui >= 2) mbar_wait(b_ofree + 8 * ob, ((ui >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
+        for (int j = 0; j < n; ++j, ++g) {
+          const int st = g % L::kStages;
+          mbar_wait(b_pfull, g & 1, abort_flag, p.err, kWaitTimeoutNs);
+          if (*abort_flag) break;
+          tc_fence_after();
+          const uint64_t dV = dV0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t offP = ((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4;
+            umma_bf16_ss(tmem + 2 * N + N * ob, dV + static_cast<uint64_t>((kk * 2048) >> 4), dP0 + offP, idO,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          // the stage (its K was read by S^T, which completed before P was written) and P are free
+          umma_commit(b_empty + 8 * st);
+          umma_commit(b_pvdone);
+        }
+      }
+      umma_commit(b_drain2);
+      mbar_wait_drain(b_drain2, 0, kWaitTimeoutNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -513,6 +509,8 @@ struct PrepParams {
   const int32_t* f_off;
   const int32_t* p_idx;
   const int32_t* f_idx;
+  const int32_t* entry_row;  // [P] flat plan row of each partial entry
+  const int32_t* cu_q_rows;  // [B+1] plan row prefix of the sequences
   const int32_t* page_table;
   int32_t* remap;
   int4* units;
@@ -523,6 +521,7 @@ struct PrepParams {
   int B, Hmask, rows, pages_per_seq, page_size, chunks, chunk_rows, T;
 };
 
+// K tile entries of (mask head, sequence) row r = hm * B + b.
 __device__ __forceinline__ int row_entries(const PrepParams& p, int r, int* p0, int* np, int* f0, int* b_out) {
   const int hm = r / p.B, b = r % p.B;
   const int32_t* sq = p.seq + 8 * b;
@@ -538,20 +537,64 @@ __device__ __forceinline__ int row_entries(const PrepParams& p, int r, int* p0, 
   return *np + (__ldg(p.f_off + flat + 1) - *f0);
 }
 
-__global__ void __launch_bounds__(1024) k_decode_prep(PrepParams p) {
+// Largest i in [lo, hi) with a[i] <= x (a ascending, a[lo] <= x).
+__device__ __forceinline__ int last_le(const int32_t* a, int lo, int hi, long long x) {
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Block 0: units per row (exclusive scan into cu_units) and the unit
+// descriptors.  Every other block: the page conversion of 256 list entries
+// (partial entries first, then full ones), one thread each.
+__global__ void __launch_bounds__(256) k_decode_prep(PrepParams p) {
+  if (blockIdx.x > 0) {
+    const long long e = static_cast<long long>(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    if (e >= p.nP + p.nF) return;
+    const bool partial = e < p.nP;
+    long long flat;
+    int lt;
+    if (partial) {
+      flat = __ldg(p.entry_row + e);
+      lt = __ldg(p.p_idx + e);
+    } else {
+      const long long ef = e - p.nP;
+      flat = last_le(p.f_off, 0, p.Hmask * p.rows, ef);  // the last row starting at or before ef holds it
+      lt = __ldg(p.f_idx + ef);
+    }
+    const int row = static_cast<int>(flat % p.rows);
+    const int b = last_le(p.cu_q_rows, 0, p.B, row);
+    const int k_len = __ldg(p.seq + 8 * b + 3);
+    const int32_t* table = p.page_table + static_cast<long long>(b) * p.pages_per_seq;
+    int32_t* out = p.remap + e * p.chunks;
+    for (int c = 0; c < p.chunks; ++c) {
+      const long long lrow = static_cast<long long>(lt) * kTile + static_cast<long long>(c) * p.chunk_rows;
+      int32_t phys = -1;
+      if (lrow < k_len) {
+        const long long pg = lrow / p.page_size;
+        const int page = (pg < p.pages_per_seq) ? __ldg(table + pg) : -1;
+        if (page < 0 || page >= p.num_pages)
+          atomicOr(p.err, DEVERR_PAGE);
+        else
+          phys = static_cast<int32_t>(static_cast<long long>(page) * p.page_size + lrow % p.page_size);
+      }
+      out[c] = phys;
+    }
+    return;
+  }
   __shared__ int32_t s_warp[32];
   __shared__ int32_t s_carry;
   const int R = p.B * p.Hmask;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
-  // units per (mask head, sequence) row, exclusive scan into cu_units
-  for (int base = 0; base < R; base += 1024) {
+  for (int base = 0; base < R; base += blockDim.x) {
     const int r = base + threadIdx.x;
-    int cnt = 0;
+    int cnt = 0, n = 0, p0 = 0, np = 0, f0 = 0, b = 0;
     if (r < R) {
-      int p0, np, f0, b;
-      const int n = row_entries(p, r, &p0, &np, &f0, &b);
+      n = row_entries(p, r, &p0, &np, &f0, &b);
       cnt = (n + p.T - 1) / p.T;
     }
     int x = cnt;
@@ -563,55 +606,27 @@ __global__ void __launch_bounds__(1024) k_decode_prep(PrepParams p) {
     if (lane == 31) s_warp[wid] = x;
     __syncthreads();
     if (wid == 0) {
-      int s = s_warp[lane];
+      int v = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += y;
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
       }
-      s_warp[lane] = s;
+      s_warp[lane] = v;
     }
     __syncthreads();
-    const int excl = s_carry + (wid ? s_warp[wid - 1] : 0) + x - cnt;
-    if (r < R) p.cu_units[r] = excl;
+    const int u0 = s_carry + (wid ? s_warp[wid - 1] : 0) + x - cnt;
+    if (r < R) {
+      p.cu_units[r] = u0;
+      for (int k = 0; k < cnt; ++k) p.units[u0 + k] = make_int4(r / p.B, b, k * p.T, min(n, (k + 1) * p.T));
+    }
     __syncthreads();
-    if (threadIdx.x == 0) s_carry += s_warp[31];
+    if (threadIdx.x == 0) s_carry += s_warp[nw - 1];
     __syncthreads();
   }
   if (threadIdx.x == 0) {
     p.cu_units[R] = s_carry;
     *p.nunits = s_carry;
-  }
-  __syncthreads();
-  // one warp per row: unit descriptors and the page conversion of its entries
-  for (int r = wid; r < R; r += 32) {
-    int p0, np, f0, b;
-    const int n = row_entries(p, r, &p0, &np, &f0, &b);
-    const int k_len = __ldg(p.seq + 8 * b + 3);
-    const int u0 = p.cu_units[r];
-    for (int k = lane; k * p.T < n; k += 32)
-      p.units[u0 + k] = make_int4(r / p.B, b, k * p.T, min(n, (k + 1) * p.T));
-    const int32_t* table = p.page_table + static_cast<long long>(b) * p.pages_per_seq;
-    for (int e = lane; e < n; e += 32) {
-      const bool partial = e < np;
-      const long long ep = partial ? static_cast<long long>(p0) + e : static_cast<long long>(f0) + (e - np);
-      const int lt = partial ? __ldg(p.p_idx + ep) : __ldg(p.f_idx + ep);
-      int32_t* out = p.remap + (partial ? ep : p.nP + ep) * p.chunks;
-      for (int c = 0; c < p.chunks; ++c) {
-        const long long lrow = static_cast<long long>(lt) * kTile + static_cast<long long>(c) * p.chunk_rows;
-        int32_t phys = -1;
-        if (lrow < k_len) {
-          const long long pg = lrow / p.page_size;
-          const int page = (pg < p.pages_per_seq) ? __ldg(table + pg) : -1;
-          if (page < 0 || page >= p.num_pages) {
-            atomicOr(p.err, DEVERR_PAGE);
-          } else {
-            phys = static_cast<int32_t>(static_cast<long long>(page) * p.page_size + lrow % p.page_size);
-          }
-        }
-        out[c] = phys;
-      }
-    }
   }
 }
 
@@ -758,6 +773,8 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   pp.f_off = pl->f_off;
   pp.p_idx = pl->p_idx;
   pp.f_idx = pl->f_idx;
+  pp.entry_row = pl->entry_row;
+  pp.cu_q_rows = pl->cu_q_rows;
   pp.page_table = a.page_table;
   pp.remap = remap;
   pp.units = units;
@@ -775,7 +792,8 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   pp.chunks = s.chunks;
   pp.chunk_rows = s.chunk_rows;
   pp.T = s.T;
-  k_decode_prep<<<1, 1024, 0, st>>>(pp);
+  const long long entries = pl->P + pl->F;
+  k_decode_prep<<<static_cast<unsigned>(1 + (entries + 255) / 256), 256, 0, st>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = "decode prep launch failed";

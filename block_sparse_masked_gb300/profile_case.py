@@ -4,7 +4,8 @@ use under a profiler: ``python -m block_sparse_masked_gb300.profile_case
 
 The workload is the seeded synthetic one of ``workloads.py``; ``--heads``
 keeps its per-head structure with fewer heads so that a capture holds a few
-GB at most.  The plan is built once; the launches follow it back to back;
+GB at most.  ``--workload decode_paged`` runs fa_decode_paged instead
+(``--heads`` then sets the number of sequences).  The plan is built once; the launches follow it back to back;
 the last one is timed with CUDA events and printed (not a benchmark number:
 see ``bench.py``).
 """
@@ -29,6 +30,22 @@ def main():
     from . import runner
     from . import workloads as W
 
+    if args.workload == "decode_paged":
+        w = W.decode_paged(0, **({"B": args.heads} if args.heads > 0 else {}))
+        dp = runner.decode_to_device(w)
+        plan = runner.decode_plan(dp)
+        for _ in range(args.launches):
+            runner.decode(dp, plan)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        runner.decode(dp, plan)
+        e1.record()
+        torch.cuda.synchronize()
+        print(f"decode_paged B={w.B}: last call {e0.elapsed_time(e1):.4f} ms, "
+              f"device error flags {fa.fa_device_error_flags()}")
+        plan.free()
+        return
     kw = {}
     if args.heads > 0:
         kw["H"] = args.heads
