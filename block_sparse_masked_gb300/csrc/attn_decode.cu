@@ -16,25 +16,28 @@
 //     payload stays indexed by list entry and needs no conversion.
 //
 // Three launches:
-//   k_decode_prep     one CTA: splits each (mask head, sequence) K tile list
-//                     into units of at most T tiles (the Split-K partition of
+//   k_decode_prep     converts every list entry to the physical rows of its
+//                     pages through the page table (one thread per entry),
+//                     and in its first CTA scans the rows' entry counts;
+//   k_decode<N>       persistent, one CTA per SM.  The K tiles of all rows
+//                     and K/V heads, concatenated, are cut into C equal
+//                     ranges, one per CTA (the Split-K partition of
 //                     "Decoupling Logical Masks from GPU Execution for Dynamic
-//                     Block-Sparse Attention", Split-K paragraph) and converts
-//                     every list entry to physical rows through the page table;
-//   k_decode<N>       persistent, one CTA per SM, units dealt round-robin: a
-//                     unit is one K/V head, one sequence and up to T of its K
-//                     tiles.  The G = Hq/Hk query heads of the K/V head (the
+//                     Block-Sparse Attention", Split-K paragraph, sized so
+//                     that every CTA streams the same number of tiles); a
+//                     range falls into pieces, one per (row, K/V head) it
+//                     touches.  The G = Hq/Hk query heads of the K/V head (the
 //                     GQA group; N = G rounded up to 16) form the N columns of
 //                     keys-major products on the tensor cores:
 //                       S^T = K Q^T (M = 128 keys) into TMEM,
 //                       P^T = exp2(S^T - m) (bf16, shared memory, K-major),
 //                       O^T += V^T P^T (M = 128 head dims),
-//                     with a lazily updated per-column reference max; the
-//                     unit's unnormalised O, its reference max m and its sum l
-//                     go to a workspace;
-//   k_decode_combine  one warp per (query row, head): merges the units of the
-//                     row with weights 2^(m_u - max m), divides by the merged
-//                     l, writes O (bf16) and LSE (natural log).
+//                     with a lazily updated per-column reference max; each
+//                     piece's unnormalised O, reference max m and sum l go to
+//                     a workspace slot;
+//   k_decode_combine  one warp per (query row, head): merges the pieces of
+//                     the row with weights 2^(m - max m), divides by the
+//                     merged l, writes O (bf16) and LSE (natural log).
 // The path is bound by HBM bandwidth (every visible K/V byte is read once per
 // K/V head); the tensor cores keep the arithmetic off the issue slots.
 #include <cuda.h>
@@ -74,14 +77,13 @@ struct DecParams {
   const uint32_t* payload;
   // k_decode_prep outputs
   const int32_t* remap;    // [(P + F) * chunks]: physical start row of each page chunk, -1 past k_len
-  const int4* units;       // [units]: (mask head, sequence, first entry, end entry)
-  const int32_t* nunits;   // [1]
-  // unit results
+  const int32_t* cu_rows;  // [R + 1]: prefix of the rows' entry counts (row r = mask head * B + sequence)
+  // piece results
   float* part_o;           // [slots][G][D]: unnormalised O
   float* part_ml;          // [slots][2][G]: reference max (log2 units), sum l
   uint32_t* err;
-  int B, Hq, Hk, Hmask, rows, G, gy, chunks, chunk_rows, oob_row;
-  long long nP, nF, max_units;
+  int B, Hq, Hk, Hmask, rows, G, gy, chunks, chunk_rows, oob_row, R;
+  long long nP, nF;
   float scale_log2;
 };
 
@@ -107,34 +109,73 @@ struct DecLayout {
   static_assert(kNeed <= 232448, "shared memory budget");
 };
 
-// One unit as every role sees it.
+// The work is the sequence of segments s = r * gy + gi, row r = hm * B + b
+// (mask head, sequence), gi the K/V head of the GQA group (always 0 for
+// per-head masks): segment s holds the K tiles of row r for that K/V head.
+// CTA c of C takes the tiles [W c / C, W (c + 1) / C) of the concatenation
+// (W tiles in all), so every CTA streams the same number of K/V tiles; its
+// range falls into pieces, one per segment it touches.  A piece's results
+// go to slot s + c, which no other piece uses.
+__device__ __forceinline__ long long seg_start(const int32_t* cu_rows, int R, int gy, long long s) {
+  if (s >= static_cast<long long>(R) * gy) return static_cast<long long>(gy) * __ldg(cu_rows + R);
+  const long long r = s / gy, gi = s % gy;
+  const long long a = __ldg(cu_rows + r), n = __ldg(cu_rows + r + 1) - a;
+  return gy * a + gi * n;
+}
+__device__ __forceinline__ long long seg_start(const DecParams& p, long long s) {
+  return seg_start(p.cu_rows, p.R, p.gy, s);
+}
+
+// One piece as every role sees it.
 struct Unit {
   int hm, b, hk, e0, n;   // mask head, sequence, K/V head, first list entry, entries
   int p0, np, f0;         // the row's partial and full lists
   int q_off, k_len;
-  long long slot;         // workspace slot of the unit's results
+  long long slot;         // workspace slot of the piece's results
 };
 
-__device__ __forceinline__ Unit load_unit(const DecParams& p, long long u) {
-  Unit x;
-  const int4 d = __ldg(p.units + bsm_idx(u / p.gy, p.max_units, p.err));
-  const int gi = static_cast<int>(u % p.gy);
-  x.hm = d.x;
-  x.b = static_cast<int>(bsm_idx(d.y, p.B, p.err));
-  x.e0 = d.z;
-  x.n = d.w - d.z;
-  x.hk = (p.Hmask == 1) ? gi : x.hm;
-  const int32_t* sq = p.seq + 8 * x.b;
-  x.q_off = __ldg(sq + 0);
-  x.k_len = __ldg(sq + 3);
-  const long long flat = bsm_idx(static_cast<long long>(x.hm) * p.rows + __ldg(sq + 4),
-                                 static_cast<long long>(p.Hmask) * p.rows, p.err);
-  x.p0 = __ldg(p.p_off + flat);
-  x.np = __ldg(p.p_off + flat + 1) - x.p0;
-  x.f0 = __ldg(p.f_off + flat);
-  x.slot = u;
-  return x;
-}
+struct Pieces {
+  long long pos, end, s, S;
+  int c;
+  __device__ __forceinline__ void init(const DecParams& p, int cta, int C) {
+    const long long W = static_cast<long long>(p.gy) * __ldg(p.cu_rows + p.R);
+    c = cta;
+    pos = W * cta / C;
+    end = W * (cta + 1) / C;
+    S = static_cast<long long>(p.R) * p.gy;
+    // the last segment starting at or before pos
+    long long lo = 0, hi = S;
+    while (hi - lo > 1) {
+      const long long mid = (lo + hi) >> 1;
+      if (seg_start(p, mid) <= pos) lo = mid; else hi = mid;
+    }
+    s = lo;
+  }
+  // the next piece of this CTA's range; false at its end
+  __device__ __forceinline__ bool next(const DecParams& p, Unit* x) {
+    if (pos >= end) return false;
+    while (s + 1 < S && seg_start(p, s + 1) <= pos) ++s;  // past empty segments
+    const long long a = seg_start(p, s), z = seg_start(p, s + 1);
+    const long long r = s / p.gy;
+    const int gi = static_cast<int>(s % p.gy);
+    x->hm = static_cast<int>(r / p.B);
+    x->b = static_cast<int>(bsm_idx(r % p.B, p.B, p.err));
+    x->hk = (p.Hmask == 1) ? gi : x->hm;
+    x->e0 = static_cast<int>(pos - a);
+    x->n = static_cast<int>((z < end ? z : end) - pos);
+    const int32_t* sq = p.seq + 8 * x->b;
+    x->q_off = __ldg(sq + 0);
+    x->k_len = __ldg(sq + 3);
+    const long long flat = bsm_idx(static_cast<long long>(x->hm) * p.rows + __ldg(sq + 4),
+                                   static_cast<long long>(p.Hmask) * p.rows, p.err);
+    x->p0 = __ldg(p.p_off + flat);
+    x->np = __ldg(p.p_off + flat + 1) - x->p0;
+    x->f0 = __ldg(p.f_off + flat);
+    x->slot = s + c;
+    pos += x->n;
+    return true;
+  }
+};
 
 // Warp reduction of 16 columns: on return every lane holds, for column
 // (lane & 15), the max (or sum) over the 32 lanes.  v is consumed.
@@ -265,7 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // TMEM columns: S^T buffers at 0 and N, O^T buffers at 2N and 3N
-  const long long total = static_cast<long long>(__ldg(p.nunits)) * p.gy;
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
@@ -274,8 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       int g = 0, issued = 0, ui = 0, q_issued = 0;
-      for (long long u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++ui) {
-        const Unit x = load_unit(p, u);
+      Pieces it;
+      it.init(p, blockIdx.x, gridDim.x);
+      Unit x;
+      for (; !*abort_flag && it.next(p, &x); ++ui) {
         const int qb = ui & 1;
         if (ui >= 2) mbar_wait(b_qempty + 8 * qb, ((ui >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
         if (*abort_flag) break;
@@ -322,8 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK0 = sdesc_sw128(sRing, 16, 1024);
       const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
       int g = 0, ui = 0;
-      for (long long u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++ui) {
-        const int n = load_unit(p, u).n, qb = ui & 1;
+      Pieces it;
+      it.init(p, blockIdx.x, gridDim.x);
+      Unit x;
+      for (; !*abort_flag && it.next(p, &x); ++ui) {
+        const int n = x.n, qb = ui & 1;
         mbar_wait(b_qfull + 8 * qb, (ui >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
         const uint64_t dQ = dQ0 + static_cast<uint64_t>((qb * L::kQBytes) >> 4);
         for (int j = 0; j < n; ++j, ++g) {
@@ -341,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(b_sfull + 8 * sb);
         }
-        // the unit's Q buffer is free once its last S^T completes
+        // the piece's Q buffer is free once its last S^T completes
         umma_commit(b_qempty + 8 * qb);
       }
       // every MMA issued above completes before TMEM is released
@@ -356,10 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV0 = sdesc_sw128(sRing + kTileBytes, 16384, 1024);
       const uint64_t dP0 = sdesc_sw128(sP, 16, 1024);
       int g = 0, ui = 0;
-      for (long long u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++ui) {
-        const int n = load_unit(p, u).n, ob = ui & 1;
-        // the unit's first P V overwrites its O^T buffer: the epilogue of the
-        // unit two before must have read it
+      Pieces it;
+      it.init(p, blockIdx.x, gridDim.x);
+      Unit x;
+      for (; !*abort_flag && it.next(p, &x); ++ui) {
+        const int n = x.n, ob = ui & 1;
+        // the piece's first P V overwrites its O^T buffer: the epilogue of the
+        // piece two before must have read it
         if (ui >= 2) mbar_wait(b_ofree + 8 * ob, ((ui >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
         for (int j = 0; j < n; ++j, ++g) {
           const int st = g % L::kStages;
@@ -390,8 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     int g = 0, ui = 0;
     bool stop = false;
-    for (long long u = blockIdx.x; u < total && !stop; u += gridDim.x, ++ui) {
-      const Unit x = load_unit(p, u);
+    Pieces it;
+    it.init(p, blockIdx.x, gridDim.x);
+    Unit x;
+    for (; !stop && it.next(p, &x); ++ui) {
       const int ob = ui & 1;
       float l_part[N];
 #pragma unroll
@@ -472,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(b_pfull);
       }
       if (stop) break;
-      // unit epilogue: O^T and the column sums
+      // piece epilogue: O^T and the column sums
       const bool ok = mbar_wait(b_pvdone, (g - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
       stop = group_or(2, !ok || *abort_flag);
       if (stop) break;
@@ -491,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.part_ml[x.slot * 2 * p.G + t] = mref[t];
         p.part_ml[x.slot * 2 * p.G + p.G + t] = lsum;
       }
-      named_bar_sync(1, 128);  // mref is reset for the next unit only after every thread read it
+      named_bar_sync(1, 128);  // mref is reset for the next piece only after every thread read it
     }
   }
   tc_fence_before();
@@ -513,12 +563,10 @@ struct PrepParams {
   const int32_t* cu_q_rows;  // [B+1] plan row prefix of the sequences
   const int32_t* page_table;
   int32_t* remap;
-  int4* units;
-  int32_t* cu_units;  // [Hmask*B + 1]
-  int32_t* nunits;
+  int32_t* cu_rows;  // [Hmask*B + 1]: prefix of the rows' entry counts
   uint32_t* err;
   long long nP, nF, num_pages;
-  int B, Hmask, rows, pages_per_seq, page_size, chunks, chunk_rows, T;
+  int B, Hmask, rows, pages_per_seq, page_size, chunks, chunk_rows;
 };
 
 // K tile entries of (mask head, sequence) row r = hm * B + b.
@@ -546,8 +594,7 @@ __device__ __forceinline__ int last_le(const int32_t* a, int lo, int hi, long lo
   return lo;
 }
 
-// Block 0: units per row (exclusive scan into cu_units) and the unit
-// descriptors.  Every other block: the page conversion of 256 list entries
+// Block 0: entries per row, exclusive scan into cu_rows.  Every other block: the page conversion of 256 list entries
 // (partial entries first, then full ones), one thread each.
 __global__ void __launch_bounds__(256) k_decode_prep(PrepParams p) {
   if (blockIdx.x > 0) {
@@ -592,10 +639,10 @@ __global__ void __launch_bounds__(256) k_decode_prep(PrepParams p) {
   __syncthreads();
   for (int base = 0; base < R; base += blockDim.x) {
     const int r = base + threadIdx.x;
-    int cnt = 0, n = 0, p0 = 0, np = 0, f0 = 0, b = 0;
+    int cnt = 0;
     if (r < R) {
-      n = row_entries(p, r, &p0, &np, &f0, &b);
-      cnt = (n + p.T - 1) / p.T;
+      int p0, np, f0, b;
+      cnt = row_entries(p, r, &p0, &np, &f0, &b);
     }
     int x = cnt;
 #pragma unroll
@@ -615,31 +662,34 @@ __global__ void __launch_bounds__(256) k_decode_prep(PrepParams p) {
       s_warp[lane] = v;
     }
     __syncthreads();
-    const int u0 = s_carry + (wid ? s_warp[wid - 1] : 0) + x - cnt;
-    if (r < R) {
-      p.cu_units[r] = u0;
-      for (int k = 0; k < cnt; ++k) p.units[u0 + k] = make_int4(r / p.B, b, k * p.T, min(n, (k + 1) * p.T));
-    }
+    if (r < R) p.cu_rows[r] = s_carry + (wid ? s_warp[wid - 1] : 0) + x - cnt;
     __syncthreads();
     if (threadIdx.x == 0) s_carry += s_warp[nw - 1];
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    p.cu_units[R] = s_carry;
-    *p.nunits = s_carry;
-  }
+  if (threadIdx.x == 0) p.cu_rows[R] = s_carry;
 }
 
 // ------------------------------------------------------------ combine
 struct CombineParams {
   const float* part_o;
   const float* part_ml;
-  const int32_t* cu_units;
+  const int32_t* cu_rows;
   __nv_bfloat16* o;
   float* lse;
-  int B, Hq, Hk, Hmask, G, gy, total_q;
+  int B, Hq, Hk, Hmask, G, gy, total_q, R, C;
 };
 
+// The CTA of k_decode (C of them over W tiles) whose range holds tile x.
+__device__ __forceinline__ int cta_of(long long x, long long W, int C) {
+  long long c = x * C / W;
+  while (c + 1 < C && W * (c + 1) / C <= x) ++c;
+  while (c > 0 && W * c / C > x) --c;
+  return static_cast<int>(c);
+}
+
+// One warp per (query row, head): the pieces of its segment are those of
+// the CTAs whose ranges meet the segment, in slots s + c.
 __global__ void __launch_bounds__(256) k_decode_combine(CombineParams p) {
   const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -648,17 +698,20 @@ __global__ void __launch_bounds__(256) k_decode_combine(CombineParams p) {
   const int b = qr;  // one query row per sequence
   const int hm = (p.Hmask == 1) ? 0 : h;
   const int gi = (p.Hmask == 1) ? h / p.G : 0, c = h % p.G;
-  const int u0 = __ldg(p.cu_units + hm * p.B + b), u1 = __ldg(p.cu_units + hm * p.B + b + 1);
+  const long long sg = static_cast<long long>(hm * p.B + b) * p.gy + gi;
+  const long long x0 = seg_start(p.cu_rows, p.R, p.gy, sg), x1 = seg_start(p.cu_rows, p.R, p.gy, sg + 1);
+  const long long W = static_cast<long long>(p.gy) * __ldg(p.cu_rows + p.R);
+  const int c0 = (x1 > x0) ? cta_of(x0, W, p.C) : 0, c1 = (x1 > x0) ? cta_of(x1 - 1, W, p.C) : -1;
   float M = -INFINITY;
-  for (int u = u0; u < u1; ++u) {
-    const long long slot = static_cast<long long>(u) * p.gy + gi;
+  for (int k = c0; k <= c1; ++k) {
+    const long long slot = sg + k;
     const float l = __ldg(p.part_ml + slot * 2 * p.G + p.G + c);
     if (l > 0.0f) M = fmaxf(M, __ldg(p.part_ml + slot * 2 * p.G + c));
   }
   float Lsum = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  for (int u = u0; u < u1; ++u) {
-    const long long slot = static_cast<long long>(u) * p.gy + gi;
+  for (int k = c0; k <= c1; ++k) {
+    const long long slot = sg + k;
     const float l = __ldg(p.part_ml + slot * 2 * p.G + p.G + c);
     if (!(l > 0.0f)) continue;
     const float w = exp2f(__ldg(p.part_ml + slot * 2 * p.G + c) - M);
@@ -725,26 +778,21 @@ size_t decode_workspace_bytes(const DecodeLaunch& a, DecodeSizes* z) {
   s.chunk_rows = a.page_size < kTile ? a.page_size : kTile;
   s.chunks = kTile / s.chunk_rows;
   const long long entries = pl->P + pl->F;
-  const long long work = entries * s.gy;  // tile loads over every unit
-  // units of at most T tiles: about four per SM, at least 4 tiles each
-  long long T = (work + 4LL * a.num_sms - 1) / (4LL * a.num_sms);
-  if (T < 4) T = 4;
-  if (T > 1024) T = 1024;
-  s.T = static_cast<int>(T);
+  const long long work = entries * s.gy;  // K/V tiles over every segment
+  // one persistent CTA per SM, fewer when there are fewer tiles
+  s.C = static_cast<int>(work < a.num_sms ? (work > 0 ? work : 1) : a.num_sms);
   const long long rows = static_cast<long long>(pl->Hmask) * g.batch;
-  s.max_units = rows + (entries + T - 1) / T;
+  s.slots = rows * s.gy + s.C;  // piece slots s + c
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   size_t off = 0;
   s.off_remap = off;
   off += al(4ull * static_cast<size_t>(entries > 0 ? entries : 1) * s.chunks);
-  s.off_units = off;
-  off += al(16ull * static_cast<size_t>(s.max_units > 0 ? s.max_units : 1));
   s.off_cu = off;
-  off += al(4ull * static_cast<size_t>(rows + 2));
+  off += al(4ull * static_cast<size_t>(rows + 1));
   s.off_part_o = off;
-  off += al(4ull * static_cast<size_t>(s.max_units) * s.gy * s.G * D);
+  off += al(4ull * static_cast<size_t>(s.slots) * s.G * D);
   s.off_part_ml = off;
-  off += al(8ull * static_cast<size_t>(s.max_units) * s.gy * s.G);
+  off += al(8ull * static_cast<size_t>(s.slots) * s.G);
   s.bytes = off;
   *z = s;
   return off;
@@ -756,9 +804,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   const Geometry& g = pl->geom;
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* remap = reinterpret_cast<int32_t*>(w + s.off_remap);
-  int4* units = reinterpret_cast<int4*>(w + s.off_units);
   int32_t* cu = reinterpret_cast<int32_t*>(w + s.off_cu);
-  int32_t* nunits = cu + pl->Hmask * g.batch + 1;
   float* part_o = reinterpret_cast<float*>(w + s.off_part_o);
   float* part_ml = reinterpret_cast<float*>(w + s.off_part_ml);
   uint32_t* err = fwd_error_word();
@@ -777,9 +823,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   pp.cu_q_rows = pl->cu_q_rows;
   pp.page_table = a.page_table;
   pp.remap = remap;
-  pp.units = units;
-  pp.cu_units = cu;
-  pp.nunits = nunits;
+  pp.cu_rows = cu;
   pp.err = err;
   pp.nP = pl->P;
   pp.nF = pl->F;
@@ -791,7 +835,6 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   pp.page_size = a.page_size;
   pp.chunks = s.chunks;
   pp.chunk_rows = s.chunk_rows;
-  pp.T = s.T;
   const long long entries = pl->P + pl->F;
   k_decode_prep<<<static_cast<unsigned>(1 + (entries + 255) / 256), 256, 0, st>>>(pp);
   cudaError_t e = cudaGetLastError();
@@ -818,8 +861,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   p.f_idx = pl->f_idx;
   p.payload = pl->payload;
   p.remap = remap;
-  p.units = units;
-  p.nunits = nunits;
+  p.cu_rows = cu;
   p.part_o = part_o;
   p.part_ml = part_ml;
   p.err = err;
@@ -835,10 +877,9 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   p.oob_row = static_cast<int>(cache_rows);
   p.nP = pl->P;
   p.nF = pl->F;
-  p.max_units = s.max_units;
+  p.R = pl->Hmask * g.batch;
   p.scale_log2 = a.scale * kLog2e;
-  const long long max_work = s.max_units * s.gy;
-  const int grid = static_cast<int>(max_work < a.num_sms ? (max_work > 0 ? max_work : 1) : a.num_sms);
+  const int grid = s.C;
   if (N == 16)
     e = launch_decode_n<16>(mq, mk, mv, p, grid, st);
   else if (N == 32)
@@ -853,7 +894,9 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   CombineParams cp{};
   cp.part_o = part_o;
   cp.part_ml = part_ml;
-  cp.cu_units = cu;
+  cp.cu_rows = cu;
+  cp.R = pl->Hmask * g.batch;
+  cp.C = s.C;
   cp.o = static_cast<__nv_bfloat16*>(a.o);
   cp.lse = a.lse;
   cp.B = g.batch;

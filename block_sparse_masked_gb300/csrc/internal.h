@@ -227,9 +227,9 @@ struct DecodeLaunch {
   int num_sms;
 };
 struct DecodeSizes {
-  int G, gy, chunks, chunk_rows, T;
-  long long max_units;
-  size_t off_remap, off_units, off_cu, off_part_o, off_part_ml, bytes;
+  int G, gy, chunks, chunk_rows, C;  // C: CTAs of the decode kernel
+  long long slots;                   // piece result slots
+  size_t off_remap, off_cu, off_part_o, off_part_ml, bytes;
 };
 // Workspace layout of one decode call; returns its size in bytes.
 size_t decode_workspace_bytes(const DecodeLaunch& a, DecodeSizes* s);

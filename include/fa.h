@@ -235,10 +235,10 @@ int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, con
  * page_size], row j % page_size: before the attention kernel, one small
  * kernel converts every K tile of the plan's lists into the physical rows
  * of its pages (the page table becomes part of the index lists; the
- * attention loop sees physical rows only), and splits each sequence's list
- * into units of a few K tiles (Split-K).  The attention kernel runs one
- * persistent CTA per SM over the units; a last kernel merges the units of
- * each query row.
+ * attention loop sees physical rows only).  The attention kernel runs one
+ * persistent CTA per SM; the K tiles of all sequences and K/V heads are cut
+ * into equal ranges, one per CTA (Split-K: a sequence's list may be split
+ * over several CTAs); a last kernel merges the pieces of each query row.
  *   q: device bf16 [batch, heads_q, 128]; k_cache, v_cache: device bf16
  *   [num_pages, page_size, heads_k, 128]; page_table: device int32
  *   [batch, pages_per_seq] (entries for pages past a sequence's k_len are
@@ -248,8 +248,8 @@ int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, con
  * of the device error flags (fa_device_error_flags) and reads zeros.
  * One mask for every head (Hmask = 1, any GQA group up to 64 query heads
  * per K/V head), or per-head masks without GQA; no score mods
- * (FA_ERR_UNSUPPORTED otherwise).  A workspace (index conversion, units,
- * per-unit O, max and sum) comes from the plan's allocator or the
+ * (FA_ERR_UNSUPPORTED otherwise).  A workspace (index conversion, row
+ * prefix, per-piece O, max and sum) comes from the plan's allocator or the
  * library's pool and is returned in stream order.  Asynchronous on
  * `stream`: three kernel launches.  Pointers must be 16-byte aligned.
  */
