@@ -94,9 +94,9 @@ struct DecLayout {
   static constexpr int kOffRing = 0;
   static constexpr int kOffQ = kStages * kStageBytes;        // [2 buffers][2 halves][N rows][128 B]
   static constexpr int kQBytes = 2 * N * 128;
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;          // P: [2 key halves][N rows][128 B]
-  static constexpr int kOffSmall = kOffP + kQBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2;
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;          // P: [2 buffers][2 key halves][N rows][128 B]
+  static constexpr int kOffSmall = kOffP + 2 * kQBytes;
+  static constexpr int kNumBars = 2 * kStages + 2 * 8;
   static constexpr int kSmTmem = 8 * kNumBars;
   static constexpr int kSmAbort = kSmTmem + 4;
   static constexpr int kSmRed = (kSmAbort + 4 + 15) & ~15;  // [4 warps][N] floats
@@ -215,7 +215,8 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const float (&f)[N]) {
 
 // Per-column reduction of v[N] over the 128 softmax threads (thread t =
 // 32 warp + lane); red is the [4][N] exchange area.  Thread t < N gets the
-// result for column t; the others get 0.
+// result for column t; the others get 0.  The caller passes another barrier
+// of the 128 threads before red is written again.
 template <int N, bool MAX>
 __device__ __forceinline__ float group_reduce(const float (&v)[N], float* red, int warp, int lane) {
 #pragma unroll
@@ -233,7 +234,6 @@ __device__ __forceinline__ float group_reduce(const float (&v)[N], float* red, i
     const float a = red[t], b = red[N + t], x = red[2 * N + t], y = red[3 * N + t];
     out = MAX ? fmaxf(fmaxf(a, b), fmaxf(x, y)) : (a + b) + (x + y);
   }
-  named_bar_sync(1, 128);  // red may be reused after this
   return out;
 }
 
@@ -268,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_full = bars, b_empty = b_full + 8 * L::kStages;
   const uint32_t b_qfull = b_empty + 8 * L::kStages, b_qempty = b_qfull + 16;
   const uint32_t b_sfull = b_qempty + 16, b_sfree = b_sfull + 16;
-  const uint32_t b_pfull = b_sfree + 16, b_pvdone = b_pfull + 8;
-  const uint32_t b_ofree = b_pvdone + 8, b_drain = b_ofree + 16, b_drain2 = b_drain + 8;
+  const uint32_t b_pfull = b_sfree + 16, b_pvdone = b_pfull + 16;  // [2] each: one per P buffer
+  const uint32_t b_ofree = b_pvdone + 16, b_drain = b_ofree + 16, b_drain2 = b_drain + 8;
   static_assert(8 * L::kNumBars == L::kSmTmem, "barrier count");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(small + L::kSmTmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(small + L::kSmAbort);
@@ -289,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_sfull + 8 * i, 1);
       mbar_init(b_sfree + 8 * i, 4);  // lane 0 of each softmax warp
       mbar_init(b_ofree + 8 * i, 4);
+      mbar_init(b_pfull + 8 * i, 4);
+      mbar_init(b_pvdone + 8 * i, 1);
     }
-    mbar_init(b_pfull, 4);
-    mbar_init(b_pvdone, 1);
     mbar_init(b_drain, 1);
     mbar_init(b_drain2, 1);
     *abort_flag = 0;
@@ -301,6 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
+  // P rows of query columns past the group stay zero: only rows < G are written
+  for (int i = threadIdx.x; i < 2 * L::kQBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(gbase + L::kOffP)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -410,20 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // piece two before must have read it
         if (ui >= 2) mbar_wait(b_ofree + 8 * ob, ((ui >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
         for (int j = 0; j < n; ++j, ++g) {
-          const int st = g % L::kStages;
-          mbar_wait(b_pfull, g & 1, abort_flag, p.err, kWaitTimeoutNs);
+          const int st = g % L::kStages, pb = g & 1;
+          mbar_wait(b_pfull + 8 * pb, (g >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
           if (*abort_flag) break;
           tc_fence_after();
           const uint64_t dV = dV0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+          const uint64_t dP = dP0 + static_cast<uint64_t>((pb * L::kQBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t offP = ((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4;
-            umma_bf16_ss(tmem + 2 * N + N * ob, dV + static_cast<uint64_t>((kk * 2048) >> 4), dP0 + offP, idO,
+            umma_bf16_ss(tmem + 2 * N + N * ob, dV + static_cast<uint64_t>((kk * 2048) >> 4), dP + offP, idO,
                          (j > 0 || kk > 0) ? 1u : 0u);
           }
           // the stage (its K was read by S^T, which completed before P was written) and P are free
           umma_commit(b_empty + 8 * st);
-          umma_commit(b_pvdone);
+          umma_commit(b_pvdone + 8 * pb);
         }
       }
       umma_commit(b_drain2);
@@ -478,15 +483,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha[t] = need ? exp2f(mo - mn) : 1.0f;
           mref[t] = mn;
         }
-        const bool any = group_or(2, need);
-        // P V of the previous step has completed: the P buffer is free and O^T is current
-        if (g > 0) ok = mbar_wait(b_pvdone, (g - 1) & 1, abort_flag, p.err, kWaitTimeoutNs) && ok;
-        stop = group_or(2, !ok || *abort_flag);
-        if (stop) break;
+        // P buffer g & 1 is free once the P V of step g - 2 has completed
+        const int pb = g & 1;
+        if (g >= 2) ok = mbar_wait(b_pvdone + 8 * pb, ((g >> 1) - 1) & 1, abort_flag, p.err, kWaitTimeoutNs) && ok;
+        // one barrier in the common case: stop and rescale are both rare
+        bool any = false;
+        if (group_or(2, need || !ok || *abort_flag)) {
+          stop = group_or(2, !ok || *abort_flag);
+          if (stop) break;
+          any = true;  // no thread had a failed wait, so some column's max rose
+        }
         if (any) {
 #pragma unroll
           for (int c = 0; c < N; ++c) l_part[c] *= alpha[c];
           if (j > 0) {
+            // O^T is rescaled between the P V of step g - 1 and that of step g
+            ok = mbar_wait(b_pvdone + 8 * (pb ^ 1), ((g - 1) >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
+            stop = group_or(2, !ok || *abort_flag);
+            if (stop) break;
             tc_fence_after();
             float o[N];
             ld_cols<N>(lane_addr + 2 * N + N * ob, o);
@@ -496,16 +510,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
         }
-        // P (bf16) into the K-major P buffer: row c, column (key) t
-        const uint32_t prow = sP + (t >> 6) * (N * 128);
+        // P (bf16) into the K-major P buffer: row c, column (key) t; rows of
+        // columns past the group stay zero
+        const uint32_t prow = sP + pb * L::kQBytes + (t >> 6) * (N * 128);
         const uint32_t chunk = static_cast<uint32_t>((t & 63) >> 3), byte = static_cast<uint32_t>((t & 7) * 2);
 #pragma unroll
         for (int c = 0; c < N; ++c) {
-          const float pv = exp2f(s[c] - mref[c]);
-          l_part[c] += pv;
-          const __nv_bfloat16 hv = __float2bfloat16_rn(pv);
-          const uint32_t a = prow + c * 128 + ((chunk ^ static_cast<uint32_t>(c & 7)) << 4) + byte;
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t*>(&hv)) : "memory");
+          if (c < p.G) {
+            const float pv = exp2f(s[c] - mref[c]);
+            l_part[c] += pv;
+            const __nv_bfloat16 hv = __float2bfloat16_rn(pv);
+            const uint32_t a = prow + c * 128 + ((chunk ^ static_cast<uint32_t>(c & 7)) << 4) + byte;
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<const uint16_t*>(&hv)) : "memory");
+          }
         }
         // keys past the sequence: their V rows (unused cache memory) become
         // zeros, so that 0 * V stays 0 in the product
@@ -519,11 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_pfull);
+        if (lane == 0) mbar_arrive(b_pfull + 8 * pb);
       }
       if (stop) break;
       // piece epilogue: O^T and the column sums
-      const bool ok = mbar_wait(b_pvdone, (g - 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
+      const bool ok = mbar_wait(b_pvdone + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag, p.err, kWaitTimeoutNs);
       stop = group_or(2, !ok || *abort_flag);
       if (stop) break;
       tc_fence_after();
