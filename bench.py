@@ -228,7 +228,7 @@ def roofline(flops: float, alg_bytes: float, ms: float, peaks: dict, peak_src: s
     return r
 
 
-def time_forward_alone(runner, dp, plan, flush, stream, reps: int):
+def time_forward_alone(runner, dp, plan, flush, stream, reps: int, choice: int = 0):
     """Event pairs around each forward launch; L2 flushed first, and a queued
     sleep keeps the host ahead so that the pair brackets the launch itself."""
     import torch
@@ -237,7 +237,7 @@ def time_forward_alone(runner, dp, plan, flush, stream, reps: int):
         flush.zero_()
         torch.cuda._sleep(SLEEP_CYCLES)
         kev[i][0].record(stream)
-        runner.forward(dp, plan)
+        runner.forward(dp, plan, choice=choice)
         kev[i][1].record(stream)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in kev]
@@ -306,6 +306,21 @@ def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, s
             runner.forward(dp, plan)
         torch.cuda.synchronize()
         ms = statistics.mean(time_forward_alone(runner, dp, plan, flush, stream, reps))
+        # the other physical plan for this mask (Tessera-style plan choice),
+        # timed the same way; the library's rule picks the default one
+        alt = None
+        if w.mask_kind == "blocks" and w.d == 128 and w.block_q % 64 == 0 and w.block_kv % 64 == 0:
+            alt = ("coarsened_128x128", fa.FA_FWD_COARSENED, "direct_64x64")
+        elif w.mask_kind == "intervals" and not (w.softcap and w.softcap > 0) and w.alibi_slopes is None:
+            alt = ("one_q_tile_per_task", fa.FA_FWD_ONE_TILE, "two_q_tiles_per_task")
+        choices = None
+        if alt is not None:
+            for _ in range(2):
+                runner.forward(dp, plan, choice=alt[1])
+            torch.cuda.synchronize()
+            alt_ms = statistics.mean(time_forward_alone(runner, dp, plan, flush, stream, reps, alt[1]))
+            choices = {alt[2] + "_ms": ms, alt[0] + "_ms": alt_ms, "default": alt[2],
+                       "regret_of_default": ms / min(ms, alt_ms)}
         plan.free()
         b_us, b_ms = time_plan_builds(fa, runner, dp, flush, stream, max(10, reps // 2))
         rf = roofline(flops, algorithmic_bytes(w, info), ms, peaks, peak_src, known_traffic(name))
@@ -315,7 +330,7 @@ def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, s
                      "bound": rf["bound"], "frac": rf["frac"], "alg_bytes": rf["alg_bytes"],
                      "traffic": rf["traffic"], "plan_build_us": b_us, "plan_gpu_ms": b_ms,
                      "visible_pairs": info["visible_pairs"] * (w.Hq if info["mask_heads"] == 1 else 1),
-                     "kernel": fwd_kernel_name(w), "backward": bwd}
+                     "kernel": fwd_kernel_name(w), "plan_choices": choices, "backward": bwd}
         del dp, plan, w
         torch.cuda.empty_cache()
     out["decode_paged"] = time_decode(fa, runner, W, flush, stream, peaks, peak_src, reps, seed)

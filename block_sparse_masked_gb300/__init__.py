@@ -50,6 +50,8 @@ FA_DTYPE_BF16 = 0
 FA_PLAN_BACKWARD = 1
 FA_MOD_SOFTCAP = 1
 FA_MOD_ALIBI = 2
+FA_FWD_ONE_TILE = 16    # plan choice: one Q tile per task for interval plans
+FA_FWD_COARSENED = 32   # plan choice: 128x128 tiles for 64-aligned block plans
 FA_TILE_Q = 128
 FA_TILE_K = 128
 FA_PAYLOAD_WORDS = 4
@@ -272,11 +274,12 @@ def fa_plan_free(plan: Plan, stream=None):
 
 
 def fa_fwd(plan: Plan, q, k, v, o, lse, geom: FaGeometry, scale: float, softcap: float = 0.0,
-           alibi_slopes=None, stream=None):
-    """Launch the forward; alibi_slopes is a host float32 array of heads_q values or None."""
+           alibi_slopes=None, stream=None, choice: int = 0):
+    """Launch the forward; alibi_slopes is a host float32 array of heads_q
+    values or None; choice holds FA_FWD_* plan-choice bits."""
     mods = None
     keep = None
-    flags = 0
+    flags = int(choice)
     if softcap and softcap > 0:
         flags |= FA_MOD_SOFTCAP
     if alibi_slopes is not None:

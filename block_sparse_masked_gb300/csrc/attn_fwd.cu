@@ -1069,7 +1069,7 @@ cudaError_t launch_d(const FwdLaunch& a, cudaStream_t st, const char** why) {
 // with two warpgroups per tile, runs it faster; block-mask plans also stay
 // here, with empty 64-key halves skipped.
 static bool use_pair(const FwdLaunch& a) {
-  return a.plan->mask_kind == MASK_INTERVALS && (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) == 0;
+  return a.plan->mask_kind == MASK_INTERVALS && (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI | FA_FWD_ONE_TILE)) == 0;
 }
 cudaError_t launch_fwd_d64(const FwdLaunch& a, cudaStream_t st, const char** why) {
   if (use_pair(a)) return launch_fwd_pair_d64(a, st, why);

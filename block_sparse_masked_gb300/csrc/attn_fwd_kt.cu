@@ -808,7 +808,7 @@ bool make_map64(CUtensorMap* m, const void* ptr, int64_t rows, int64_t heads, ui
 bool fwd_kt_applies(const FwdLaunch& a) {
   const fa_plan* pl = a.plan;
   return pl->mask_kind == MASK_BLOCKS && pl->geom.head_dim == D &&
-         (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)) == 0 && pl->block_q > 0 && pl->block_kv > 0 &&
+         (a.flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI | FA_FWD_COARSENED)) == 0 && pl->block_q > 0 && pl->block_kv > 0 &&
          pl->block_q % kHalf == 0 && pl->block_kv % kHalf == 0;
 }
 

@@ -550,7 +550,7 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
   a.lse = lse;
   a.scale = scale;
   if (mods) {
-    a.flags = mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI);
+    a.flags = mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI | FA_FWD_ONE_TILE | FA_FWD_COARSENED);
     a.softcap = mods->softcap;
     a.slopes = mods->alibi_slopes;
     if ((a.flags & FA_MOD_SOFTCAP) && !(mods->softcap > 0.0f))

@@ -58,10 +58,11 @@ def build_plan(dp: DeviceProblem, stream=None, allocator=None, backward: bool = 
                                 stream=stream, allocator=allocator, backward=backward)
 
 
-def forward(dp: DeviceProblem, plan: Plan, stream=None):
+def forward(dp: DeviceProblem, plan: Plan, stream=None, choice: int = 0):
+    """fa_fwd on the problem; choice: FA_FWD_* plan-choice bits."""
     w = dp.w
     fa_fwd(plan, dp.q, dp.k, dp.v, dp.o, dp.lse, dp.geom, w.scale, softcap=w.softcap,
-           alibi_slopes=w.alibi_slopes, stream=stream)
+           alibi_slopes=w.alibi_slopes, stream=stream, choice=choice)
     return dp.o, dp.lse
 
 

@@ -49,6 +49,16 @@ enum {
 enum { FA_LAYOUT_BSHD = 0, FA_LAYOUT_THD = 1 };
 enum { FA_DTYPE_BF16 = 0 };
 enum { FA_MOD_SOFTCAP = 1, FA_MOD_ALIBI = 2 };
+/* Physical plan choices of fa_fwd, also passed in fa_mods.flags ("Decoupling
+ * Logical Masks from GPU Execution for Dynamic Block-Sparse Attention",
+ * physical mappings and task organisation).  By default interval plans
+ * without mods run two vertically adjacent Q tiles per task, and block plans
+ * whose logical blocks are multiples of 64 (head_dim 128, no mods) run the
+ * Direct mapping: one 64-row half of a Q tile per task, stepping through
+ * its live 64x64 blocks.  FA_FWD_ONE_TILE runs one Q tile per task
+ * instead; FA_FWD_COARSENED runs a block plan on whole 128x128 tiles (the
+ * Coarsened mapping).  Results agree within the forward's tolerance. */
+enum { FA_FWD_ONE_TILE = 16, FA_FWD_COARSENED = 32 };
 
 /* Physical tile of this build's consumer. */
 #define FA_TILE_Q 128
@@ -172,7 +182,8 @@ int fa_plan_free(fa_plan* plan, void* stream);
  *   FA_MOD_SOFTCAP: s <- softcap * tanh(s / softcap)
  *   FA_MOD_ALIBI:   s <- s + alibi_slopes[h] * (k - q)   (sample-local k, q)
  * applied in that order.  alibi_slopes is a host array of heads_q floats,
- * read during the call. */
+ * read during the call.  flags may also hold the plan choices FA_FWD_*
+ * (fa_fwd only). */
 typedef struct {
   int32_t flags;
   float softcap;

@@ -34,6 +34,7 @@ DEVERR_BOUNDS = 4
 IN_CHILD = os.environ.get("BSM_FA_CHECKED") == "1"
 
 SMALL_SUITES = ["tests/test_gpu_plan.py", "tests/test_gpu_fwd.py", "tests/test_gpu_plan_backward.py",
+                "tests/test_gpu_decode.py",
                 "tests/test_gpu_bwd.py", "tests/test_gpu_checked.py"]
 
 

@@ -282,3 +282,23 @@ def test_block_mask_growing_scores_rescale():
     dp, plan = run(w)
     PT.check_rows(w, dp.o, dp.lse, all_rows(w))
     plan.free()
+
+
+@pytest.mark.parametrize("name,choice", [
+    ("blocks64", fa.FA_FWD_COARSENED),   # Coarsened 128x128 tiles instead of the Direct 64x64 steps
+    ("intervals", fa.FA_FWD_ONE_TILE),   # one Q tile per task instead of two
+])
+def test_plan_choices_agree_with_the_oracle(name, choice):
+    if name == "blocks64":
+        w = _block_problem(61, B=1, S=700, H=2, Hk=1, blk_q=64, blk_kv=128, density=0.3, Sk=650)
+    else:
+        w = _random_problem(62, B=2, S=500, H=2, d=128, nfunc=3)
+    dp = runner.to_device(w)
+    plan = runner.build_plan(dp)
+    rows = all_rows(w)
+    for c in (0, choice):
+        runner.forward(dp, plan, choice=c)
+        torch.cuda.synchronize()
+        assert fa.fa_device_error_flags() == 0
+        PT.check_rows(w, dp.o, dp.lse, rows)
+    plan.free()
