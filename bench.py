@@ -228,6 +228,13 @@ def roofline(flops: float, alg_bytes: float, ms: float, peaks: dict, peak_src: s
     return r
 
 
+def plan_kw(w) -> dict:
+    """Block plans ask for quadrant bits only: the library keeps them alone
+    when they are exact (64-aligned blocks over 64-multiple lengths), which
+    is all the Direct 64x64 forward reads; otherwise it builds the words."""
+    return {"quadrant_payload": True} if w.mask_kind == "blocks" else {}
+
+
 def time_forward_alone(runner, dp, plan, flush, stream, reps: int, choice: int = 0):
     """Event pairs around each forward launch; L2 flushed first, and a queued
     sleep keeps the host ahead so that the pair brackets the launch itself."""
@@ -243,7 +250,7 @@ def time_forward_alone(runner, dp, plan, flush, stream, reps: int, choice: int =
     return [a.elapsed_time(b) for a, b in kev]
 
 
-def time_plan_builds(fa, runner, dp, flush, stream, reps: int):
+def time_plan_builds(fa, runner, dp, flush, stream, reps: int, **kw):
     """Host microseconds of each build (the call, including its one header
     read-back) and stream milliseconds until its last planner kernel ends."""
     import torch
@@ -253,7 +260,7 @@ def time_plan_builds(fa, runner, dp, flush, stream, reps: int):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        p = runner.build_plan(dp)
+        p = runner.build_plan(dp, **kw)
         e1.record(stream)
         host_us.append(fa.fa_plan_info_get(p)["build_us"])
         torch.cuda.synchronize()
@@ -323,6 +330,10 @@ def per_config_table(fa, runner, W, flush, stream, peaks, peak_src, reps: int, s
                        "regret_of_default": ms / min(ms, alt_ms)}
         plan.free()
         b_us, b_ms = time_plan_builds(fa, runner, dp, flush, stream, max(10, reps // 2))
+        if plan_kw(w):
+            qb_us, qb_ms = time_plan_builds(fa, runner, dp, flush, stream, max(10, reps // 2), **plan_kw(w))
+            choices = dict(choices or {}, plan_build_us_quadrant_payload=qb_us,
+                           plan_gpu_ms_quadrant_payload=qb_ms)
         rf = roofline(flops, algorithmic_bytes(w, info), ms, peaks, peak_src, known_traffic(name))
         bwd = time_backward(fa, runner, dp, flush, stream, max(5, reps // 2), flops, peaks)
         out[name] = {"workload": WORKLOAD_DESC[name], "fwd_ms": ms, "tflops": rf["tflops"],
@@ -477,7 +488,8 @@ def main():
     w = W.make(args.workload, args.seed + rank)
     dp = runner.to_device(w)
     stream = torch.cuda.current_stream()
-    plan = runner.build_plan(dp)
+    pkw = plan_kw(w)
+    plan = runner.build_plan(dp, **pkw)
     info = fa.fa_plan_info_get(plan, count_visible=True)
     plan.free()
     flops_step = visible_flops(info, w.Hq, w.d)
@@ -487,7 +499,7 @@ def main():
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        p = runner.build_plan(dp)
+        p = runner.build_plan(dp, **pkw)
         if ev is not None:
             ev[1].record(stream)
         runner.forward(dp, p)
@@ -526,7 +538,7 @@ def main():
     value = whole_job_tflops(flops_step, world, ms_per_step)
 
     # The forward kernel alone, for the roofline (see time_forward_alone).
-    plan_f = runner.build_plan(dp)
+    plan_f = runner.build_plan(dp, **pkw)
     torch.cuda.synchronize()
     fwd_ms = time_forward_alone(runner, dp, plan_f, flush, stream, args.steps)
     plan_f.free()
@@ -567,7 +579,7 @@ def main():
         for si in s_in:
             stream.wait_stream(si)
         stream.wait_event(outd[i])  # this copy's previous O/LSE have left the device
-        p = runner.build_plan(b)
+        p = runner.build_plan(b, **pkw)
         runner.forward(b, p)
         used[i].record(stream)
         s_out.wait_event(used[i])
@@ -605,6 +617,7 @@ def main():
         "config": workload_config(args),
         "plan_build_us": statistics.median(build_us),
         "plan_gpu_ms": statistics.median(plan_ms),
+        "plan_flags": "FA_PLAN_QUADRANT_PAYLOAD" if pkw else "none",
         "fwd_ms": fwd_mean,
         "fwd_ms_in_step": statistics.mean(fwd_in_step_ms),
         "fwd_tflops": fwd_tflops,

@@ -48,6 +48,7 @@ FA_LAYOUT_BSHD = 0
 FA_LAYOUT_THD = 1
 FA_DTYPE_BF16 = 0
 FA_PLAN_BACKWARD = 1
+FA_PLAN_QUADRANT_PAYLOAD = 2  # block plans: keep only the quadrant bits when they are exact
 FA_MOD_SOFTCAP = 1
 FA_MOD_ALIBI = 2
 FA_FWD_ONE_TILE = 16    # plan choice: one Q tile per task for interval plans
@@ -255,12 +256,14 @@ def fa_plan_build_intervals(geom: FaGeometry, mask_func, Hmask: int, nfunc: int,
 
 def fa_plan_build_blocks(geom: FaGeometry, block_mask, Hmask: int, block_q: int, block_kv: int,
                          stream=None, allocator: Optional[Allocator] = None,
-                         backward: bool = False) -> Plan:
-    """fa_plan_build_blocks, or fa_plan_build_blocks_ex with FA_PLAN_BACKWARD."""
+                         backward: bool = False, quadrant_payload: bool = False) -> Plan:
+    """fa_plan_build_blocks, or fa_plan_build_blocks_ex with FA_PLAN_BACKWARD
+    and/or FA_PLAN_QUADRANT_PAYLOAD."""
     out = _vp()
-    if backward:
+    flags = (FA_PLAN_BACKWARD if backward else 0) | (FA_PLAN_QUADRANT_PAYLOAD if quadrant_payload else 0)
+    if flags:
         _check(lib().fa_plan_build_blocks_ex(_c.byref(geom), _ptr(block_mask), Hmask, block_q,
-                                             block_kv, FA_PLAN_BACKWARD, _alloc_arg(allocator),
+                                             block_kv, flags, _alloc_arg(allocator),
                                              _stream_handle(stream), _c.byref(out)))
     else:
         _check(lib().fa_plan_build_blocks(_c.byref(geom), _ptr(block_mask), Hmask, block_q, block_kv,
@@ -369,7 +372,8 @@ def fa_plan_export(plan: Plan) -> dict:
         "partial_idx": np.zeros(P, np.int32),
         "full_offset": np.zeros(Hm * R + 1, np.int32),
         "full_idx": np.zeros(F, np.int32),
-        "payload": np.zeros((P, FA_TILE_Q, FA_PAYLOAD_WORDS), np.uint32),
+        # empty for a plan that keeps only quadrant bits (FA_PLAN_QUADRANT_PAYLOAD)
+        "payload": np.zeros((P if info["payload_bytes"] else 0, FA_TILE_Q, FA_PAYLOAD_WORDS), np.uint32),
         "work_desc": np.zeros((T, 4), np.int32),
         "halves": np.zeros(P, np.uint8),
         "quads": np.zeros(P, np.uint8),

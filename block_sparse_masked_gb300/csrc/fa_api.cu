@@ -347,6 +347,11 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   std::memcpy(plan->header, hdr, sizeof(hdr));
   plan->device = dev;
   plan->signature = bsm::Signature{}.hash();
+  // quadrant bits alone describe every partial entry of a 64-aligned block
+  // plan over 64-multiple lengths: the predicate words are then left out
+  plan->quads_only = (flags & FA_PLAN_QUADRANT_PAYLOAD) && !bwd && margs.kind == bsm::MASK_BLOCKS &&
+                     margs.block_q % 64 == 0 && margs.block_kv % 64 == 0 && g.seqlen_q % 64 == 0 &&
+                     g.seqlen_k % 64 == 0;
   if (allocator) {
     plan->alloc = *allocator;
     plan->custom_alloc = true;
@@ -356,7 +361,7 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   const size_t q_cur = c2.take(4ull * (B + 1)), q_seq = c2.take(32ull * B),
                q_po = c2.take(4ull * (nflat + 1)), q_fo = c2.take(4ull * (nflat + 1)),
                q_pi = c2.take(4ull * plan->P), q_fi = c2.take(4ull * plan->F),
-               q_pay = c2.take(16ull * bsm::kTile * plan->P), q_work = c2.take(16ull * plan->tasks),
+               q_pay = c2.take(plan->quads_only ? 0 : 16ull * bsm::kTile * plan->P), q_work = c2.take(16ull * plan->tasks),
                q_cq = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
                q_ck = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
                q_er = c2.take(4ull * plan->P), q_hv = c2.take(plan->P), q_qd = c2.take(plan->P);
@@ -373,7 +378,7 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   plan->f_off = reinterpret_cast<int32_t*>(pm + q_fo);
   plan->p_idx = reinterpret_cast<int32_t*>(pm + q_pi);
   plan->f_idx = reinterpret_cast<int32_t*>(pm + q_fi);
-  plan->payload = reinterpret_cast<uint32_t*>(pm + q_pay);
+  plan->payload = plan->quads_only ? nullptr : reinterpret_cast<uint32_t*>(pm + q_pay);
   plan->work_desc = reinterpret_cast<int32_t*>(pm + q_work);
   if (g.layout == FA_LAYOUT_THD) {
     plan->cu_seqlens_q = reinterpret_cast<int32_t*>(pm + q_cq);
@@ -478,7 +483,8 @@ int fa_plan_build_intervals_ex(const fa_geometry* geom, const int32_t* mask_func
   m.mask_func = mask_func;
   m.nfunc = nfunc;
   m.Hmask = Hmask;
-  if (flags & ~static_cast<uint32_t>(FA_PLAN_BACKWARD)) return fail(FA_ERR_INVALID_ARG, "unknown plan flags");
+  if (flags & ~static_cast<uint32_t>(FA_PLAN_BACKWARD | FA_PLAN_QUADRANT_PAYLOAD))
+    return fail(FA_ERR_INVALID_ARG, "unknown plan flags");
   return build_common(geom, m, flags, allocator, stream, out);
 }
 
@@ -507,7 +513,8 @@ int fa_plan_build_blocks_ex(const fa_geometry* geom, const uint8_t* block_mask, 
   m.nbq = cdiv(geom->seqlen_q, block_q);
   m.nbk = cdiv(geom->seqlen_k, block_kv);
   m.Hmask = Hmask;
-  if (flags & ~static_cast<uint32_t>(FA_PLAN_BACKWARD)) return fail(FA_ERR_INVALID_ARG, "unknown plan flags");
+  if (flags & ~static_cast<uint32_t>(FA_PLAN_BACKWARD | FA_PLAN_QUADRANT_PAYLOAD))
+    return fail(FA_ERR_INVALID_ARG, "unknown plan flags");
   return build_common(geom, m, flags, allocator, stream, out);
 }
 
@@ -537,6 +544,10 @@ int fa_fwd(const fa_plan* plan, const void* q, const void* k, const void* v, voi
   if (dev != plan->device) return fail(FA_ERR_PLAN_MISMATCH, "plan was built on device %d", plan->device);
   if (!(scale > 0.0f) || !std::isfinite(scale))
     return fail(FA_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (plan->quads_only &&
+      ((mods && (mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI | FA_FWD_COARSENED))) || g.head_dim != 128))
+    return fail(FA_ERR_UNSUPPORTED,
+                "a plan built with FA_PLAN_QUADRANT_PAYLOAD runs only the Direct 64x64 forward (head_dim 128, no mods)");
   if (plan->tasks == 0) return FA_OK;  // nothing to compute (e.g. no Q rows)
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   for (const void* ptr : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)})
@@ -711,7 +722,7 @@ int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream, f
   info->head_dim = plan->geom.head_dim;
   info->layout = plan->geom.layout;
   info->num_tasks = plan->tasks;
-  info->payload_bytes = plan->P * bsm::kTile * bsm::kPayloadWords * 4;
+  info->payload_bytes = plan->quads_only ? 0 : plan->P * bsm::kTile * bsm::kPayloadWords * 4;
   info->plan_bytes = static_cast<int64_t>(plan->mem.bytes + plan->bmem.bytes);
   info->signature = plan->signature;
   info->build_us = plan->build_us;
@@ -747,7 +758,7 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst) {
       {dst->partial_idx, plan->p_idx, 4ull * plan->P},
       {dst->full_offset, plan->f_off, 4ull * (nflat + 1)},
       {dst->full_idx, plan->f_idx, 4ull * plan->F},
-      {dst->payload, plan->payload, 16ull * bsm::kTile * plan->P},
+      {dst->payload, plan->payload, plan->quads_only ? 0 : 16ull * bsm::kTile * plan->P},
       {dst->work_desc, plan->work_desc, 16ull * plan->tasks},
       {dst->halves, plan->halves, static_cast<size_t>(plan->P)},
       {dst->quads, plan->quads, static_cast<size_t>(plan->P)},

@@ -96,6 +96,7 @@ struct fa_plan {
   // [P] quadrant (a, s) = rows 64a.. x key columns 64s..: bit 2a+s any element visible, bit 4+2a+s all
   uint8_t* quads = nullptr;
   int32_t block_q = 0, block_kv = 0;  // logical block geometry of a block-mask plan
+  bool quads_only = false;  // FA_PLAN_QUADRANT_PAYLOAD took effect: payload is null, quads describe the entries
   // backward K2Q view ("Flex Attention Mask Plan Design" §4.4, §4.7); absent
   // (k_rows = 0, null pointers) unless the plan was built with FA_PLAN_BACKWARD
   bool backward = false;

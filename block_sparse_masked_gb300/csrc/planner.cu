@@ -617,11 +617,12 @@ __device__ __forceinline__ QuadBits payload_blocks_entry(const BackParams& p, lo
     }
     r = seg_end;
   }
-  uint4* dst = reinterpret_cast<uint4*>(p.payload) + e * kTile + lane;
+  // a plan that keeps only quadrant bits has no payload words to write
+  uint4* dst = p.payload ? reinterpret_cast<uint4*>(p.payload) + e * kTile + lane : nullptr;
   QuadBits qb;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
+    if (dst) dst[32 * i] = make_uint4(mine[i][0], mine[i][1], mine[i][2], mine[i][3]);
     qb.add(i, mine[i]);
   }
   return qb;
@@ -699,6 +700,29 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
       sF[f][t] = (q0 + t < q_len) ? __ldg(Fg + static_cast<long long>(f) * p.total_q + q0 + t) : 0;
   }
   __syncthreads();  // the row's p_idx (written by warp 0) and sF are visible to the CTA
+  if (KIND == MASK_BLOCKS && p.payload == nullptr) {
+    // quadrant bits only (64-aligned logical blocks over 64-multiple
+    // lengths): each 64x64 quadrant lies inside one logical block pair and
+    // inside or outside the sample as a whole, so it is wholly visible or
+    // wholly masked; one thread per entry reads its four block-mask bytes
+    const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
+    for (int k = threadIdx.x; k < np; k += blockDim.x) {
+      const long long e = bsm_idx(pstart + k, p.nP, p.err);
+      const int j = p.p_idx[e];
+      uint32_t live = 0u;
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int qr = q0 + 64 * a, kc = j * kTile + 64 * s2;
+          if (qr < q_len && kc < k_len && __ldg(M + static_cast<long long>(qr / p.block_q) * p.nbk + kc / p.block_kv))
+            live |= 1u << (2 * a + s2);
+        }
+      p.halves[e] = static_cast<uint8_t>(((live & 5u) ? 1u : 0u) | ((live & 10u) ? 2u : 0u));
+      p.quads[e] = static_cast<uint8_t>(live | (live << 4));
+    }
+    return;
+  }
   for (int k = wi; k < np; k += 4) {
     const long long e = bsm_idx(pstart + k, p.nP, p.err);
     const int j = p.p_idx[e];
@@ -985,11 +1009,16 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
 }
 
 // ------------------------------------------------------------ statistics
-__global__ void k_count_visible(const uint32_t* payload, long long nwords, long long full_tiles,
-                                unsigned long long* out) {
+// Visible pairs of a plan: set payload bits of the partial entries (or,
+// for a plan that keeps only quadrant bits, 64 x 64 per fully visible
+// quadrant) plus 128 x 128 per full entry.
+__global__ void k_count_visible(const uint32_t* payload, long long nwords, const uint8_t* quads,
+                                long long nquads, long long full_tiles, unsigned long long* out) {
   unsigned long long acc = 0;
   for (long long i = blockIdx.x * 256LL + threadIdx.x; i < nwords; i += 256LL * gridDim.x)
     acc += __popc(payload[i]);
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < nquads; i += 256LL * gridDim.x)
+    acc += 64ull * 64ull * __popc(static_cast<uint32_t>(quads[i]) >> 4);
   for (int o = 16; o; o >>= 1) acc += __shfl_down_sync(kFull, acc, o);
   if ((threadIdx.x & 31) == 0) atomicAdd(out, acc);
   if (blockIdx.x == 0 && threadIdx.x == 0)
@@ -1169,8 +1198,9 @@ cudaError_t launch_back_k2q(const Geometry& g, const PlanWorkspace& ws, fa_plan*
 cudaError_t launch_count_visible(const fa_plan* plan, unsigned long long* out, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(unsigned long long), st);
   if (e != cudaSuccess) return e;
-  const long long nwords = plan->P * kTile * kPayloadWords;
-  k_count_visible<<<1024, 256, 0, st>>>(plan->payload, nwords, plan->F, out);
+  const long long nwords = plan->quads_only ? 0 : plan->P * kTile * kPayloadWords;
+  const long long nquads = plan->quads_only ? plan->P : 0;
+  k_count_visible<<<1024, 256, 0, st>>>(plan->payload, nwords, plan->quads, nquads, plan->F, out);
   return cudaGetLastError();
 }
 

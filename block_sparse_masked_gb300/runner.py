@@ -49,13 +49,16 @@ def to_device(w: Workload, device="cuda") -> DeviceProblem:
     return DeviceProblem(w, q, k, v, mask, cu_q, cu_k, g, o, lse)
 
 
-def build_plan(dp: DeviceProblem, stream=None, allocator=None, backward: bool = False) -> Plan:
+def build_plan(dp: DeviceProblem, stream=None, allocator=None, backward: bool = False,
+               quadrant_payload: bool = False) -> Plan:
+    """The workload's plan; quadrant_payload asks block plans for quadrant bits only."""
     w = dp.w
     if w.mask_kind == "intervals":
         return fa_plan_build_intervals(dp.geom, dp.mask, w.mask_func.shape[0], w.mask_func.shape[1],
                                        stream=stream, allocator=allocator, backward=backward)
     return fa_plan_build_blocks(dp.geom, dp.mask, w.block_mask.shape[0], w.block_q, w.block_kv,
-                                stream=stream, allocator=allocator, backward=backward)
+                                stream=stream, allocator=allocator, backward=backward,
+                                quadrant_payload=quadrant_payload)
 
 
 def forward(dp: DeviceProblem, plan: Plan, stream=None, choice: int = 0):

@@ -144,6 +144,22 @@ int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func,
  * return FA_ERR_INVALID_ARG.
  */
 #define FA_PLAN_BACKWARD 1u
+/*
+ * FA_PLAN_QUADRANT_PAYLOAD (block plans only): when block_q, block_kv,
+ * seqlen_q and seqlen_k are all multiples of 64, every 64x64 quadrant of a
+ * 128x128 tile is wholly visible or wholly masked, so the per-entry
+ * quadrant bits describe the partial tiles exactly.  The plan then keeps
+ * only those bits (a block-granular payload: "Decoupling Logical Masks from
+ * GPU Execution for Dynamic Block-Sparse Attention", launch preparation
+ * derives only the metadata the selected plan needs) and not the 2 KB of
+ * predicate words per partial entry; the planner neither writes nor
+ * allocates them.  Such a plan runs the Direct 64x64 forward only: fa_fwd
+ * with score mods or FA_FWD_COARSENED returns FA_ERR_UNSUPPORTED, and
+ * fa_plan_info_get reports payload_bytes = 0.  For plans that are not
+ * quadrant-exact, and together with FA_PLAN_BACKWARD (whose key-major view
+ * is built from the words), the flag has no effect.
+ */
+#define FA_PLAN_QUADRANT_PAYLOAD 2u
 int fa_plan_build_intervals_ex(const fa_geometry* geom, const int32_t* mask_func, int32_t Hmask,
                                int32_t nfunc, uint32_t flags, const fa_allocator* allocator, void* stream,
                                fa_plan** out);

@@ -302,3 +302,21 @@ def test_plan_choices_agree_with_the_oracle(name, choice):
         assert fa.fa_device_error_flags() == 0
         PT.check_rows(w, dp.o, dp.lse, rows)
     plan.free()
+
+
+def test_quadrant_payload_plan_forward():
+    # a plan with quadrant bits only (64-aligned blocks, 64-multiple lengths)
+    # runs the Direct 64x64 forward; the Coarsened choice and mods are refused
+    w = _block_problem(63, B=2, S=640, H=2, Hk=1, blk_q=64, blk_kv=192, density=0.3, Sk=576)
+    dp = runner.to_device(w)
+    plan = runner.build_plan(dp, quadrant_payload=True)
+    assert fa.fa_plan_info_get(plan)["payload_bytes"] == 0
+    runner.forward(dp, plan)
+    torch.cuda.synchronize()
+    assert fa.fa_device_error_flags() == 0
+    PT.check_rows(w, dp.o, dp.lse, all_rows(w))
+    with pytest.raises(fa.FaError):
+        runner.forward(dp, plan, choice=fa.FA_FWD_COARSENED)
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd(plan, dp.q, dp.k, dp.v, dp.o, dp.lse, dp.geom, w.scale, softcap=30.0)
+    plan.free()

@@ -173,3 +173,47 @@ def test_plan_parity_schedule_counts_in_global_memory():
     dp, plan = PT.gpu_plan(w)
     PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w))
     plan.free()
+
+
+def _quads_to_payload(quads: np.ndarray) -> np.ndarray:
+    """Predicate words [P][128][4] of entries whose quadrants are each wholly
+    visible or wholly masked, from their 'all visible' quadrant bits."""
+    out = np.zeros((len(quads), 128, 4), np.uint32)
+    for a in range(2):
+        for s in range(2):
+            on = ((quads >> (4 + 2 * a + s)) & 1).astype(bool)
+            out[on, 64 * a:64 * (a + 1), 2 * s:2 * s + 2] = 0xFFFFFFFF
+    return out
+
+
+@pytest.mark.parametrize("seed", [0])
+def test_quadrant_payload_plan_video_block_sparse(seed):
+    # 64x64 logical blocks over S = 32768: every quadrant is all or nothing,
+    # so the plan keeps the quadrant bits and no predicate words
+    w = W.make("video_block_sparse", seed)
+    dp = runner.to_device(w)
+    plan = runner.build_plan(dp, quadrant_payload=True)
+    info = fa.fa_plan_info_get(plan, count_visible=True)
+    assert info["payload_bytes"] == 0
+    gpu = fa.fa_plan_export(plan)
+    ref = OP.build_plan_by_heads(w.mask_only(), processes=16)
+    assert gpu["payload"].size == 0
+    gpu["payload"] = _quads_to_payload(gpu["quads"])  # the words the quadrant bits stand for
+    PT.compare_plan(gpu, ref)
+    assert info["visible_pairs"] == ref.visible_pairs
+    plan.free()
+
+
+def test_quadrant_payload_flag_without_exact_quadrants_builds_words():
+    # 64-aligned blocks but a length that is not a multiple of 64: the flag has no effect
+    gen = torch.Generator().manual_seed(3)
+    S = 700
+    z = torch.zeros(1, S, 2, 64, dtype=torch.bfloat16)
+    bm = W.random_block_mask(3, 2, -(-S // 64), -(-S // 64), 0.3)
+    w = W.Workload("blk", W.LAYOUT_BSHD, 1, S, S, 2, 2, 64, z, z, z, 1.0, "blocks", block_mask=bm,
+                   block_q=64, block_kv=64)
+    dp = runner.to_device(w)
+    plan = runner.build_plan(dp, quadrant_payload=True)
+    assert fa.fa_plan_info_get(plan)["payload_bytes"] > 0
+    PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w.mask_only()))
+    plan.free()
