@@ -73,7 +73,8 @@ constexpr float kNoMax = -1.0e30f;    // reference max of a column before its fi
 
 constexpr int D = 128;
 constexpr int kHalf = 64;                       // Q rows per sub-task, keys per position
-constexpr int kCols = 32;                       // query columns per softmax warpgroup
+constexpr int kGroups = 2;                      // softmax warpgroups (each 128 threads, one key per thread)
+constexpr int kCols = kHalf / kGroups;          // query columns per softmax warpgroup
 constexpr int kHalfBytes = kHalf * D * 2;       // 16 KB
 constexpr int kSlotBytes = 2 * kHalfBytes;      // ring slot: two positions
 constexpr int kKSlots = 3, kVSlots = 2;
@@ -98,18 +99,20 @@ constexpr int kSmAbort = kSmTmem + 4;
 constexpr int kSmClc = (kSmAbort + 4 + 15) & ~15;        // 2 x 16-byte responses
 constexpr int kSmSub = kSmClc + 32;                      // kSubRing records
 constexpr int kSmBcast = kSmSub + kSubRing * 32;         // one record copy per softmax warpgroup
-constexpr int kSmDesc = kSmBcast + 2 * 32;               // kDescRing step descriptors
+constexpr int kSmDesc = kSmBcast + kGroups * 32;         // kDescRing step descriptors
 constexpr int kSmM = kSmDesc + kDescRing * 32;           // [64] floats: reference max of each query column
 constexpr int kSmM2 = kSmM + 64 * 4;                     // [64] floats: new reference max, then 1/l
-constexpr int kSmXch = kSmM2 + 64 * 4;                   // [2 warpgroups][4 warps][32] floats
-constexpr int kSmallBytes = kSmXch + 2 * 4 * kCols * 4;
+constexpr int kSmXch = kSmM2 + 64 * 4;                   // [warpgroups][4 warps][kCols] floats
+constexpr int kSmallBytes = kSmXch + kGroups * 4 * kCols * 4;
 constexpr int kNeed = kOffSmall + kSmallBytes;
 // dynamic shared memory starts 1 KB-aligned in practice; what is left up to
 // the per-block limit is slack for a misaligned start (checked at run time)
 constexpr int kSmem = (kNeed + 1024 <= 232448) ? kNeed + 1024 : 232448;
 static_assert(kNeed <= 232448, "shared memory budget");
 
-constexpr int kWarpProducer = 8, kWarpS = 9, kWarpPV = 10, kThreads = 352;
+constexpr int kWarpProducer = 4 * kGroups, kWarpS = kWarpProducer + 1, kWarpPV = kWarpProducer + 2;
+constexpr int kThreads = 32 * (kWarpPV + 1);
+constexpr int kSoftmaxThreads = 128 * kGroups;
 
 struct KtParams {
   const int32_t* work;
@@ -171,13 +174,12 @@ __device__ __forceinline__ bool group_any(uint32_t id, bool v) {
   return r != 0;
 }
 
-// Warp reduce-scatter of 32 per-lane values: afterwards lane l holds, in
-// v[0], the reduction over the warp of column l.
+// Warp reduce-scatter of kCols per-lane values: afterwards lane l holds, in
+// v[0], the reduction over the warp of column l % kCols.
 template <bool MAX>
 __device__ __forceinline__ void warp_reduce_scatter32(float (&v)[kCols], int lane) {
 #pragma unroll
-  for (int r = 0; r < 5; ++r) {
-    const int half = 16 >> r;
+  for (int half = kCols / 2; half >= 1; half >>= 1) {
     const bool upper = (lane & half) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
@@ -187,13 +189,31 @@ __device__ __forceinline__ void warp_reduce_scatter32(float (&v)[kCols], int lan
       v[i] = MAX ? fmaxf(keep, got) : keep + got;
     }
   }
+#pragma unroll
+  for (int o = kCols; o < 32; o <<= 1) {  // fewer columns than lanes: fold the lane groups
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], o);
+    v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+  }
+}
+
+// kCols fp32 columns of this thread's TMEM lane, and their store.
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&x)[kCols]) {
+  if constexpr (kCols == 32) {
+    tmem_ld32f(taddr, *reinterpret_cast<float(*)[32]>(&x[0]));
+  } else {
+    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+  }
+}
+__device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[kCols]) {
+#pragma unroll
+  for (int c = 0; c < kCols; c += 16) tmem_st16(taddr + c, *reinterpret_cast<const uint32_t(*)[16]>(&x[c]));
 }
 
 // 32 scores of this thread's TMEM lane in log2 units, -inf where the
 // predicate bits pm are 0 (bit c: column c).
 __device__ __forceinline__ void load_scores(uint32_t taddr, float (&x)[kCols], uint32_t pm, uint64_t sc2,
                                             float scale_log2) {
-  tmem_ld32f(taddr, x);
+  ld_cols(taddr, x);
   if (pm == ~0u) {
 #pragma unroll
     for (int c = 0; c < kCols; c += 2) f2_unpack(f2_mul(f2_pack(x[c], x[c + 1]), sc2), x[c], x[c + 1]);
@@ -240,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_qfull + 8 * i, 1);
-      mbar_init(b_qempty + 8 * i, 2);  // thread 0 of each softmax warpgroup
-      mbar_init(b_ofree + 8 * i, 256);
+      mbar_init(b_qempty + 8 * i, kGroups);  // thread 0 of each softmax warpgroup
+      mbar_init(b_ofree + 8 * i, kSoftmaxThreads);
     }
     for (int s = 0; s < kKSlots; ++s) {
       mbar_init(b_kfull + 8 * s, 1);
@@ -253,19 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSBuf; ++i) {
       mbar_init(b_sfull + 8 * i, 1);
-      mbar_init(b_sfree + 8 * i, 256);
+      mbar_init(b_sfree + 8 * i, kSoftmaxThreads);
     }
     for (int i = 0; i < kPBuf; ++i) {
-      mbar_init(b_pfull + 8 * i, 256);
+      mbar_init(b_pfull + 8 * i, kSoftmaxThreads);
       mbar_init(b_pvdone + 8 * i, 1);
     }
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(b_dfull + 8 * i, 1);
-      mbar_init(b_dempty + 8 * i, 3);  // thread 0 of each softmax warpgroup and the V loader
+      mbar_init(b_dempty + 8 * i, kGroups + 1);  // thread 0 of each softmax warpgroup and the V loader
     }
     for (int i = 0; i < kSubRing; ++i) {
       mbar_init(b_tfull + 8 * i, 1);
-      mbar_init(b_tempty + 8 * i, 4);  // S issuer, P V issuer, thread 0 of each softmax warpgroup
+      mbar_init(b_tempty + 8 * i, kGroups + 2);  // S issuer, P V issuer, thread 0 of each softmax warpgroup
     }
     mbar_init(b_clc, 1);
     mbar_init(b_drain, 1);
@@ -547,13 +567,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int wg = warp >> 2;         // query columns 32 wg .. 32 wg + 31
+    const int wg = warp >> 2;         // query columns kCols wg .. kCols wg + kCols - 1
     const int t = threadIdx.x & 127;  // key t of a step; head-dimension column t in the epilogue
     const int cb = kCols * wg;
     const uint32_t bar_id = 1 + wg;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-    float* xch = reinterpret_cast<float*>(small + kSmXch) + wg * 4 * kCols;  // [4 warps][32]
+    float* xch = reinterpret_cast<float*>(small + kSmXch) + wg * 4 * kCols;  // [4 warps][kCols]
     Sub* bcast = reinterpret_cast<Sub*>(small + kSmBcast) + wg;
     const int pos = t >> 6;
     int g = 0, si = 0;
@@ -634,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (need) {
           // exact column max over the 128 keys (x is reloaded afterwards)
           warp_reduce_scatter32<true>(x, lane);
-          xch[(warp & 3) * kCols + lane] = x[0];
+          if (lane < kCols) xch[(warp & 3) * kCols + lane] = x[0];
           group_sync();
           if (t < kCols) {
             const float cm = fmaxf(fmaxf(xch[t], xch[kCols + t]), fmaxf(xch[2 * kCols + t], xch[3 * kCols + t]));
@@ -656,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // thread's O^T row (head dimension t)
             mbar_wait(b_pvdone + 8 * ((g - 1) % kPBuf), ((g - 1) / kPBuf) & 1, abort_flag, p.err, kWaitTimeoutNs);
             tc_fence_after();
-            tmem_ld32f(lane_addr + kColO + kHalf * ob + cb, x);
+            ld_cols(lane_addr + kColO + kHalf * ob + cb, x);
 #pragma unroll
             for (int c = 0; c < kCols; c += 2) {
               const float2 mo = *reinterpret_cast<const float2*>(mref + cb + c);
@@ -664,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               x[c] *= ex2_approx(mo.x - mn.x);
               x[c + 1] *= ex2_approx(mo.y - mn.y);
             }
-            tmem_st32(lane_addr + kColO + kHalf * ob + cb, reinterpret_cast<const uint32_t(&)[32]>(x[0]));
+            st_cols(lane_addr + kColO + kHalf * ob + cb, x);
             tmem_st_wait();
           }
           group_sync();  // every thread has read the old maxima
@@ -690,8 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t prow = sP + pb * kHalfBytes + t * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(prow + (((4 * wg + u) ^ (t & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        for (int u = 0; u < kCols / 8; ++u)
+          st_shared_v4(prow + ((((kCols / 8) * wg + u) ^ (t & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                       pk[4 * u + 3]);
         fence_proxy_async_smem();
         mbar_arrive(b_pfull + 8 * pb);
       }
@@ -704,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kCols; c += 2) f2_unpack(l2[c / 2], v[c], v[c + 1]);
         warp_reduce_scatter32<false>(v, lane);
-        xch[(warp & 3) * kCols + lane] = v[0];
+        if (lane < kCols) xch[(warp & 3) * kCols + lane] = v[0];
         group_sync();
         if (t < kCols) {
           const float l = (xch[t] + xch[kCols + t]) + (xch[2 * kCols + t] + xch[3 * kCols + t]);
@@ -717,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         group_sync();
       }
       float o[kCols];
-      tmem_ld32f(lane_addr + kColO + kHalf * ob + cb, o);
+      ld_cols(lane_addr + kColO + kHalf * ob + cb, o);
       tc_fence_before();
       mbar_arrive(b_ofree + 8 * ob);
 #pragma unroll
@@ -729,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         o[c + 3] *= il.w;
       }
       if (s.qv == kHalf) {
-        // stage this group's 32 output rows (row cb + c, column t) in the
+        // stage this group's kCols output rows (row cb + c, column t) in the
         // half's Q buffer (no MMA reads it any more: the last P V has
         // completed) and store them with TMA
         const uint32_t stage = sQ + qb * kHalfBytes + (t >> 6) * 8192;
