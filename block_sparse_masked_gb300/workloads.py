@@ -252,6 +252,8 @@ class DecodeWorkload:
     mask_func: np.ndarray           # int32 [1, nfunc, B*q_len]
     scale: float
     mask_name: str = "causal"
+    softcap: float = 0.0            # 0 disables the tanh softcap
+    alibi_slopes: Optional[np.ndarray] = None  # float32 [Hq] or None; bias slope * (k - q_abs)
 
     @property
     def offsets(self) -> np.ndarray:

@@ -4,7 +4,9 @@ Decoding ("FlexAttention: A Programming Model for Generating Optimized
 Attention Kernels", summary page, §3.4 Modification Conversion for
 Inference): the query rows are the newest tokens of each sequence, at
 absolute position offset + q_idx, and the mask and score_mod are evaluated
-there (mask(b, h, q_idx + offset, kv_idx)).  Here offset = k_len - q_len:
+there (mask(b, h, q_idx + offset, kv_idx); an ALiBi score_mod adds
+slope_h * (kv_idx - (q_idx + offset)); the tanh softcap does not depend on
+positions).  Here offset = k_len - q_len:
 the new tokens' keys are already in the cache.  The interval endpoints of
 a decode row are given at its absolute position (``DecodeWorkload.mask_func``),
 so the visible keys are [0, F0) U [F1, F2) U ... over the logical keys
@@ -43,8 +45,10 @@ def _rows(w, b: int, h: int, k: np.ndarray, v: np.ndarray):
     rows = np.arange(b * w.q_len, (b + 1) * w.q_len)
     q = A.as_f64(w.q[torch.from_numpy(rows), h])
     vis = M.interval_visible(w.mask_func[hm][:, rows], k_len)
-    q_abs = (k_len - w.q_len) + np.arange(w.q_len)  # absolute positions (used by position-dependent mods)
-    return A.attention_dense(q, k[:, hk], v[:, hk], vis, q_abs, w.scale)
+    # absolute positions: the score_mod converted for inference sees q_idx + offset
+    q_abs = (k_len - w.q_len) + np.arange(w.q_len)
+    slope = None if w.alibi_slopes is None else float(w.alibi_slopes[h])
+    return A.attention_dense(q, k[:, hk], v[:, hk], vis, q_abs, w.scale, softcap=w.softcap, slope=slope)
 
 
 def decode_rows(w, b: int, h: int):

@@ -102,11 +102,14 @@ def test_page_permutation_changes_nothing():
     assert np.array_equal(oa, ob) and np.array_equal(la, lb)
 
 
-@pytest.mark.parametrize("mask", ["causal", "sliding"])
-def test_decode_row_equals_training_row_at_offset(mask):
+@pytest.mark.parametrize("mask,mods", [("causal", False), ("sliding", False), ("causal", True),
+                                       ("sliding", True)])
+def test_decode_row_equals_training_row_at_offset(mask, mods):
     window, sink = 50, 4
     w, logical = _contiguous(4, B=2, Hq=2, Hk=2, d=16, k_lens=[180, 77], page_size=16, mask=mask,
                              window=window, sink=sink)
+    if mods:  # the score_mod converted for inference: ALiBi at the absolute position, softcap
+        w.softcap, w.alibi_slopes = 3.0, W.alibi_slopes(w.Hq)
     for b in range(w.B):
         n = int(w.k_lens[b])
         kb, vb = logical[b]
@@ -118,7 +121,8 @@ def test_decode_row_equals_training_row_at_offset(mask):
         else:
             mf = W.sliding_sink_rows(np.arange(n), window, sink)
         tw = W.Workload("train", W.LAYOUT_BSHD, 1, n, n, w.Hq, w.Hk, w.d, q, kb[None], vb[None], w.scale,
-                        "intervals", mask_func=mf.astype(np.int32)[None])
+                        "intervals", mask_func=mf.astype(np.int32)[None], softcap=w.softcap,
+                        alibi_slopes=w.alibi_slopes)
         for h in range(w.Hq):
             o_dec, l_dec = D.decode_rows(w, b, h)
             o_tr, l_tr = A.attention_rows(tw, 0, h, np.array([n - 1]))
@@ -171,4 +175,21 @@ def test_per_head_masks_follow_their_own_rows():
             vis = ((j > n - 1 - windows[h]) & (j <= n - 1))[None, :]
             o, _ = D.decode_rows(w, b, h)
             ref = _sdpa(A.as_f64(w.q[b:b + 1, h]), kb[:, h], vb[:, h], w.scale, vis)
+            np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+def test_alibi_decode_equals_sdpa_with_additive_bias():
+    # identity paging, causal, ALiBi only: SDPA with the bias slope * (k - pos)
+    w, logical = _contiguous(9, B=2, Hq=4, Hk=2, d=16, k_lens=[150, 33], page_size=16)
+    w.alibi_slopes = W.alibi_slopes(w.Hq)
+    for b in range(w.B):
+        n = int(w.k_lens[b])
+        kb, vb = (A.as_f64(t) for t in logical[b])
+        for h in range(w.Hq):
+            bias = (float(w.alibi_slopes[h]) * (np.arange(n) - (n - 1)))[None, :]
+            q = A.as_f64(w.q[b:b + 1, h])
+            qt, kt, vt = (torch.from_numpy(x)[None, None] for x in (q, kb[:, h // 2], vb[:, h // 2]))
+            ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(bias)[None, None],
+                                                 scale=w.scale)[0, 0].numpy()
+            o, _ = D.decode_rows(w, b, h)
             np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
