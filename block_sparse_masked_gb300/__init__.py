@@ -297,14 +297,17 @@ def fa_fwd(plan: Plan, q, k, v, o, lse, geom: FaGeometry, scale: float, softcap:
 
 
 def fa_decode_paged(plan: Plan, q, k_cache, v_cache, page_table, page_size: int, o, lse,
-                    geom: FaGeometry, scale: float, stream=None):
+                    geom: FaGeometry, scale: float, softcap: float = 0.0, alibi_slopes=None, stream=None):
     """Decoding over a paged KV cache (see fa.h): q [batch, heads_q, d],
     k_cache / v_cache [num_pages, page_size, heads_k, d], page_table
-    [batch, pages_per_seq] int32, all on the device."""
+    [batch, pages_per_seq] int32, all on the device; score mods as fa_fwd,
+    at the queries' absolute positions."""
+    mods, keep = _mods(softcap, alibi_slopes)
     _check(lib().fa_decode_paged(plan.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
                                  int(page_table.shape[1]), int(page_size), int(k_cache.shape[0]),
-                                 _ptr(o), _ptr(lse), _c.byref(geom), float(scale), None,
-                                 _stream_handle(stream)))
+                                 _ptr(o), _ptr(lse), _c.byref(geom), float(scale),
+                                 _c.byref(mods) if mods else None, _stream_handle(stream)))
+    del keep
 
 
 def _mods(softcap, alibi_slopes):

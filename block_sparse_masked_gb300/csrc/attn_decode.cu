@@ -85,7 +85,18 @@ struct DecParams {
   int B, Hq, Hk, Hmask, rows, G, gy, chunks, chunk_rows, oob_row, R;
   long long nP, nF;
   float scale_log2;
+  // score mods (FA_MOD_SOFTCAP, FA_MOD_ALIBI) at the query's absolute position
+  int flags;
+  float y_scale, cap_log2;      // softcap: log2(e) * cap * tanh(y_scale * s)
+  float slopes_l2[kMaxHeads];   // ALiBi slope * log2(e) per Q head
 };
+
+// tanh(y) = 1 - 2 / (exp(2y) + 1); absolute error ~1e-7, which the softcap
+// scales by the cap
+__device__ __forceinline__ float tanh_exp2(float y) {
+  const float e = ex2_approx(2.0f * kLog2e * y);
+  return 1.0f - __fdividef(2.0f, e + 1.0f);
+}
 
 template <int N>
 struct DecLayout {
@@ -471,8 +482,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_sfree + 8 * sb);
+        if (p.flags) {
+          // softcap(scale * s), then ALiBi slope * (k - q) with the query at k_len - 1
+          const float dk = static_cast<float>(kpos - (x.k_len - 1));
 #pragma unroll
-        for (int c = 0; c < N; ++c) s[c] = (vis && c < p.G) ? s[c] * p.scale_log2 : -INFINITY;
+          for (int c = 0; c < N; ++c) {
+            float z = (p.flags & FA_MOD_SOFTCAP) ? p.cap_log2 * tanh_exp2(s[c] * p.y_scale) : s[c] * p.scale_log2;
+            if ((p.flags & FA_MOD_ALIBI) && c < p.G) z += p.slopes_l2[x.hk * p.G + c] * dk;
+            s[c] = (vis && c < p.G) ? z : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < N; ++c) s[c] = (vis && c < p.G) ? s[c] * p.scale_log2 : -INFINITY;
+        }
         const float tmax = group_reduce<N, true>(s, red, warp, lane);
         // reference max per column: raised when a score exceeds it by more than 2^8
         bool need = false;
@@ -896,6 +918,11 @@ cudaError_t launch_decode(const DecodeLaunch& a, const DecodeSizes& s, void* ws,
   p.nF = pl->F;
   p.R = pl->Hmask * g.batch;
   p.scale_log2 = a.scale * kLog2e;
+  p.flags = a.flags;
+  p.y_scale = (a.flags & FA_MOD_SOFTCAP) ? a.scale / a.softcap : 0.0f;
+  p.cap_log2 = a.softcap * kLog2e;
+  if (a.flags & FA_MOD_ALIBI)
+    for (int h = 0; h < g.heads_q; ++h) p.slopes_l2[h] = a.slopes[h] * kLog2e;
   const int grid = s.C;
   if (N == 16)
     e = launch_decode_n<16>(mq, mk, mv, p, grid, st);

@@ -664,8 +664,16 @@ int fa_decode_paged(const fa_plan* plan, const void* q, const void* k_cache, con
   if (!(plan->Hmask == 1 || (plan->Hmask == g.heads_q && G == 1)))
     return fail(FA_ERR_UNSUPPORTED, "decoding takes one mask for every head, or per-head masks without GQA");
   if (G > 64) return fail(FA_ERR_UNSUPPORTED, "decoding supports at most 64 query heads per K/V head");
-  if (mods && (mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI)))
-    return fail(FA_ERR_UNSUPPORTED, "decoding takes no score mods");
+  int mod_flags = 0;
+  if (mods) {
+    mod_flags = mods->flags & (FA_MOD_SOFTCAP | FA_MOD_ALIBI);
+    if ((mod_flags & FA_MOD_SOFTCAP) && !(mods->softcap > 0.0f))
+      return fail(FA_ERR_INVALID_ARG, "softcap must be > 0 when FA_MOD_SOFTCAP is set");
+    if ((mod_flags & FA_MOD_ALIBI) && !mods->alibi_slopes)
+      return fail(FA_ERR_INVALID_ARG, "FA_MOD_ALIBI needs alibi_slopes");
+    if ((mod_flags & FA_MOD_ALIBI) && g.heads_q > bsm::kMaxHeads)
+      return fail(FA_ERR_UNSUPPORTED, "ALiBi supports at most %d query heads", bsm::kMaxHeads);
+  }
   if (page_size < 16 || (page_size & (page_size - 1)) != 0)
     return fail(FA_ERR_INVALID_ARG, "page_size must be a power of two >= 16");
   if (pages_per_seq < 1 || num_pages < 1 || num_pages * static_cast<int64_t>(page_size) + 128 > INT32_MAX)
@@ -695,6 +703,9 @@ int fa_decode_paged(const fa_plan* plan, const void* q, const void* k_cache, con
   a.lse = lse;
   a.scale = scale;
   a.num_sms = sms;
+  a.flags = mod_flags;
+  a.softcap = mods ? mods->softcap : 0.0f;
+  a.slopes = mods ? mods->alibi_slopes : nullptr;
   bsm::DecodeSizes z{};
   const size_t bytes = bsm::decode_workspace_bytes(a, &z);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

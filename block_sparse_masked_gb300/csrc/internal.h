@@ -226,6 +226,9 @@ struct DecodeLaunch {
   float* lse;
   float scale;
   int num_sms;
+  int flags;             // FA_MOD_SOFTCAP | FA_MOD_ALIBI
+  float softcap;
+  const float* slopes;   // host, heads_q
 };
 struct DecodeSizes {
   int G, gy, chunks, chunk_rows, C;  // C: CTAs of the decode kernel

@@ -119,5 +119,5 @@ def decode_plan(dp: DecodeProblem, stream=None, allocator=None) -> Plan:
 def decode(dp: DecodeProblem, plan: Plan, stream=None):
     w = dp.w
     fa_decode_paged(plan, dp.q, dp.k_cache, dp.v_cache, dp.page_table, w.page_size, dp.o, dp.lse, dp.geom,
-                    w.scale, stream=stream)
+                    w.scale, softcap=w.softcap, alibi_slopes=w.alibi_slopes, stream=stream)
     return dp.o, dp.lse

@@ -274,8 +274,10 @@ int fa_bwd(const fa_plan* plan, const void* q, const void* k, const void* v, con
  * A page number outside [0, num_pages) for a key that is needed sets bit 3
  * of the device error flags (fa_device_error_flags) and reads zeros.
  * One mask for every head (Hmask = 1, any GQA group up to 64 query heads
- * per K/V head), or per-head masks without GQA; no score mods
- * (FA_ERR_UNSUPPORTED otherwise).  A workspace (index conversion, row
+ * per K/V head), or per-head masks without GQA (FA_ERR_UNSUPPORTED
+ * otherwise).  mods (may be NULL) as for fa_fwd, converted for inference:
+ * the ALiBi bias is alibi_slopes[h] * (k - (k_len - 1)), the query's
+ * absolute position.  A workspace (index conversion, row
  * prefix, per-piece O, max and sum) comes from the plan's allocator or the
  * library's pool and is returned in stream order.  Asynchronous on
  * `stream`: three kernel launches.  Pointers must be 16-byte aligned.

@@ -150,3 +150,23 @@ def test_rejects_unsupported_inputs():
     with pytest.raises(fa.FaError):
         fa.fa_decode_paged(plan, dp.q, dp.k_cache, dp.v_cache, dp.page_table, 48, dp.o, dp.lse, dp.geom, w.scale)
     plan.free()
+
+
+@pytest.mark.parametrize("softcap,alibi", [(30.0, False), (0.0, True), (20.0, True)])
+def test_score_mods_at_the_absolute_position(softcap, alibi):
+    w = W.decode_paged(21, B=6, Hq=16, Hk=4, kmin=1, kmax=3000, page_size=64, mask="sliding", window=1000,
+                       sink=4)
+    w.softcap = softcap
+    if alibi:
+        w.alibi_slopes = W.alibi_slopes(w.Hq)
+    dp, flags = run(w)
+    assert flags == 0
+    check(w, dp)
+
+
+def test_score_mods_on_the_decode_workload():
+    w = W.decode_paged(1, B=8)
+    w.softcap, w.alibi_slopes = 50.0, W.alibi_slopes(w.Hq)
+    dp, flags = run(w)
+    assert flags == 0
+    check(w, dp, heads=[0, 13, 31])
