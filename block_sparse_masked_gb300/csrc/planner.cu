@@ -770,6 +770,9 @@ struct K2QParams {
   int32_t* dq_order;
   int32_t* dq_order_full;
   uint32_t* kpayload;        // [P'*128*4]: key c, word w, bit l = (query 32w+l, key c) visible
+  // quadrant-exact block plans (64-aligned blocks, 64-multiple lengths): the
+  // Q2K quadrant bits, from which the key-major words follow directly
+  const uint8_t* quads;
   int rows, k_rows;
   // bounds of the checked build: Q2K partial entries, K2Q partial and full
   // entries, and the device error word
@@ -844,6 +847,21 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
     const long long eq = bsm_idx(__ldg(p.p_off + static_cast<long long>(hm) * p.rows + row_begin + i) +
                                      popc_partial_below(wv, wf, j),
                                  p.nP, p.err);
+    uint4* dst = reinterpret_cast<uint4*>(p.kpayload + e * (kTile * kPayloadWords));
+    if (p.quads) {
+      // each 64x64 quadrant is wholly visible or wholly masked: key 32 kc +
+      // lane (key half kc / 2) sees query word w (query half w / 2) in full
+      // exactly when the quadrant's "all visible" bit is set
+      const uint32_t q = __ldg(p.quads + eq);
+#pragma unroll
+      for (int kc = 0; kc < kPayloadWords; ++kc) {
+        uint32_t w4[kPayloadWords];
+#pragma unroll
+        for (int w = 0; w < kPayloadWords; ++w) w4[w] = ((q >> (4 + 2 * (w >> 1) + (kc >> 1))) & 1u) ? kFull : 0u;
+        dst[32 * kc + lane] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      continue;
+    }
     const uint32_t* src = p.payload + eq * (kTile * kPayloadWords);
     uint32_t mine[kPayloadWords][kPayloadWords];  // [key chunk][query word] for key 32 chunk + lane
 #pragma unroll
@@ -859,7 +877,6 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
         }
         mine[kc][wq] = got;
       }
-    uint4* dst = reinterpret_cast<uint4*>(p.kpayload + e * (kTile * kPayloadWords));
 #pragma unroll
     for (int kc = 0; kc < kPayloadWords; ++kc)
       dst[32 * kc + lane] = make_uint4(mine[kc][0], mine[kc][1], mine[kc][2], mine[kc][3]);
@@ -1190,6 +1207,9 @@ cudaError_t launch_back_k2q(const Geometry& g, const PlanWorkspace& ws, fa_plan*
   p.kP = plan->kP;
   p.kF = plan->kF;
   p.err = checked_error_word();
+  const bool exact = plan->mask_kind == MASK_BLOCKS && plan->block_q % 64 == 0 && plan->block_kv % 64 == 0 &&
+                     plan->geom.seqlen_q % 64 == 0 && plan->geom.seqlen_k % 64 == 0;
+  p.quads = exact ? plan->quads : nullptr;
   const dim3 grid(plan->k_rows > 0 ? static_cast<unsigned>(plan->k_rows) : 1u, plan->Hmask);
   k_back_k2q<<<grid, 128, 0, st>>>(p);
   return cudaGetLastError();
