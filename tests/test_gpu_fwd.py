@@ -244,7 +244,7 @@ def _block_problem(seed, B, S, H, Hk, blk_q, blk_kv, density, diagonal=True, Sk=
                       block_mask=bm, block_q=blk_q, block_kv=blk_kv)
 
 
-@pytest.mark.parametrize("geom", [(128, 64), (64, 192), (128, 128)])
+@pytest.mark.parametrize("geom", [(128, 64), (64, 192), (128, 128), (256, 256), (128, 384)])
 def test_block_mask_64_multiple_geometries(geom):
     # logical blocks that are multiples of 64 run one 64-row half of a Q tile
     # against pairs of its live 64x64 quadrants; ragged tails on both axes

@@ -90,7 +90,7 @@ def test_plan_parity_wide(seed, shape):
     plan.free()
 
 
-@pytest.mark.parametrize("geom", [(64, 64), (48, 80), (128, 32), (200, 300), (16, 128)])
+@pytest.mark.parametrize("geom", [(64, 64), (48, 80), (128, 32), (200, 300), (16, 128), (256, 256), (128, 384)])
 @pytest.mark.parametrize("S", [700, 1024])
 def test_block_plan_parity_geometries(geom, S):
     BQ, BKV = geom

@@ -112,6 +112,36 @@ def test_block_plan_preserves_EM(T, geom):
         assert np.array_equal(rec, em)
 
 
+@pytest.mark.parametrize("geom", [(256, 256), (128, 384), (384, 128)])
+@pytest.mark.parametrize("S", [1024, 1000])
+def test_refined_geometry_has_no_partial_tile_away_from_tails(geom, S):
+    """Logical blocks that are whole multiples of the 128x128 tile (the
+    Refined mapping of "Decoupling Logical Masks from GPU Execution for
+    Dynamic Block-Sparse Attention", physical tiles inside logical blocks):
+    every tile lies inside one block, so it is empty or fully visible; only
+    a tile that the sequence end cuts can be partial, and the plan still
+    reproduces E(M)."""
+    import torch
+    BQ, BKV = geom
+    nbq, nbk = -(-S // BQ), -(-S // BKV)
+    bm = W.random_block_mask(17, 2, nbq, nbk, 0.4)
+    w = W.Workload("blk", W.LAYOUT_BSHD, 1, S, S, 2, 2, 8,
+                   torch.zeros(1, S, 2, 8), torch.zeros(1, S, 2, 8), torch.zeros(1, S, 2, 8),
+                   1.0, "blocks", block_mask=bm, block_q=BQ, block_kv=BKV)
+    p = P.build_plan(w)
+    last_q, last_k = (S - 1) // 128, (S - 1) // 128
+    tail = S % 128 != 0
+    for hm in range(2):
+        for r in range(p.rows):
+            f = hm * p.rows + r
+            for kt in p.partial_idx[p.partial_offset[f]:p.partial_offset[f + 1]].tolist():
+                assert tail and (r == last_q or kt == last_k), (hm, r, kt)
+        em = np.kron(bm[hm], np.ones((BQ, BKV), np.uint8))[:S, :S].astype(bool)
+        assert np.array_equal(P.visible_from_plan(p, hm, 0, S, S), em)
+    if not tail:
+        assert p.partial_idx.size == 0 and p.full_idx.size > 0
+
+
 def test_interval_plan_preserves_visibility_and_counts():
     w = _tiny_interval_workload(seed=9, B=0, S=0, nfunc=5, Hmask=2,
                                 varlen_lens=[300, 5, 128, 257])
