@@ -448,13 +448,23 @@ __device__ void front_finish(const FrontParams& p) {
   }
 }
 
-// One CTA per padded row: blockIdx.x = b * nq_max + lr (rows past a sample's
-// end, and x >= rows_ub, only arrive), blockIdx.y = mask head.  The last CTA
-// to arrive (atomic count after a device-wide fence) finishes the stage.
+// Padded rows per CTA of the front stage: one for interval masks; four for
+// block masks, whose rows are cheap (a few bytes of the block mask per K
+// tile), so that fewer CTAs pay the device-wide fence and the arrival.
+template <int KIND>
+constexpr int kFrontRows = (KIND == MASK_INTERVALS) ? 1 : 4;
+
+// kFrontRows padded rows per CTA: x = blockIdx.x * kFrontRows + i =
+// b * nq_max + lr (rows past a sample's end, and x >= rows_ub, only arrive),
+// blockIdx.y = mask head.  The last CTA to arrive (atomic count after a
+// device-wide fence) finishes the stage.
 template <int KIND>
 __global__ void __launch_bounds__(KIND == MASK_INTERVALS ? 128 : 256) k_front(FrontParams p) {
-  const int x = blockIdx.x, hm = blockIdx.y;
-  if (x < p.rows_ub) {
+  const int hm = blockIdx.y;
+#pragma unroll 1
+  for (int i = 0; i < kFrontRows<KIND>; ++i) {
+    const int x = blockIdx.x * kFrontRows<KIND> + i;
+    if (x >= p.rows_ub) break;
     const int b = x / p.nq_max, lr = x % p.nq_max;
     const SampleGeo sg = sample_geo(p, b);
     if (lr < cdiv(sg.q_len, kTile)) {
@@ -1090,11 +1100,14 @@ cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspa
   p.kp_off = ws.kp_off;
   p.kf_off = ws.kf_off;
   // at least one CTA, so that the last-CTA stage also runs without rows
-  const dim3 grid(ws.rows_ub > 0 ? ws.rows_ub : 1, m.Hmask);
-  if (m.kind == MASK_INTERVALS)
+  if (m.kind == MASK_INTERVALS) {
+    const dim3 grid(ws.rows_ub > 0 ? ws.rows_ub : 1, m.Hmask);
     k_front<MASK_INTERVALS><<<grid, 128, 0, st>>>(p);
-  else
+  } else {
+    constexpr int R = kFrontRows<MASK_BLOCKS>;
+    const dim3 grid(ws.rows_ub > 0 ? (ws.rows_ub + R - 1) / R : 1, m.Hmask);
     k_front<MASK_BLOCKS><<<grid, 256, 0, st>>>(p);
+  }
   return cudaGetLastError();
 }
 
