@@ -92,7 +92,7 @@ class FaPlanBwdHostView(_c.Structure):
 class FaPlanHostView(_c.Structure):
     _fields_ = [("cu_q_rows", _vp), ("sequence_desc", _vp), ("partial_offset", _vp),
                 ("partial_idx", _vp), ("full_offset", _vp), ("full_idx", _vp), ("payload", _vp),
-                ("work_desc", _vp), ("halves", _vp), ("quads", _vp)]
+                ("work_desc", _vp), ("halves", _vp), ("quads", _vp), ("lpt", _vp)]
 
 
 class FaError(RuntimeError):
@@ -380,6 +380,7 @@ def fa_plan_export(plan: Plan) -> dict:
         "work_desc": np.zeros((T, 4), np.int32),
         "halves": np.zeros(P, np.uint8),
         "quads": np.zeros(P, np.uint8),
+        "lpt": np.zeros(T, np.int32),
     }
     view = FaPlanHostView(*[a.ctypes.data if a.size else None for a in arrs.values()])
     _check(lib().fa_plan_export(plan.handle, _c.byref(view)))

@@ -17,7 +17,10 @@
 //
 // Tasks come from cluster launch control as in attn_fwd.cu (one CTA per
 // work_desc entry; a running CTA takes over entries of CTAs that have not
-// started).  352 threads, warp-specialised:
+// started), in the plan's consumer order: longest task first, so that the
+// last tasks to start are the shortest (with a few tasks per SM, the §4.8
+// order -- sections, then cost -- starts heavy tasks of the last sections
+// last and the launch ends on them).  352 threads, warp-specialised:
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: thread r owns
 //               score row r (TMEM lane r) and all 128 key columns, so the row
 //               max and sum stay in the thread.  Each group walks its own
@@ -90,6 +93,7 @@ struct PCfg {
 
 struct PairParams {
   const int32_t* work;
+  const int32_t* lpt;  // the order in which tasks are taken: work_desc positions, longest first
   const int32_t* seq;
   const int32_t* p_off;
   const int32_t* f_off;
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (;;) {
         const int t = tasks.next(abort_flag, p.err, kWaitTimeoutNs);
         if (t < 0 || t >= p.ntasks) break;
-        const PairTask k = load_pair(p, t);
+        const PairTask k = load_pair(p, __ldg(p.lpt + bsm_idx(t, p.ntasks, p.err)));
         if (k.skip) continue;
         publish(k);
         const int nA = k.t[0].np + k.t[0].nf, nB = k.t[1].np + k.t[1].nf;
@@ -637,6 +641,7 @@ cudaError_t launch_pair_impl(const FwdLaunch& a, cudaStream_t st, const char** w
   }
   PairParams p{};
   p.work = pl->work_desc;
+  p.lpt = pl->lpt;
   p.seq = pl->seq_desc;
   p.p_off = pl->p_off;
   p.f_off = pl->f_off;

@@ -266,7 +266,8 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
                o_pc = c1.take(4ull * nflat_ub), o_fc = c1.take(4ull * nflat_ub),
                o_po = c1.take(4ull * (nflat_ub + 1)), o_fo = c1.take(4ull * (nflat_ub + 1)),
                o_hist = c1.take(4ull * NS * (C + 1)), o_cursor = c1.take(4ull * NS * (C + 1)),
-               o_work = c1.take(16ull * rows_ub * g.heads_q);
+               o_work = c1.take(16ull * rows_ub * g.heads_q), o_lpt = c1.take(4ull * rows_ub * g.heads_q),
+               o_lbkt = c1.take(4ull * rows_ub * g.heads_q), o_lhist = c1.take(4ull * 32 * (C + 1));
   // backward K2Q view: padded K rows (mask head, sample, K tile)
   const bool bwd = (flags & FA_PLAN_BACKWARD) != 0;
   const long long kflat_ub = bwd ? static_cast<long long>(Hmask) * B * kt_ub : 0;
@@ -289,6 +290,9 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   ws.hist = reinterpret_cast<int32_t*>(w1 + o_hist);
   ws.cursors = reinterpret_cast<int32_t*>(w1 + o_cursor);
   ws.work = reinterpret_cast<int32_t*>(w1 + o_work);
+  ws.lpt = reinterpret_cast<int32_t*>(w1 + o_lpt);
+  ws.lbkt = reinterpret_cast<int32_t*>(w1 + o_lbkt);
+  ws.lhist = reinterpret_cast<int32_t*>(w1 + o_lhist);
   if (bwd) {
     ws.kp_cnt = reinterpret_cast<int32_t*>(w1 + o_kpc);
     ws.kf_cnt = reinterpret_cast<int32_t*>(w1 + o_kfc);
@@ -364,7 +368,8 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
                q_pay = c2.take(plan->quads_only ? 0 : 16ull * bsm::kTile * plan->P), q_work = c2.take(16ull * plan->tasks),
                q_cq = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
                q_ck = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
-               q_er = c2.take(4ull * plan->P), q_hv = c2.take(plan->P), q_qd = c2.take(plan->P);
+               q_er = c2.take(4ull * plan->P), q_hv = c2.take(plan->P), q_qd = c2.take(plan->P),
+               q_lpt = c2.take(4ull * plan->tasks);
   uint8_t* pm = static_cast<uint8_t*>(al.get(c2.off));
   if (!pm) {
     delete plan;
@@ -380,6 +385,7 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   plan->f_idx = reinterpret_cast<int32_t*>(pm + q_fi);
   plan->payload = plan->quads_only ? nullptr : reinterpret_cast<uint32_t*>(pm + q_pay);
   plan->work_desc = reinterpret_cast<int32_t*>(pm + q_work);
+  plan->lpt = reinterpret_cast<int32_t*>(pm + q_lpt);
   if (g.layout == FA_LAYOUT_THD) {
     plan->cu_seqlens_q = reinterpret_cast<int32_t*>(pm + q_cq);
     plan->cu_seqlens_k = reinterpret_cast<int32_t*>(pm + q_ck);
@@ -773,6 +779,7 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst) {
       {dst->work_desc, plan->work_desc, 16ull * plan->tasks},
       {dst->halves, plan->halves, static_cast<size_t>(plan->P)},
       {dst->quads, plan->quads, static_cast<size_t>(plan->P)},
+      {dst->lpt, plan->lpt, 4ull * plan->tasks},
   };
   for (auto& it : items) {
     if (!it.d || it.n == 0) continue;

@@ -89,6 +89,7 @@ struct fa_plan {
   int32_t* f_idx = nullptr;         // [F]
   uint32_t* payload = nullptr;      // [P*128*4]
   int32_t* work_desc = nullptr;     // [tasks*4]
+  int32_t* lpt = nullptr;           // [tasks] work_desc positions, cost descending (stable)
   int32_t* cu_seqlens_q = nullptr;  // clones (THD)
   int32_t* cu_seqlens_k = nullptr;
   int32_t* entry_row = nullptr;     // [P] planner scratch kept with the plan: flat row of each entry
@@ -132,6 +133,9 @@ struct PlanWorkspace {
   int32_t* hist;          // schedule counting buffers [num_sections*(max_cost+1)]
   int32_t* cursors;
   int32_t* work;          // schedule output [rows_ub*heads_q*4]
+  int32_t* lpt;           // consumer order: work_desc positions by cost [rows_ub*heads_q]
+  int32_t* lbkt;          // its scratch: cost bucket of every position [rows_ub*heads_q]
+  int32_t* lhist;         // and per-warp bucket counts [32*(max_cost+1)]
   int rows_ub, nq_max, kt_ub, words;
   // backward K2Q view; kp_cnt null when not built
   int32_t* kp_cnt = nullptr;  // [Hmask*B*kt_ub], zero before the front stage

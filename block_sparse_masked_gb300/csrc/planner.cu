@@ -491,9 +491,9 @@ __global__ void __launch_bounds__(KIND == MASK_INTERVALS ? 128 : 256) k_front(Fr
 // ------------------------------------------------------------ back
 struct BackParams {
   // exact-size copies from the workspace (and the caller's cu_seqlens)
-  const int32_t* src[7];
-  int32_t* dst[7];
-  long long count[7];
+  const int32_t* src[8];
+  int32_t* dst[8];
+  long long count[8];
   // workspace
   const uint32_t* vis_bits;
   const uint32_t* full_bits;
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
     const long long tid = (static_cast<long long>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
     const long long nthreads = static_cast<long long>(gridDim.x) * gridDim.y * blockDim.x;
 #pragma unroll
-    for (int a = 0; a < 7; ++a)
+    for (int a = 0; a < 8; ++a)
       for (long long i = tid; i < p.count[a]; i += nthreads) p.dst[a][i] = __ldg(p.src[a] + i);
   }
   const int row = blockIdx.x, hm = blockIdx.y;
@@ -904,6 +904,9 @@ struct SchedParams {
   int32_t* hist;     // [NS*(C+1)]
   int32_t* cursors;  // [NS*(C+1)]
   int32_t* work;     // [tasks*4]
+  int32_t* lpt;      // [tasks] consumer order (null: not built)
+  int32_t* lbkt;     // [tasks] scratch: bucket of every work_desc position
+  int32_t* lhist;    // [32*(C+1)] scratch: per-warp bucket counts, then starts
   int B, Hq, Hk, Hmask, C, NS;
   int in_smem;       // 1: histogram and cursors live in dynamic shared memory (2*NS*(C+1) ints)
   uint32_t* err;     // device error word (checked build)
@@ -1033,6 +1036,66 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
       __syncwarp();
     }
   }
+  // 4. the consumer order (lpt): every work_desc position by cost bucket
+  //    (cost descending, zero-cost tasks last), stable in work_desc order --
+  //    the longest-first order in which a consumer with few tasks per SM
+  //    takes them.  Per-warp bucket counts over contiguous chunks of
+  //    positions, a scan over (bucket, warp), then each warp scatters its
+  //    chunk in order.
+  if (p.lpt != nullptr) {
+    __syncthreads();  // every work_desc entry is written
+    const long long T = static_cast<long long>(p.Hq) * rows;
+    const int nw = blockDim.x >> 5, w = threadIdx.x >> 5;
+    const long long chunk = (T + nw - 1) / nw;
+    const long long c0 = min(T, static_cast<long long>(w) * chunk), c1 = min(T, c0 + chunk);
+    int32_t* wh = p.lhist + static_cast<long long>(w) * (C + 1);
+    for (int c = lane; c <= C; c += 32) wh[c] = 0;
+    __syncwarp();
+    for (long long i = c0 + lane; i < c1; i += 32) {
+      const int32_t* wd = p.work + 4 * i;
+      const int b = wd[2];
+      const int bucket = task_bucket(p, task_cost(p, rows, wd[1], p.seq[8 * b + 4] + wd[0]));
+      p.lbkt[i] = bucket;
+      atomicAdd(&wh[bucket], 1);
+    }
+    __syncthreads();
+    // start of (bucket c, warp w): the positions of buckets < c, then those
+    // of warps < w in bucket c
+    long long carry = 0;
+    for (int cb = 0; cb <= C; cb += blockDim.x) {
+      const int c = cb + threadIdx.x;
+      long long tot_c = 0;
+      if (c <= C)
+        for (int ww = 0; ww < nw; ++ww) tot_c += p.lhist[static_cast<long long>(ww) * (C + 1) + c];
+      long long all;
+      const long long base_c = carry + block_excl_scan(tot_c, &all);
+      if (c <= C) {
+        long long run = base_c;
+        for (int ww = 0; ww < nw; ++ww) {
+          int32_t* cell = p.lhist + static_cast<long long>(ww) * (C + 1) + c;
+          const int v = *cell;
+          *cell = static_cast<int32_t>(run);
+          run += v;
+        }
+      }
+      carry += all;
+    }
+    __syncthreads();
+    for (long long i0 = c0; i0 < c1; i0 += 32) {
+      const long long i = i0 + lane;
+      const bool act = i < c1;
+      const unsigned amask = __ballot_sync(kFull, act);
+      if (act) {
+        const int bucket = p.lbkt[i];
+        const unsigned same = __match_any_sync(amask, bucket);
+        const int rank = __popc(same & ((1u << lane) - 1));
+        p.lpt[bsm_idx(wh[bucket] + rank, T, p.err)] = static_cast<int32_t>(i);
+        __syncwarp(amask);
+        if (rank == 0) wh[bucket] += __popc(same);
+      }
+      __syncwarp();
+    }
+  }
 }
 
 // ------------------------------------------------------------ statistics
@@ -1114,7 +1177,7 @@ cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspa
 cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmask, int num_sections,
                             int max_cost, cudaStream_t st) {
   if (ws.rows_ub == 0) return cudaSuccess;
-  SchedParams p{ws.seq, ws.cu_rows, ws.p_off, ws.f_off, ws.hist, ws.cursors, ws.work,
+  SchedParams p{ws.seq, ws.cu_rows, ws.p_off, ws.f_off, ws.hist, ws.cursors, ws.work, ws.lpt, ws.lbkt, ws.lhist,
                 g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections, 0, checked_error_word()};
   // histogram and cursors in shared memory when they fit (shared-memory
   // atomics and the single CTA's scans then stay on chip)
@@ -1144,13 +1207,14 @@ cudaError_t launch_back(const Geometry& g, const MaskArgs& m, const PlanWorkspac
   const int rows = static_cast<int>(plan->rows);
   const long long nflat = static_cast<long long>(m.Hmask) * rows;
   BackParams p{};
-  const int32_t* src[7] = {ws.cu_rows, ws.seq, ws.p_off, ws.f_off, cu_q_src, cu_k_src, ws.work};
-  int32_t* dst[7] = {plan->cu_q_rows, plan->seq_desc, plan->p_off, plan->f_off, plan->cu_seqlens_q,
-                     plan->cu_seqlens_k, plan->work_desc};
-  const long long cnt[7] = {g.batch + 1LL, 8LL * g.batch, nflat + 1, nflat + 1,
+  const int32_t* src[8] = {ws.cu_rows, ws.seq, ws.p_off, ws.f_off, cu_q_src, cu_k_src, ws.work, ws.lpt};
+  int32_t* dst[8] = {plan->cu_q_rows, plan->seq_desc, plan->p_off, plan->f_off, plan->cu_seqlens_q,
+                     plan->cu_seqlens_k, plan->work_desc, plan->lpt};
+  const long long cnt[8] = {g.batch + 1LL, 8LL * g.batch, nflat + 1, nflat + 1,
                             (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0,
-                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0, 4LL * plan->tasks};
-  for (int a = 0; a < 7; ++a) {
+                            (g.layout == FA_LAYOUT_THD) ? g.batch + 1LL : 0, 4LL * plan->tasks,
+                            (ws.lpt != nullptr) ? plan->tasks : 0};
+  for (int a = 0; a < 8; ++a) {
     p.src[a] = src[a];
     p.dst[a] = dst[a];
     p.count[a] = cnt[a];

@@ -323,7 +323,12 @@ int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream,
  *   execution order, halves [P] (bit s: some element of key columns
  *   64s..64s+63 of the partial tile is visible), quads [P] (quadrant
  *   (a, s) = tile rows 64a..64a+63 x key columns 64s..64s+63: bit 2a+s set
- *   if one of its elements is visible, bit 4+2a+s if all are).  Synchronous.
+ *   if one of its elements is visible, bit 4+2a+s if all are), lpt [T] (the
+ *   positions of work_desc ordered by task cost -- partial + full entries of
+ *   the task's row -- descending, ties in work_desc order, zero-cost tasks
+ *   last: the longest-first order in which a consumer with few tasks per SM
+ *   takes the tasks; "Flex Attention Mask Plan Design" §4.8 leaves the
+ *   consumer's traversal of the task list open).  Synchronous.
  */
 typedef struct {
   int32_t* cu_q_rows;
@@ -336,6 +341,7 @@ typedef struct {
   int32_t* work_desc;
   uint8_t* halves;
   uint8_t* quads;
+  int32_t* lpt;
 } fa_plan_host_view;
 
 int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst);

@@ -30,6 +30,11 @@ Follows "Flex Attention Mask Plan Design":
   tasks are ordered by L2 section (the (sample, K/V head) pair whose K/V the
   task reads), then descending cost, then the tie order (head, m_block);
   zero-cost tasks follow in (batch, head, m_block) order.
+* Consumer order ``lpt[tasks]``: the positions of work_desc sorted by task
+  cost, descending, ties in work_desc order (a stable sort), so zero-cost
+  tasks stay last: the longest-first order in which a consumer with few
+  tasks per SM takes the tasks (§4.8 fixes the task list; the traversal is
+  the consumer's).
 
 The classification here is computed by expanding each Q tile into a dense
 boolean matrix and testing every element, which is independent of the GPU's
@@ -69,6 +74,7 @@ class Plan:
     sequence_desc: np.ndarray      # int64 [B, 8]
     work_desc: np.ndarray          # int64 [tasks, 4]
     visible_pairs: int             # |visible (q, k)| summed over mask heads and samples
+    lpt: np.ndarray                # int64 [tasks]: work_desc positions, cost descending (stable)             # |visible (q, k)| summed over mask heads and samples
 
     @property
     def header(self):
@@ -201,7 +207,8 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
         work = np.zeros((0, 4), np.int64)
     return Plan(T_Q, T_KV, len(heads), w.Hq, w.Hk, rows, cu_q_rows, k_tiles, row_batch, row_mblock,
                 row_qvalid, p_cnt, f_cnt, _csr(p_cnt), _csr(f_cnt), partial_idx, full_idx,
-                payload, halves_arr, quads_arr, seq, work, visible_pairs)
+                payload, halves_arr, quads_arr, seq, work, visible_pairs,
+                consumer_order(work, seq, p_cnt, f_cnt, Hmask))
 
 
 def schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, Hq, Hk, Hmask) -> np.ndarray:
@@ -228,6 +235,16 @@ def schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, Hq, Hk, Hmask) -> 
     out = np.array([(t[2], t[1], t[0], int(row_qvalid[t[3]])) for t in pos + zero],
                    dtype=np.int64).reshape(-1, 4)
     return out
+
+
+def consumer_order(work, sequence_desc, p_cnt, f_cnt, Hmask) -> np.ndarray:
+    """Positions of work_desc by task cost (partial + full entries of the
+    task's Q plan row), descending, ties in work_desc order."""
+    cost = np.zeros(len(work), np.int64)
+    for i, (m, h, b, _) in enumerate(np.asarray(work).tolist()):
+        hm, r = (0 if Hmask == 1 else h), int(sequence_desc[b, 4]) + m
+        cost[i] = int(p_cnt[hm, r]) + int(f_cnt[hm, r])
+    return np.argsort(-cost, kind="stable").astype(np.int64)
 
 
 def visible_from_plan(p: Plan, hm: int, b: int, q_len: int, k_len: int) -> np.ndarray:
@@ -288,4 +305,5 @@ def build_plan_by_heads(w, T_Q: int = 128, T_KV: int = 128, processes: int = 8) 
                 np.concatenate([q.payload for q in parts]),
                 np.concatenate([q.halves for q in parts]),
                 np.concatenate([q.quads for q in parts]), first.sequence_desc, work,
-                sum(q.visible_pairs for q in parts))
+                sum(q.visible_pairs for q in parts),
+                consumer_order(work, first.sequence_desc, p_cnt, f_cnt, w.Hmask))

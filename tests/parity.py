@@ -36,6 +36,7 @@ def compare_plan(gpu: dict, ref: OP.Plan):
     assert np.array_equal(gpu["halves"], ref.halves)
     assert np.array_equal(gpu["quads"], ref.quads)
     assert np.array_equal(gpu["work_desc"], ref.work_desc)
+    assert np.array_equal(gpu["lpt"], ref.lpt)
 
 
 def gpu_plan(w):

@@ -88,4 +88,4 @@ def test_struct_sizes_match_header():
     assert ctypes.sizeof(fa.FaGeometry) == 56
     assert ctypes.sizeof(fa.FaMods) == 16
     assert ctypes.sizeof(fa.FaPlanInfo) == 144
-    assert ctypes.sizeof(fa.FaPlanHostView) == 80  # ten array pointers
+    assert ctypes.sizeof(fa.FaPlanHostView) == 88  # eleven array pointers

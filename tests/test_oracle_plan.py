@@ -245,6 +245,29 @@ def test_schedule_brute_force_comparator():
     assert [tuple(x) for x in p.work_desc.tolist()] == want
 
 
+@pytest.mark.parametrize("seed,Hmask", [(21, 2), (22, 1)])
+def test_consumer_order_is_longest_first(seed, Hmask):
+    """The consumer order lists every work_desc position once, each task
+    before every task of smaller cost and before the tasks of equal cost
+    that come later in work_desc (checked pair by pair from the task costs
+    read off the CSR counts, not through a sort)."""
+    w = _tiny_interval_workload(seed=seed, B=0, S=0, nfunc=3, Hmask=Hmask, H=2,
+                                varlen_lens=[300, 40, 520, 129])
+    p = P.build_plan(w, 128, 128)
+    T = p.work_desc.shape[0]
+    assert sorted(p.lpt.tolist()) == list(range(T))
+    cost = []
+    for (m, h, b, _) in p.work_desc.tolist():
+        hm, r = (0 if Hmask == 1 else h), int(p.cu_q_rows[b]) + m
+        cost.append(int(p.partial_count[hm, r] + p.full_count[hm, r]))
+    assert len(set(cost)) > 2  # the ordering is exercised
+    order = p.lpt.tolist()
+    for i in range(T):
+        for j in range(i + 1, T):
+            a, c = order[i], order[j]
+            assert cost[a] > cost[c] or (cost[a] == cost[c] and a < c), (i, j)
+
+
 def test_sequence_desc_and_workload_shapes():
     w = W.varlen_doc_causal(0)
     lens = np.diff(w.cu_seqlens_q)
@@ -301,7 +324,7 @@ def _assert_same_plan(a, b):
         assert getattr(a, f) == getattr(b, f), f
     for f in ("cu_q_rows", "k_tiles", "row_batch", "row_mblock", "row_qvalid", "partial_count",
               "full_count", "partial_offset", "full_offset", "partial_idx", "full_idx", "payload",
-              "halves", "quads", "sequence_desc", "work_desc"):
+              "halves", "quads", "sequence_desc", "work_desc", "lpt"):
         x, y = getattr(a, f), getattr(b, f)
         assert x.shape == y.shape and np.array_equal(x, y), f
 
