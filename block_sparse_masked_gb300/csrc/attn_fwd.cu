@@ -86,7 +86,6 @@ constexpr uint32_t kBarSoftmax = 1;  // named barrier of the softmax warps
 
 struct FwdParams {
   const int32_t* work;
-  const int32_t* lpt;  // null: tasks in work_desc order; else the order tasks are taken in
   const int32_t* seq;
   const int32_t* p_off;
   const int32_t* f_off;
@@ -117,7 +116,7 @@ constexpr int kTaskRing = 2;  // tasks a CTA may hold ahead of its softmax warps
 
 __device__ __forceinline__ Task load_task(const FwdParams& p, int t) {
   Task k;
-  const int* wd = p.work + 4LL * (p.lpt ? __ldg(p.lpt + t) : t);
+  const int* wd = p.work + 4LL * t;
   k.m_block = wd[0];
   k.h = static_cast<int>(bsm_idx(wd[1], p.Hq, &g_fwd_err));
   k.b = static_cast<int>(bsm_idx(wd[2], p.B, &g_fwd_err));
@@ -969,10 +968,6 @@ cudaError_t launch_impl(const FwdLaunch& a, cudaStream_t st, const char** why) {
   FwdParams p{};
   p.ntasks = static_cast<int>(pl->tasks);
   p.work = pl->work_desc;
-  // interval plans: longest task first (with a few dozen tasks per SM the
-  // launch then ends on the shortest); block plans keep the §4.8 order,
-  // whose head-grouped sections keep each head's K/V in L2
-  p.lpt = (pl->mask_kind == MASK_INTERVALS) ? pl->lpt : nullptr;
   p.seq = pl->seq_desc;
   p.p_off = pl->p_off;
   p.f_off = pl->f_off;

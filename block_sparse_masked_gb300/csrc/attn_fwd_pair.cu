@@ -639,6 +639,10 @@ cudaError_t launch_pair_impl(const FwdLaunch& a, cudaStream_t st, const char** w
     *why = "cuTensorMapEncodeTiled failed (pointer alignment or driver entry point)";
     return cudaErrorInvalidValue;
   }
+  if (pl->lpt == nullptr) {  // built for every interval plan, the only plans routed here
+    *why = "the plan carries no longest-first task order";
+    return cudaErrorInvalidValue;
+  }
   PairParams p{};
   p.work = pl->work_desc;
   p.lpt = pl->lpt;

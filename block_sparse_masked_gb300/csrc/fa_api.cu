@@ -290,7 +290,9 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   ws.hist = reinterpret_cast<int32_t*>(w1 + o_hist);
   ws.cursors = reinterpret_cast<int32_t*>(w1 + o_cursor);
   ws.work = reinterpret_cast<int32_t*>(w1 + o_work);
-  ws.lpt = reinterpret_cast<int32_t*>(w1 + o_lpt);
+  // the longest-first order is built for interval plans only: block plans
+  // are taken in work_desc order, whose sections keep each head's K/V in L2
+  ws.lpt = (margs.kind == bsm::MASK_INTERVALS) ? reinterpret_cast<int32_t*>(w1 + o_lpt) : nullptr;
   ws.lbkt = reinterpret_cast<int32_t*>(w1 + o_lbkt);
   ws.lhist = reinterpret_cast<int32_t*>(w1 + o_lhist);
   if (bwd) {
@@ -369,7 +371,7 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
                q_cq = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
                q_ck = c2.take(g.layout == FA_LAYOUT_THD ? 4ull * (B + 1) : 0),
                q_er = c2.take(4ull * plan->P), q_hv = c2.take(plan->P), q_qd = c2.take(plan->P),
-               q_lpt = c2.take(4ull * plan->tasks);
+               q_lpt = c2.take(margs.kind == bsm::MASK_INTERVALS ? 4ull * plan->tasks : 0);
   uint8_t* pm = static_cast<uint8_t*>(al.get(c2.off));
   if (!pm) {
     delete plan;
@@ -385,7 +387,7 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   plan->f_idx = reinterpret_cast<int32_t*>(pm + q_fi);
   plan->payload = plan->quads_only ? nullptr : reinterpret_cast<uint32_t*>(pm + q_pay);
   plan->work_desc = reinterpret_cast<int32_t*>(pm + q_work);
-  plan->lpt = reinterpret_cast<int32_t*>(pm + q_lpt);
+  plan->lpt = (margs.kind == bsm::MASK_INTERVALS) ? reinterpret_cast<int32_t*>(pm + q_lpt) : nullptr;
   if (g.layout == FA_LAYOUT_THD) {
     plan->cu_seqlens_q = reinterpret_cast<int32_t*>(pm + q_cq);
     plan->cu_seqlens_k = reinterpret_cast<int32_t*>(pm + q_ck);
@@ -779,8 +781,10 @@ int fa_plan_export(const fa_plan* plan, fa_plan_host_view* dst) {
       {dst->work_desc, plan->work_desc, 16ull * plan->tasks},
       {dst->halves, plan->halves, static_cast<size_t>(plan->P)},
       {dst->quads, plan->quads, static_cast<size_t>(plan->P)},
-      {dst->lpt, plan->lpt, 4ull * plan->tasks},
+      {dst->lpt, plan->lpt, plan->lpt ? 4ull * plan->tasks : 0},
   };
+  if (dst->lpt && !plan->lpt)  // block plans: work_desc order
+    for (long long t = 0; t < plan->tasks; ++t) dst->lpt[t] = static_cast<int32_t>(t);
   for (auto& it : items) {
     if (!it.d || it.n == 0) continue;
     cudaError_t e = cudaMemcpy(it.d, it.s, it.n, cudaMemcpyDeviceToHost);

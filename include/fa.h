@@ -327,8 +327,10 @@ int fa_plan_info_get(const fa_plan* plan, int32_t count_visible, void* stream,
  *   positions of work_desc ordered by task cost -- partial + full entries of
  *   the task's row -- descending, ties in work_desc order, zero-cost tasks
  *   last: the longest-first order in which a consumer with few tasks per SM
- *   takes the tasks; "Flex Attention Mask Plan Design" §4.8 leaves the
- *   consumer's traversal of the task list open).  Synchronous.
+ *   takes the tasks; block-mask plans carry no such order on the device and
+ *   export the identity, work_desc's own section order, which their
+ *   forwards keep for L2 reuse; "Flex Attention Mask Plan Design" §4.8
+ *   leaves the consumer's traversal of the task list open).  Synchronous.
  */
 typedef struct {
   int32_t* cu_q_rows;

@@ -30,11 +30,13 @@ Follows "Flex Attention Mask Plan Design":
   tasks are ordered by L2 section (the (sample, K/V head) pair whose K/V the
   task reads), then descending cost, then the tie order (head, m_block);
   zero-cost tasks follow in (batch, head, m_block) order.
-* Consumer order ``lpt[tasks]``: the positions of work_desc sorted by task
-  cost, descending, ties in work_desc order (a stable sort), so zero-cost
-  tasks stay last: the longest-first order in which a consumer with few
-  tasks per SM takes the tasks (§4.8 fixes the task list; the traversal is
-  the consumer's).
+* Consumer order ``lpt[tasks]``: for interval masks, the positions of
+  work_desc sorted by task cost, descending, ties in work_desc order (a
+  stable sort), so zero-cost tasks stay last: the longest-first order in
+  which a consumer with few tasks per SM takes the tasks.  For block masks,
+  work_desc's own order (the identity): their consumers keep the section
+  order, under which a (sample, K/V head)'s K/V stays in L2 (§4.8 fixes the
+  task list; the traversal is the consumer's).
 
 The classification here is computed by expanding each Q tile into a dense
 boolean matrix and testing every element, which is independent of the GPU's
@@ -208,7 +210,7 @@ def build_plan(w, T_Q: int = 128, T_KV: int = 128, with_payload: bool = True,
     return Plan(T_Q, T_KV, len(heads), w.Hq, w.Hk, rows, cu_q_rows, k_tiles, row_batch, row_mblock,
                 row_qvalid, p_cnt, f_cnt, _csr(p_cnt), _csr(f_cnt), partial_idx, full_idx,
                 payload, halves_arr, quads_arr, seq, work, visible_pairs,
-                consumer_order(work, seq, p_cnt, f_cnt, Hmask))
+                consumer_order(work, seq, p_cnt, f_cnt, Hmask, w.mask_kind))
 
 
 def schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, Hq, Hk, Hmask) -> np.ndarray:
@@ -237,9 +239,12 @@ def schedule(row_batch, row_mblock, row_qvalid, p_cnt, f_cnt, Hq, Hk, Hmask) -> 
     return out
 
 
-def consumer_order(work, sequence_desc, p_cnt, f_cnt, Hmask) -> np.ndarray:
-    """Positions of work_desc by task cost (partial + full entries of the
-    task's Q plan row), descending, ties in work_desc order."""
+def consumer_order(work, sequence_desc, p_cnt, f_cnt, Hmask, mask_kind) -> np.ndarray:
+    """Interval masks: positions of work_desc by task cost (partial + full
+    entries of the task's Q plan row), descending, ties in work_desc order.
+    Block masks: work_desc order."""
+    if mask_kind != "intervals":
+        return np.arange(len(work), dtype=np.int64)
     cost = np.zeros(len(work), np.int64)
     for i, (m, h, b, _) in enumerate(np.asarray(work).tolist()):
         hm, r = (0 if Hmask == 1 else h), int(sequence_desc[b, 4]) + m
@@ -306,4 +311,4 @@ def build_plan_by_heads(w, T_Q: int = 128, T_KV: int = 128, processes: int = 8) 
                 np.concatenate([q.halves for q in parts]),
                 np.concatenate([q.quads for q in parts]), first.sequence_desc, work,
                 sum(q.visible_pairs for q in parts),
-                consumer_order(work, first.sequence_desc, p_cnt, f_cnt, w.Hmask))
+                consumer_order(work, first.sequence_desc, p_cnt, f_cnt, w.Hmask, w.mask_kind))

@@ -268,6 +268,18 @@ def test_consumer_order_is_longest_first(seed, Hmask):
             assert cost[a] > cost[c] or (cost[a] == cost[c] and a < c), (i, j)
 
 
+
+def test_block_plan_consumer_order_is_work_desc_order():
+    """Block-mask plans keep work_desc's section order (the identity), even
+    where task costs differ, so each (sample, K/V head) section's tasks stay
+    together."""
+    w = _small_block_workload(H=2, S=1000, BQ=64, BKV=64, seed=5, density=0.3)
+    p = P.build_plan(w, 128, 128)
+    T = p.work_desc.shape[0]
+    costs = {int(p.partial_count[h, r] + p.full_count[h, r]) for h in range(2) for r in range(p.rows)}
+    assert len(costs) > 2
+    assert p.lpt.tolist() == list(range(T))
+
 def test_sequence_desc_and_workload_shapes():
     w = W.varlen_doc_causal(0)
     lens = np.diff(w.cu_seqlens_q)
