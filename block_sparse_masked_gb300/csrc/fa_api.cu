@@ -118,9 +118,10 @@ cudaEvent_t front_event(int dev) {
   return ev[dev];
 }
 
-// Control words of the front stage (two device words, zero at launch and
-// left at zero by it): a per-device free list hands each in-flight build
-// its own pair.  New pairs are zeroed in stream order before their first use.
+// Control words of the front stage (two 32-bit words, then two 64-bit
+// entry totals; zero at launch and left at zero by it): a per-device free
+// list hands each in-flight build its own set.  New sets are zeroed in
+// stream order before their first use.
 std::mutex g_ctl_mu;
 std::vector<unsigned*> g_ctl_free[128];
 
@@ -139,7 +140,7 @@ unsigned* ctl_take(int dev, cudaStream_t st) {
     cudaGetLastError();
     return nullptr;
   }
-  if (cudaMemsetAsync(p, 0, 8, st) != cudaSuccess) {
+  if (cudaMemsetAsync(p, 0, 24, st) != cudaSuccess) {
     cudaFree(p);
     return nullptr;
   }
@@ -247,6 +248,8 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   const long long rows_ub_ll = static_cast<long long>(B) * nq_max;
   if (rows_ub_ll > (1LL << 26)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles");
   if (rows_ub_ll * margs.Hmask >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles x mask heads");
+  // forward tasks (Q tiles x Q heads) are indexed in 32-bit arithmetic
+  if (rows_ub_ll * g.heads_q >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles x Q heads");
   const int rows_ub = static_cast<int>(rows_ub_ll);
   const int words = std::max(1, cdiv(kt_ub, 32));
   const int Hmask = margs.Hmask;

@@ -102,6 +102,7 @@ struct FrontParams {
   long long* host_header;  // host memory, 8 values then the ticket; may be null
   long long ticket;
   unsigned* ctl;       // [0] CTAs arrived, [1] error bits; zero at launch, zero again at exit
+  unsigned long long* tot;  // [2] partial and full entries of every row; zero at launch, zero again at exit
   // backward K2Q view (§4.4); kp_cnt is null when it is not built
   int32_t* kp_cnt;     // [Hmask*B*kt_ub] per padded K row (hm, b, K tile): zero at launch
   int32_t* kf_cnt;
@@ -232,62 +233,137 @@ __device__ __forceinline__ void classify_intervals(const FrontParams& p, const S
   if (t == 0) {
     p.p_cnt[ws_row] = pc;
     p.f_cnt[ws_row] = fc;
+    atomicAdd(&p.tot[0], static_cast<unsigned long long>(pc));
+    atomicAdd(&p.tot[1], static_cast<unsigned long long>(fc));
   }
 }
 
-// Block masks (fixed length), 256 threads: thread per K tile.  Tile (i, j)
-// touches the logical blocks [r0, r1] x [c0, c1] that overlap its in-bounds
-// part; it is visible if any is active and full if all are and the tile has
-// no Q/K tail.  Words are bit-packed with warp ballots.
-__device__ __forceinline__ void classify_blocks(const FrontParams& p, const SampleGeo& sg, int b, int lr,
-                                                int hm, long long ws_row) {
+// Block masks (fixed length), 256 threads: thread per K tile, the CTA's R
+// padded Q tile rows x0 .. x0+R-1 together.  Tile (i, j) touches the
+// logical blocks [r0, r1] x [c0, c1] that overlap its in-bounds part; it is
+// visible if any is active and full if all are and the tile has no Q/K
+// tail.  Words are bit-packed with warp ballots.  When a tile touches at
+// most two blocks each way (blocks of 64 or more that divide the tile), the
+// four mask bytes of every row are requested before any is used, so the
+// rows share one memory latency; wider spans take a loop.
+template <int R>
+__device__ __forceinline__ void classify_blocks_rows(const FrontParams& p, int hm, int x0) {
   const int t = threadIdx.x, lane = t & 31;
-  __shared__ int s_pc, s_fc;
-  if (t == 0) {
-    s_pc = 0;
-    s_fc = 0;
+  __shared__ int s_pc[R], s_fc[R];
+  if (t < R) {
+    s_pc[t] = 0;
+    s_fc[t] = 0;
   }
   __syncthreads();
-  const int q_len = sg.q_len, k_len = sg.k_len, nk = cdiv(k_len, kTile);
-  const int q0 = lr * kTile, q1 = min(q0 + kTile, q_len);
-  const bool qtail = (q1 - q0) < kTile;
-  const int r0 = q0 / p.block_q, r1 = (q1 - 1) / p.block_q;
   const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
+  int rb[R], lrr[R], qlen[R], klen[R], r0[R], r1[R];
+  bool ok[R], qtail[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int x = x0 + i;
+    ok[i] = false;
+    rb[i] = 0;
+    lrr[i] = 0;
+    qlen[i] = klen[i] = 0;
+    r0[i] = r1[i] = 0;
+    qtail[i] = false;
+    if (x < p.rows_ub) {
+      const int b = x / p.nq_max, lr = x % p.nq_max;
+      const SampleGeo sg = sample_geo(p, b);
+      if (lr < cdiv(sg.q_len, kTile)) {
+        ok[i] = true;
+        rb[i] = b;
+        lrr[i] = lr;
+        qlen[i] = sg.q_len;
+        klen[i] = sg.k_len;
+        const int q0 = lr * kTile, q1 = min(q0 + kTile, sg.q_len);
+        qtail[i] = (q1 - q0) < kTile;
+        r0[i] = q0 / p.block_q;
+        r1[i] = (q1 - 1) / p.block_q;
+      }
+    }
+  }
   const int nwords_used = p.words * 32;
   for (int j0 = 0; j0 < nwords_used; j0 += blockDim.x) {
     const int j = j0 + t;
-    bool vis = false, full = false;
-    if (j < nk) {
-      const int k0 = j * kTile, k1 = min(k0 + kTile, k_len);
-      const bool ktail = (k1 - k0) < kTile;
-      const int c0 = k0 / p.block_kv, c1 = (k1 - 1) / p.block_kv;
-      bool any = false, all = true;
-      for (int r = r0; r <= r1; ++r) {
-        const uint8_t* Mr = M + static_cast<long long>(r) * p.nbk;
-        for (int c = c0; c <= c1; ++c) {
-          const bool x = __ldg(Mr + c) != 0;
-          any |= x;
-          all &= x;
+    int c0[R], c1[R];
+    bool in[R], ktail[R], two[R];
+    uint32_t m4[R];  // bytes (r0, c0), (r0, c1), (r1, c0), (r1, c1), nonzero -> 1
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      in[i] = ok[i] && j < cdiv(klen[i], kTile);
+      c0[i] = c1[i] = 0;
+      ktail[i] = false;
+      two[i] = false;
+      m4[i] = 0u;
+      if (in[i]) {
+        const int k0 = j * kTile, k1 = min(k0 + kTile, klen[i]);
+        ktail[i] = (k1 - k0) < kTile;
+        c0[i] = k0 / p.block_kv;
+        c1[i] = (k1 - 1) / p.block_kv;
+        two[i] = (r1[i] - r0[i] <= 1) && (c1[i] - c0[i] <= 1);
+        if (two[i]) {
+          const uint8_t* A = M + static_cast<long long>(r0[i]) * p.nbk;
+          const uint8_t* Bm = M + static_cast<long long>(r1[i]) * p.nbk;
+          m4[i] = (__ldg(A + c0[i]) ? 1u : 0u) | (__ldg(A + c1[i]) ? 2u : 0u) | (__ldg(Bm + c0[i]) ? 4u : 0u) |
+                  (__ldg(Bm + c1[i]) ? 8u : 0u);
         }
       }
-      vis = any;
-      full = any && all && !qtail && !ktail;
-      if (p.kp_cnt && vis) count_k2q(p, hm, b, j, !full, full);
     }
-    const uint32_t vb = __ballot_sync(kFull, vis);
-    const uint32_t fb = __ballot_sync(kFull, full);
-    const int w = j >> 5;
-    if (lane == 0 && w < p.words) {
-      p.vis_bits[ws_row * p.words + w] = vb;
-      p.full_bits[ws_row * p.words + w] = fb;
-      atomicAdd(&s_pc, __popc(vb & ~fb));
-      atomicAdd(&s_fc, __popc(fb));
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      bool vis = false, full = false;
+      if (in[i]) {
+        bool any, all;
+        if (two[i]) {
+          any = m4[i] != 0u;
+          all = m4[i] == 0xFu;
+        } else {
+          any = false;
+          all = true;
+          for (int r = r0[i]; r <= r1[i]; ++r) {
+            const uint8_t* Mr = M + static_cast<long long>(r) * p.nbk;
+            for (int c = c0[i]; c <= c1[i]; ++c) {
+              const bool xv = __ldg(Mr + c) != 0;
+              any |= xv;
+              all &= xv;
+            }
+          }
+        }
+        vis = any;
+        full = any && all && !qtail[i] && !ktail[i];
+        if (p.kp_cnt && vis) count_k2q(p, hm, rb[i], j, !full, full);
+      }
+      const uint32_t vb = __ballot_sync(kFull, vis);
+      const uint32_t fb = __ballot_sync(kFull, full);
+      const int w = j >> 5;
+      if (ok[i] && lane == 0 && w < p.words) {
+        const long long ws_row = static_cast<long long>(hm) * p.rows_ub + x0 + i;
+        p.vis_bits[ws_row * p.words + w] = vb;
+        p.full_bits[ws_row * p.words + w] = fb;
+        atomicAdd(&s_pc[i], __popc(vb & ~fb));
+        atomicAdd(&s_fc[i], __popc(fb));
+      }
     }
   }
   __syncthreads();
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    if (t == i && ok[i]) {
+      const long long ws_row = static_cast<long long>(hm) * p.rows_ub + x0 + i;
+      p.p_cnt[ws_row] = s_pc[i];
+      p.f_cnt[ws_row] = s_fc[i];
+    }
+  }
   if (t == 0) {
-    p.p_cnt[ws_row] = s_pc;
-    p.f_cnt[ws_row] = s_fc;
+    unsigned long long a = 0, c = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      a += ok[i] ? s_pc[i] : 0;
+      c += ok[i] ? s_fc[i] : 0;
+    }
+    if (a) atomicAdd(&p.tot[0], a);
+    if (c) atomicAdd(&p.tot[1], c);
   }
 }
 
@@ -296,24 +372,46 @@ __device__ __forceinline__ void classify_blocks(const FrontParams& p, const Samp
 // in compact (mask head, row) order; the header; reset of the control words.
 constexpr int kScanItems = 8;
 
-// Exclusive scans, by the whole CTA, of two per-row counts read by
-// counts(i, a, c) for compact rows i in [0, n): offsets to off_a/off_c
-// [n + 1]; totals added to tot_a/tot_c.
-template <class Counts>
-__device__ void scan_pair(long long n, int32_t* off_a, int32_t* off_c, long long& tot_a, long long& tot_c,
-                          Counts counts) {
+// q = i / d, r = i % d for 0 <= i, in 32-bit arithmetic when i fits.
+__device__ __forceinline__ void div_idx(long long i, int d, int& q, int& r) {
+  if (i <= 0x7fffffffLL) {
+    const int ii = static_cast<int>(i);
+    q = ii / d;
+    r = ii - q * d;
+  } else {
+    q = static_cast<int>(i / d);
+    r = static_cast<int>(i % d);
+  }
+}
+
+// Exclusive scans, by the whole CTA, of two per-row counts over padded rows
+// x in [0, npad).  at(x, ci) says whether row x exists and gives its
+// position ci in compact order, which is the padded order without the rows
+// that do not exist; so the scan over padded rows, with zeros for those,
+// is the compact scan.  The counts are read (cnt_a/cnt_c at x) only for rows
+// that exist: the others were never written.  Offsets to off_a/off_c [n + 1]
+// at the compact positions; totals added to tot_a/tot_c.  Each thread takes
+// kScanItems consecutive rows, whose loads are independent.
+template <class At>
+__device__ void scan_pair_padded(long long npad, long long n, const int32_t* cnt_a, const int32_t* cnt_c,
+                                 int32_t* off_a, int32_t* off_c, long long& tot_a, long long& tot_c, At at) {
   const int nt = blockDim.x;
   long long ca = 0, cc = 0;
-  for (long long base = 0; base < n; base += static_cast<long long>(nt) * kScanItems) {
+  for (long long base = 0; base < npad; base += static_cast<long long>(nt) * kScanItems) {
     const long long i0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
     int va[kScanItems], vc[kScanItems];
+    long long ci[kScanItems];
     long long sa = 0, sc = 0;
 #pragma unroll
     for (int k = 0; k < kScanItems; ++k) {
       const long long i = i0 + k;
       va[k] = 0;
       vc[k] = 0;
-      if (i < n) counts(i, va[k], vc[k]);
+      ci[k] = -1;
+      if (i < npad && at(i, ci[k])) {
+        va[k] = __ldcg(cnt_a + i);
+        vc[k] = __ldcg(cnt_c + i);
+      }
       sa += va[k];
       sc += vc[k];
     }
@@ -322,10 +420,9 @@ __device__ void scan_pair(long long n, int32_t* off_a, int32_t* off_c, long long
     long long ec = cc + block_excl_scan(sc, &tc);
 #pragma unroll
     for (int k = 0; k < kScanItems; ++k) {
-      const long long i = i0 + k;
-      if (i < n) {
-        off_a[i] = static_cast<int32_t>(ea);
-        off_c[i] = static_cast<int32_t>(ec);
+      if (ci[k] >= 0) {
+        off_a[ci[k]] = static_cast<int32_t>(ea);
+        off_c[ci[k]] = static_cast<int32_t>(ec);
       }
       ea += va[k];
       ec += vc[k];
@@ -334,6 +431,74 @@ __device__ void scan_pair(long long n, int32_t* off_a, int32_t* off_c, long long
     cc += tc;
   }
   if (threadIdx.x == 0) {
+    off_a[n] = static_cast<int32_t>(ca);
+    off_c[n] = static_cast<int32_t>(cc);
+  }
+  __syncthreads();
+  tot_a += ca;
+  tot_c += cc;
+}
+
+// Sample prefixes (cu_rows or cu_krows) staged in shared memory for the
+// padded scans when there are at most this many samples.
+constexpr int kCuSmem = 1024;
+
+// The same scans, staged through shared memory (buf_a/buf_c: ITEMS *
+// blockDim.x ints each, 16-byte aligned): a pass loads its counts with
+// coalesced loads, all issued before any is used; each thread then scans
+// ITEMS consecutive rows out of shared memory; the offsets go back through
+// shared memory and out with coalesced stores (the compact positions of
+// consecutive existing rows are consecutive).
+template <int ITEMS, class At>
+__device__ void scan_pair_staged(long long npad, long long n, const int32_t* __restrict__ cnt_a,
+                                 const int32_t* __restrict__ cnt_c, int32_t* off_a, int32_t* off_c,
+                                 int32_t* buf_a, int32_t* buf_c, long long& tot_a, long long& tot_c, At at) {
+  static_assert(ITEMS == 4, "one int4 per thread");
+  const int nt = blockDim.x, t = threadIdx.x;
+  const long long P = static_cast<long long>(nt) * ITEMS;
+  long long ca = 0, cc = 0;
+  for (long long base = 0; base < npad; base += P) {
+    int la[ITEMS], lc[ITEMS];
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      const long long x = base + static_cast<long long>(u) * nt + t;
+      long long ci;
+      const bool ok = x < npad && at(x, ci);
+      la[u] = ok ? __ldcg(cnt_a + x) : 0;
+      lc[u] = ok ? __ldcg(cnt_c + x) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      buf_a[u * nt + t] = la[u];
+      buf_c[u * nt + t] = lc[u];
+    }
+    __syncthreads();
+    const int4 a4 = reinterpret_cast<const int4*>(buf_a)[t];
+    const int4 c4 = reinterpret_cast<const int4*>(buf_c)[t];
+    long long ta, tc;
+    const long long ea = ca + block_excl_scan(static_cast<long long>(a4.x) + a4.y + a4.z + a4.w, &ta);
+    const long long ec = cc + block_excl_scan(static_cast<long long>(c4.x) + c4.y + c4.z + c4.w, &tc);
+    reinterpret_cast<int4*>(buf_a)[t] =
+        make_int4(static_cast<int32_t>(ea), static_cast<int32_t>(ea + a4.x), static_cast<int32_t>(ea + a4.x + a4.y),
+                  static_cast<int32_t>(ea + a4.x + a4.y + a4.z));
+    reinterpret_cast<int4*>(buf_c)[t] =
+        make_int4(static_cast<int32_t>(ec), static_cast<int32_t>(ec + c4.x), static_cast<int32_t>(ec + c4.x + c4.y),
+                  static_cast<int32_t>(ec + c4.x + c4.y + c4.z));
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      const long long x = base + static_cast<long long>(u) * nt + t;
+      long long ci;
+      if (x < npad && at(x, ci)) {
+        off_a[ci] = buf_a[u * nt + t];
+        off_c[ci] = buf_c[u * nt + t];
+      }
+    }
+    ca += ta;
+    cc += tc;
+    __syncthreads();  // the buffers are read before the next pass writes them
+  }
+  if (t == 0) {
     off_a[n] = static_cast<int32_t>(ca);
     off_c[n] = static_cast<int32_t>(cc);
   }
@@ -386,16 +551,8 @@ __device__ void front_finish(const FrontParams& p) {
     p.row_batch[r] = lo;
   }
   __syncthreads();
-  const long long n = static_cast<long long>(p.Hmask) * rows;
-  long long cp = 0, cf = 0;
-  scan_pair(n, p.p_off, p.f_off, cp, cf, [&](long long i, int& a, int& c) {
-    const int hm = static_cast<int>(i / rows), r = static_cast<int>(i % rows);
-    const int b = p.row_batch[r];
-    const long long ws_row = static_cast<long long>(hm) * p.rows_ub +
-                             static_cast<long long>(b) * p.nq_max + (r - p.cu_rows[b]);
-    a = __ldcg(p.p_cnt + ws_row);
-    c = __ldcg(p.f_cnt + ws_row);
-  });
+  __shared__ int32_t s_cu[kCuSmem + 1];
+  const bool cu_smem = p.B <= kCuSmem;
   // backward K2Q view (§4.2 backward prefix, §4.4 counts, §4.5 scan): K plan
   // rows per sample, K row -> sample, and the K2Q offsets
   long long k_rows = 0, kp = 0, kf = 0;
@@ -420,15 +577,27 @@ __device__ void front_finish(const FrontParams& p) {
     }
     __syncthreads();
     const long long nk_flat = static_cast<long long>(p.Hmask) * k_rows;
-    scan_pair(nk_flat, p.kp_off, p.kf_off, kp, kf, [&](long long i, int& a, int& c) {
-      const int hm = static_cast<int>(i / k_rows), r = static_cast<int>(i % k_rows);
-      const int b = p.krow_batch[r];
-      const long long ws = (static_cast<long long>(hm) * p.B + b) * p.kt_ub + (r - p.cu_krows[b]);
-      a = __ldcg(p.kp_cnt + ws);
-      c = __ldcg(p.kf_cnt + ws);
-    });
+    if (cu_smem)
+      for (int b = threadIdx.x; b <= p.B; b += nt) s_cu[b] = p.cu_krows[b];
+    __syncthreads();
+    // padded K rows (hm, b, K tile) in the layout of kp_cnt
+    scan_pair_padded(static_cast<long long>(p.Hmask) * p.B * p.kt_ub, nk_flat, p.kp_cnt, p.kf_cnt, p.kp_off,
+                     p.kf_off, kp, kf, [&](long long x, long long& ci) {
+                       int hb, j;
+                       div_idx(x, p.kt_ub, hb, j);
+                       const int hm = hb / p.B, b = hb - hm * p.B;
+                       const int c0 = cu_smem ? s_cu[b] : p.cu_krows[b];
+                       const int c1 = cu_smem ? s_cu[b + 1] : p.cu_krows[b + 1];
+                       if (j >= c1 - c0) return false;
+                       ci = static_cast<long long>(hm) * k_rows + c0 + j;
+                       return true;
+                     });
   }
   if (threadIdx.x == 0) {
+    // entry totals of the Q2K view: every CTA added its rows' counts (the
+    // offsets themselves are scanned by the schedule stage, which runs next)
+    const long long cp = static_cast<long long>(__ldcg(&p.tot[0]));
+    const long long cf = static_cast<long long>(__ldcg(&p.tot[1]));
     uint32_t e = atomicExch(&p.ctl[1], 0u);  // read and reset the error bits
     if (cp > 0x3fffffffLL || cf > 0x3fffffffLL || kp > 0x3fffffffLL || kf > 0x3fffffffLL) e |= PLANERR_OVERFLOW;
     // {fwd Q rows, fwd partial, fwd full, bwd Q rows, bwd K rows, bwd partial,
@@ -438,6 +607,8 @@ __device__ void front_finish(const FrontParams& p) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) p.header[k] = h[k];
     p.ctl[0] = 0u;  // every CTA has arrived: the control words are free again
+    p.tot[0] = 0ull;
+    p.tot[1] = 0ull;
     if (p.host_header) {
       volatile long long* hh = p.host_header;
 #pragma unroll
@@ -461,19 +632,16 @@ constexpr int kFrontRows = (KIND == MASK_INTERVALS) ? 1 : 4;
 template <int KIND>
 __global__ void __launch_bounds__(KIND == MASK_INTERVALS ? 128 : 256) k_front(FrontParams p) {
   const int hm = blockIdx.y;
-#pragma unroll 1
-  for (int i = 0; i < kFrontRows<KIND>; ++i) {
-    const int x = blockIdx.x * kFrontRows<KIND> + i;
-    if (x >= p.rows_ub) break;
-    const int b = x / p.nq_max, lr = x % p.nq_max;
-    const SampleGeo sg = sample_geo(p, b);
-    if (lr < cdiv(sg.q_len, kTile)) {
-      const long long ws_row = static_cast<long long>(hm) * p.rows_ub + x;
-      if (KIND == MASK_INTERVALS)
-        classify_intervals(p, sg, b, lr, hm, ws_row);
-      else
-        classify_blocks(p, sg, b, lr, hm, ws_row);
+  if constexpr (KIND == MASK_INTERVALS) {
+    const int x = blockIdx.x;
+    if (x < p.rows_ub) {
+      const int b = x / p.nq_max, lr = x % p.nq_max;
+      const SampleGeo sg = sample_geo(p, b);
+      if (lr < cdiv(sg.q_len, kTile))
+        classify_intervals(p, sg, b, lr, hm, static_cast<long long>(hm) * p.rows_ub + x);
     }
+  } else {
+    classify_blocks_rows<kFrontRows<KIND>>(p, hm, blockIdx.x * kFrontRows<KIND>);
   }
   __shared__ unsigned s_last;
   __threadfence();  // every thread's outputs are visible device-wide before the CTA arrives
@@ -662,6 +830,65 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
   const long long flat = static_cast<long long>(hm) * p.rows + row;
   const long long ws_row = static_cast<long long>(hm) * p.rows_ub + static_cast<long long>(b) * p.nq_max + lr;
   const int pstart = __ldg(p.p_off + flat), np = __ldg(p.p_off + flat + 1) - pstart;
+  if (KIND == MASK_BLOCKS && p.payload == nullptr) {
+    // Quadrant bits only (64-aligned logical blocks over 64-multiple
+    // lengths): each 64x64 quadrant lies inside one logical block pair and
+    // inside or outside the sample as a whole, so it is wholly visible or
+    // wholly masked.  Thread t takes tile j = j0 + t of each 128-tile chunk:
+    // its four block-mask bytes are requested with the row's bitset words,
+    // and its list position is its rank among the row's partial (or full)
+    // tiles -- earlier chunks, earlier warps, lower lanes -- so the lists
+    // come out ascending, as warp 0 writes them below for the other plans.
+    const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
+    const int q0 = lr * kTile, t = threadIdx.x;
+    __shared__ int s_np[4], s_nf[4];
+    int pc = pstart, fc = __ldg(p.f_off + flat);
+    for (int j0 = 0; j0 < p.words * 32; j0 += 128) {
+      const int j = j0 + t, w = j >> 5;
+      uint32_t vb = 0u, fb = 0u, live = 0u;
+      if (w < p.words) {
+        vb = __ldg(p.vis_bits + ws_row * p.words + w);
+        fb = __ldg(p.full_bits + ws_row * p.words + w);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int qr = q0 + 64 * a, kc = j * kTile + 64 * s2;
+          if (qr < q_len && kc < k_len && __ldg(M + static_cast<long long>(qr / p.block_q) * p.nbk + kc / p.block_kv))
+            live |= 1u << (2 * a + s2);
+        }
+      const uint32_t pb = vb & ~fb;
+      const uint32_t below = (1u << lane) - 1u;
+      if (lane == 0) {
+        s_np[wi] = __popc(pb);
+        s_nf[wi] = __popc(fb);
+      }
+      __syncthreads();
+      int pre_p = 0, pre_f = 0, all_p = 0, all_f = 0;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        if (x < wi) {
+          pre_p += s_np[x];
+          pre_f += s_nf[x];
+        }
+        all_p += s_np[x];
+        all_f += s_nf[x];
+      }
+      __syncthreads();  // s_np / s_nf are read before the next chunk writes them
+      if ((pb >> lane) & 1u) {
+        const long long e = bsm_idx(pc + pre_p + __popc(pb & below), p.nP, p.err);
+        p.p_idx[e] = j;
+        p.entry_row[e] = static_cast<int32_t>(flat);
+        p.halves[e] = static_cast<uint8_t>(((live & 5u) ? 1u : 0u) | ((live & 10u) ? 2u : 0u));
+        p.quads[e] = static_cast<uint8_t>(live | (live << 4));
+      }
+      if ((fb >> lane) & 1u) p.f_idx[bsm_idx(fc + pre_f + __popc(fb & below), p.nF, p.err)] = j;
+      pc += all_p;
+      fc += all_f;
+    }
+    return;
+  }
   if (wi == 0) {
     int pbase = pstart, fbase = __ldg(p.f_off + flat);
     for (int w0 = 0; w0 < p.words; w0 += 32) {
@@ -710,29 +937,6 @@ __global__ void __launch_bounds__(128) k_back(BackParams p) {
       sF[f][t] = (q0 + t < q_len) ? __ldg(Fg + static_cast<long long>(f) * p.total_q + q0 + t) : 0;
   }
   __syncthreads();  // the row's p_idx (written by warp 0) and sF are visible to the CTA
-  if (KIND == MASK_BLOCKS && p.payload == nullptr) {
-    // quadrant bits only (64-aligned logical blocks over 64-multiple
-    // lengths): each 64x64 quadrant lies inside one logical block pair and
-    // inside or outside the sample as a whole, so it is wholly visible or
-    // wholly masked; one thread per entry reads its four block-mask bytes
-    const uint8_t* M = p.block_mask + static_cast<long long>(hm) * p.nbq * p.nbk;
-    for (int k = threadIdx.x; k < np; k += blockDim.x) {
-      const long long e = bsm_idx(pstart + k, p.nP, p.err);
-      const int j = p.p_idx[e];
-      uint32_t live = 0u;
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-          const int qr = q0 + 64 * a, kc = j * kTile + 64 * s2;
-          if (qr < q_len && kc < k_len && __ldg(M + static_cast<long long>(qr / p.block_q) * p.nbk + kc / p.block_kv))
-            live |= 1u << (2 * a + s2);
-        }
-      p.halves[e] = static_cast<uint8_t>(((live & 5u) ? 1u : 0u) | ((live & 10u) ? 2u : 0u));
-      p.quads[e] = static_cast<uint8_t>(live | (live << 4));
-    }
-    return;
-  }
   for (int k = wi; k < np; k += 4) {
     const long long e = bsm_idx(pstart + k, p.nP, p.err);
     const int j = p.p_idx[e];
@@ -899,8 +1103,11 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
 struct SchedParams {
   const int32_t* seq;
   const int32_t* cu_rows;
-  const int32_t* p_off;
-  const int32_t* f_off;
+  const int32_t* row_batch;  // [rows]
+  const int32_t* p_cnt;      // per padded row (mask head, sample, Q tile row): the front stage's counts
+  const int32_t* f_cnt;
+  int32_t* p_off;            // compact [Hmask*rows+1]: scanned here
+  int32_t* f_off;
   int32_t* hist;     // [NS*(C+1)]
   int32_t* cursors;  // [NS*(C+1)]
   int32_t* work;     // [tasks*4]
@@ -908,7 +1115,9 @@ struct SchedParams {
   int32_t* lbkt;     // [tasks] scratch: bucket of every work_desc position
   int32_t* lhist;    // [32*(C+1)] scratch: per-warp bucket counts, then starts
   int B, Hq, Hk, Hmask, C, NS;
+  int rows_ub, nq_max;
   int in_smem;       // 1: histogram and cursors live in dynamic shared memory (2*NS*(C+1) ints)
+  int bkt_smem;      // 1: the task buckets follow them there (Hq*rows_ub ints); 0: in lbkt
   uint32_t* err;     // device error word (checked build)
 };
 
@@ -922,39 +1131,116 @@ __device__ __forceinline__ int task_bucket(const SchedParams& p, int cost) {
   return cost > 0 ? (p.C - min(cost, p.C)) : p.C;
 }
 
+// Quotient by a divisor fixed for the whole kernel, 1 <= d < 2^31, of
+// 0 <= x < 2^31, by one multiply and a shift ("Division by Invariant
+// Integers using Multiplication", Granlund and Montgomery, 1994): with
+// L = ceil(log2 d) and m = ceil(2^(31+L) / d), m d - 2^(31+L) < 2^L, so
+// floor(x m / 2^(31+L)) = floor(x / d) for every x below 2^31.  The single
+// CTA of the schedule stage is bound by instruction issue, and a hardware-
+// less 32-bit division costs it dozens of instructions per task.
+struct InvDiv {
+  uint32_t m = 1u;
+  int sh = 31;
+  __device__ __forceinline__ explicit InvDiv(int d) {
+    int L = 0;
+    while ((1u << L) < static_cast<uint32_t>(d)) ++L;
+    const uint64_t two = 1ull << (31 + L);
+    m = static_cast<uint32_t>((two + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d));
+    sh = 31 + L;
+  }
+  __device__ __forceinline__ int q(int x) const {
+    return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(x)) * m) >> sh);
+  }
+};
+
+// Lanes of `amask` whose v equals this lane's (v in [0, 2^nbits)), by one
+// ballot per bit of v; the calling lane must be in amask.
+__device__ __forceinline__ unsigned lanes_with_same(unsigned amask, int v, int nbits) {
+  unsigned same = amask;
+  for (int k = 0; k < nbits; ++k) {
+    const unsigned bal = __ballot_sync(amask, (v >> k) & 1);
+    same &= ((v >> k) & 1) ? bal : ~bal;
+  }
+  return same;
+}
+
 // One CTA builds the whole schedule with bounded counting:
-//  1. histogram of (section, cost bucket) over every task, one warp per section;
+//  1. every task's cost bucket, kept per (head, row), and the histogram of
+//     (section, cost bucket), the whole CTA over the tasks (four per thread
+//     and pass, their loads issued together; lanes with the same histogram
+//     cell add once);
 //  2. offsets: positive-cost tasks of section s start after every positive
 //     task of sections < s, ordered by bucket (cost descending); zero-cost
 //     tasks follow every positive task, sections in order (section totals
 //     and bucket cursors one warp per section, starts by a block scan);
 //  3. scatter: one warp per section walks its tasks in tie order (head in the
-//     section's group, then m_block), 32 at a time; lanes with the same
-//     bucket take consecutive slots in lane order, so the sort is stable.
+//     section's group, then m_block), 32 at a time, reading the buckets of
+//     step 1; lanes with the same bucket take consecutive slots in lane
+//     order, so the sort is stable.
 // Section s = (sample b, K/V head hk).
 __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   const int C = p.C;
+  const int nbits = 32 - __clz(C);  // buckets lie in [0, C]
   const int group = p.Hq / p.Hk;
   const int rows = p.cu_rows[p.B];
   const long long nb = static_cast<long long>(p.NS) * (C + 1);
   extern __shared__ int32_t s_counts[];
   int32_t* const hist = p.in_smem ? s_counts : p.hist;
   int32_t* const cursors = p.in_smem ? s_counts + nb : p.cursors;
+  int32_t* const bkt = p.bkt_smem ? s_counts + 2 * nb : p.lbkt;  // [Hq*rows]: bucket of task (head, row)
   for (long long i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  // one warp per section (the sections are many and small: one per sample
-  // and K/V head, a few dozen tasks each)
-  for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
-    const int b = sct / p.Hk, hk = sct % p.Hk;
-    const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5];
-    const int n = group * nrows;
-    for (int t = threadIdx.x & 31; t < n; t += 32) {
-      const int h = hk * group + t / nrows, m = t % nrows;
-      atomicAdd(&hist[static_cast<long long>(sct) * (C + 1) + task_bucket(p, task_cost(p, rows, h, begin + m))], 1);
+  {
+    // 0. the Q2K offsets (the plan's partial/full offsets): exclusive scans
+    //    of the front stage's per-row counts, padded rows in compact order
+    __shared__ int32_t s_cu[kCuSmem + 1];
+    __shared__ __align__(16) int32_t s_sa[4 * 1024], s_sc[4 * 1024];  // staging of the scan (blockDim.x <= 1024)
+    const bool cu_smem = p.B <= kCuSmem;
+    if (cu_smem)
+      for (int b = threadIdx.x; b <= p.B; b += blockDim.x) s_cu[b] = p.cu_rows[b];
+    __syncthreads();
+    long long cp = 0, cf = 0;
+    const InvDiv by_rows_ub(p.rows_ub), by_nq(p.nq_max);
+    scan_pair_staged<4>(static_cast<long long>(p.Hmask) * p.rows_ub, static_cast<long long>(p.Hmask) * rows, p.p_cnt,
+                        p.f_cnt, p.p_off, p.f_off, s_sa, s_sc, cp, cf, [&](long long x, long long& ci) {
+                       // x < Hmask * rows_ub < 2^31 (bounded on the host)
+                       const int xi = static_cast<int>(x);
+                       const int hm = by_rows_ub.q(xi), xr = xi - hm * p.rows_ub;
+                       const int b = by_nq.q(xr), lr = xr - b * p.nq_max;
+                       const int c0 = cu_smem ? s_cu[b] : p.cu_rows[b];
+                       const int c1 = cu_smem ? s_cu[b + 1] : p.cu_rows[b + 1];
+                       if (lr >= c1 - c0) return false;
+                       ci = static_cast<long long>(hm) * rows + c0 + lr;
+                       return true;
+                     });
+  }
+  const int lane = threadIdx.x & 31;
+  const int T = p.Hq * rows;  // fits: the host bounds Hq * rows_ub below 2^31
+  constexpr int kPer = 4;
+  const InvDiv by_rows(max(rows, 1)), by_group(group);
+  for (int base = 0; base < T; base += kPer * static_cast<int>(blockDim.x)) {
+    int cost[kPer], sct[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int f = base + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      cost[u] = 0;
+      sct[u] = 0;
+      if (f < T) {
+        const int h = by_rows.q(f), r = f - h * rows;
+        cost[u] = task_cost(p, rows, h, r);
+        sct[u] = __ldg(p.row_batch + r) * p.Hk + by_group.q(h);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int f = base + u * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+      if (f < T) {
+        const int bucket = task_bucket(p, cost[u]);
+        bkt[f] = bucket;
+        atomicAdd(&hist[static_cast<long long>(sct[u]) * (C + 1) + bucket], 1);
+      }
     }
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
   // 2a. positive-cost tasks per section (one warp per section, lanes over
   //     buckets); kept in the section's bucket-0 cursor until 2b
   for (int sct = threadIdx.x >> 5; sct < p.NS; sct += blockDim.x >> 5) {
@@ -1015,21 +1301,21 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5], q_len = p.seq[8 * b + 2];
     const int n = group * nrows;
     int32_t* cur = cursors + static_cast<long long>(sct) * (C + 1);
+    const InvDiv by_nrows(max(nrows, 1));
     for (int t0 = 0; t0 < n; t0 += 32) {
       const int t = t0 + lane;
       const bool act = t < n;
       const unsigned amask = __ballot_sync(kFull, act);
       if (act) {
-        const int h = hk * group + t / nrows, m = t % nrows;
-        const int bucket = task_bucket(p, task_cost(p, rows, h, begin + m));
-        const unsigned same = __match_any_sync(amask, bucket);
+        const int hg = by_nrows.q(t), m = t - hg * nrows;
+        const int h = hk * group + hg;
+        const int bucket = bkt[h * rows + begin + m];
+        const unsigned same = lanes_with_same(amask, bucket, nbits);
         const int rank = __popc(same & ((1u << lane) - 1));
         const int pos = cur[bucket] + rank;
-        int32_t* wd = p.work + 4LL * bsm_idx(pos, static_cast<long long>(p.Hq) * rows, p.err);
-        wd[0] = m;
-        wd[1] = h;
-        wd[2] = b;
-        wd[3] = min(kTile, q_len - m * kTile);
+        // one 16-byte store per entry (work_desc is 16-byte aligned)
+        *reinterpret_cast<int4*>(p.work + 4LL * bsm_idx(pos, static_cast<long long>(p.Hq) * rows, p.err)) =
+            make_int4(m, h, b, min(kTile, q_len - m * kTile));
         __syncwarp(amask);
         if (rank == 0) cur[bucket] += __popc(same);
       }
@@ -1054,7 +1340,10 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     for (long long i = c0 + lane; i < c1; i += 32) {
       const int32_t* wd = p.work + 4 * i;
       const int b = wd[2];
-      const int bucket = task_bucket(p, task_cost(p, rows, wd[1], p.seq[8 * b + 4] + wd[0]));
+      const int row = p.seq[8 * b + 4] + wd[0];
+      // (the buckets of step 1 when they are in shared memory; lbkt is
+      // rewritten here, by position)
+      const int bucket = p.bkt_smem ? bkt[wd[1] * rows + row] : task_bucket(p, task_cost(p, rows, wd[1], row));
       p.lbkt[i] = bucket;
       atomicAdd(&wh[bucket], 1);
     }
@@ -1087,7 +1376,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
       const unsigned amask = __ballot_sync(kFull, act);
       if (act) {
         const int bucket = p.lbkt[i];
-        const unsigned same = __match_any_sync(amask, bucket);
+        const unsigned same = lanes_with_same(amask, bucket, nbits);
         const int rank = __popc(same & ((1u << lane) - 1));
         p.lpt[bsm_idx(wh[bucket] + rank, T, p.err)] = static_cast<int32_t>(i);
         __syncwarp(amask);
@@ -1155,6 +1444,7 @@ cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspa
   p.host_header = host_header;
   p.ticket = ticket;
   p.ctl = ws.ctl;
+  p.tot = reinterpret_cast<unsigned long long*>(ws.ctl + 2);
   p.kp_cnt = ws.kp_cnt;
   p.kf_cnt = ws.kf_cnt;
   p.kt_ub = ws.kt_ub;
@@ -1177,12 +1467,15 @@ cudaError_t launch_front(const Geometry& g, const MaskArgs& m, const PlanWorkspa
 cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmask, int num_sections,
                             int max_cost, cudaStream_t st) {
   if (ws.rows_ub == 0) return cudaSuccess;
-  SchedParams p{ws.seq, ws.cu_rows, ws.p_off, ws.f_off, ws.hist, ws.cursors, ws.work, ws.lpt, ws.lbkt, ws.lhist,
-                g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections, 0, checked_error_word()};
+  SchedParams p{ws.seq, ws.cu_rows, ws.row_batch, ws.p_cnt, ws.f_cnt, ws.p_off, ws.f_off, ws.hist, ws.cursors,
+                ws.work, ws.lpt, ws.lbkt, ws.lhist, g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections,
+                ws.rows_ub, ws.nq_max, 0, 0, checked_error_word()};
   // histogram and cursors in shared memory when they fit (shared-memory
-  // atomics and the single CTA's scans then stay on chip)
+  // atomics and the single CTA's scans then stay on chip), and the task
+  // buckets after them when those fit too
   constexpr size_t kSchedSmemMax = 160 * 1024;
   const size_t bytes = 8ull * num_sections * (max_cost + 1);
+  const size_t bkt_bytes = 4ull * g.heads_q * ws.rows_ub;
   size_t dyn = 0;
   if (bytes <= kSchedSmemMax) {
     static std::atomic<bool> attr_set[128];
@@ -1197,6 +1490,10 @@ cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmas
     }
     p.in_smem = 1;
     dyn = bytes;
+    if (bytes + bkt_bytes <= kSchedSmemMax) {
+      p.bkt_smem = 1;
+      dyn += bkt_bytes;
+    }
   }
   k_schedule<<<1, 1024, dyn, st>>>(p);
   return cudaGetLastError();
@@ -1366,7 +1663,7 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   const long long words = kt_ub > 0 ? (kt_ub + 31) / 32 : 1;
   const long long nflat = static_cast<long long>(Hmask) * rows_ub;
   // same sub-arrays as the allocating build's first workspace
-  const size_t sizes[] = {8, 64, 4ull * (B + 1), 32ull * B, 4ull * rows_ub, 4ull * nflat * words,
+  const size_t sizes[] = {24, 64, 4ull * (B + 1), 32ull * B, 4ull * rows_ub, 4ull * nflat * words,
                           4ull * nflat * words, 4ull * nflat, 4ull * nflat, 4ull * (nflat + 1),
                           4ull * (nflat + 1)};
   size_t off[11], need = 0;
@@ -1408,7 +1705,7 @@ extern "C" int fa_plan_header_noalloc(const fa_geometry* geom, const int32_t* ma
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the front stage leaves its control words at zero, but a call whose
   // launch failed half-way is not known to have: start from zero every time
-  e = cudaMemsetAsync(ws.ctl, 0, 8, st);
+  e = cudaMemsetAsync(ws.ctl, 0, 24, st);
   if (e == cudaSuccess)
     e = launch_front(g, m, ws, geom->cu_seqlens_q, geom->cu_seqlens_k, nullptr, 0, st);
   if (e != cudaSuccess) return report_error(FA_ERR_CUDA, "allocation-free planner stage: %s", cudaGetErrorString(e));
