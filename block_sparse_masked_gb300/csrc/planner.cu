@@ -1097,6 +1097,29 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
   }
 }
 
+// Quotient by a divisor fixed for the whole kernel, 1 <= d < 2^31, of
+// 0 <= x < 2^31, by one multiply and a shift ("Division by Invariant
+// Integers using Multiplication", Granlund and Montgomery, 1994): with
+// L = ceil(log2 d) and m = ceil(2^(31+L) / d), m d - 2^(31+L) < 2^L, so
+// floor(x m / 2^(31+L)) = floor(x / d) for every x below 2^31.  The single
+// CTA of the schedule stage is bound by instruction issue, and a hardware-
+// less 32-bit division costs it dozens of instructions per task.
+// The multiplier costs a 64-bit division: the host forms those of divisors
+// it knows, and one thread those of the rest.
+struct InvDiv {
+  uint32_t m;
+  int sh;
+  __host__ __device__ static InvDiv of(int d) {
+    int L = 0;
+    while ((1u << L) < static_cast<uint32_t>(d)) ++L;
+    const uint64_t two = 1ull << (31 + L);
+    return InvDiv{static_cast<uint32_t>((two + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d)), 31 + L};
+  }
+  __device__ __forceinline__ int q(int x) const {
+    return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(x)) * m) >> sh);
+  }
+};
+
 // ------------------------------------------------------------ schedule
 // Reads the front stage's outputs in the workspace (the number of rows
 // included) and writes work_desc there; the back stage copies it into the plan.
@@ -1116,6 +1139,7 @@ struct SchedParams {
   int32_t* lhist;    // [32*(C+1)] scratch: per-warp bucket counts, then starts
   int B, Hq, Hk, Hmask, C, NS;
   int rows_ub, nq_max;
+  InvDiv by_rows_ub, by_nq, by_group;  // of rows_ub, nq_max, Hq / Hk
   int in_smem;       // 1: histogram and cursors live in dynamic shared memory (2*NS*(C+1) ints)
   int bkt_smem;      // 1: the task buckets follow them there (Hq*rows_ub ints); 0: in lbkt
   uint32_t* err;     // device error word (checked build)
@@ -1130,28 +1154,6 @@ __device__ __forceinline__ int task_cost(const SchedParams& p, int rows, int h, 
 __device__ __forceinline__ int task_bucket(const SchedParams& p, int cost) {
   return cost > 0 ? (p.C - min(cost, p.C)) : p.C;
 }
-
-// Quotient by a divisor fixed for the whole kernel, 1 <= d < 2^31, of
-// 0 <= x < 2^31, by one multiply and a shift ("Division by Invariant
-// Integers using Multiplication", Granlund and Montgomery, 1994): with
-// L = ceil(log2 d) and m = ceil(2^(31+L) / d), m d - 2^(31+L) < 2^L, so
-// floor(x m / 2^(31+L)) = floor(x / d) for every x below 2^31.  The single
-// CTA of the schedule stage is bound by instruction issue, and a hardware-
-// less 32-bit division costs it dozens of instructions per task.
-struct InvDiv {
-  uint32_t m = 1u;
-  int sh = 31;
-  __device__ __forceinline__ explicit InvDiv(int d) {
-    int L = 0;
-    while ((1u << L) < static_cast<uint32_t>(d)) ++L;
-    const uint64_t two = 1ull << (31 + L);
-    m = static_cast<uint32_t>((two + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d));
-    sh = 31 + L;
-  }
-  __device__ __forceinline__ int q(int x) const {
-    return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(x)) * m) >> sh);
-  }
-};
 
 // Lanes of `amask` whose v equals this lane's (v in [0, 2^nbits)), by one
 // ballot per bit of v; the calling lane must be in amask.
@@ -1199,7 +1201,7 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
       for (int b = threadIdx.x; b <= p.B; b += blockDim.x) s_cu[b] = p.cu_rows[b];
     __syncthreads();
     long long cp = 0, cf = 0;
-    const InvDiv by_rows_ub(p.rows_ub), by_nq(p.nq_max);
+    const InvDiv by_rows_ub = p.by_rows_ub, by_nq = p.by_nq;
     scan_pair_staged<4>(static_cast<long long>(p.Hmask) * p.rows_ub, static_cast<long long>(p.Hmask) * rows, p.p_cnt,
                         p.f_cnt, p.p_off, p.f_off, s_sa, s_sc, cp, cf, [&](long long x, long long& ci) {
                        // x < Hmask * rows_ub < 2^31 (bounded on the host)
@@ -1216,7 +1218,10 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
   const int lane = threadIdx.x & 31;
   const int T = p.Hq * rows;  // fits: the host bounds Hq * rows_ub below 2^31
   constexpr int kPer = 4;
-  const InvDiv by_rows(max(rows, 1)), by_group(group);
+  __shared__ InvDiv s_by_rows;
+  if (threadIdx.x == 0) s_by_rows = InvDiv::of(max(rows, 1));
+  __syncthreads();
+  const InvDiv by_rows = s_by_rows, by_group = p.by_group;
   for (int base = 0; base < T; base += kPer * static_cast<int>(blockDim.x)) {
     int cost[kPer], sct[kPer];
 #pragma unroll
@@ -1301,7 +1306,10 @@ __global__ void __launch_bounds__(1024) k_schedule(SchedParams p) {
     const int begin = p.seq[8 * b + 4], nrows = p.seq[8 * b + 5], q_len = p.seq[8 * b + 2];
     const int n = group * nrows;
     int32_t* cur = cursors + static_cast<long long>(sct) * (C + 1);
-    const InvDiv by_nrows(max(nrows, 1));
+    InvDiv by_nrows{0u, 0};
+    if (lane == 0) by_nrows = InvDiv::of(max(nrows, 1));
+    by_nrows.m = __shfl_sync(kFull, by_nrows.m, 0);
+    by_nrows.sh = __shfl_sync(kFull, by_nrows.sh, 0);
     for (int t0 = 0; t0 < n; t0 += 32) {
       const int t = t0 + lane;
       const bool act = t < n;
@@ -1469,7 +1477,8 @@ cudaError_t launch_schedule(const Geometry& g, const PlanWorkspace& ws, int Hmas
   if (ws.rows_ub == 0) return cudaSuccess;
   SchedParams p{ws.seq, ws.cu_rows, ws.row_batch, ws.p_cnt, ws.f_cnt, ws.p_off, ws.f_off, ws.hist, ws.cursors,
                 ws.work, ws.lpt, ws.lbkt, ws.lhist, g.batch, g.heads_q, g.heads_k, Hmask, max_cost, num_sections,
-                ws.rows_ub, ws.nq_max, 0, 0, checked_error_word()};
+                ws.rows_ub, ws.nq_max, InvDiv::of(ws.rows_ub), InvDiv::of(ws.nq_max),
+                InvDiv::of(g.heads_q / g.heads_k), 0, 0, checked_error_word()};
   // histogram and cursors in shared memory when they fit (shared-memory
   // atomics and the single CTA's scans then stay on chip), and the task
   // buckets after them when those fit too

@@ -90,6 +90,22 @@ def test_plan_parity_wide(seed, shape):
     plan.free()
 
 
+def _many_samples(seed, Hmask):
+    """More samples than the planner stages in shared memory (1024 sample
+    prefixes): the offset scans read the sample prefixes from global memory.
+    Empty samples at both ends."""
+    lens = [0] + [int(x) for x in np.random.default_rng(9).integers(0, 260, 1100)] + [0]
+    return _interval_workload(seed, B=0, S=0, nfunc=3, Hmask=Hmask, lens=lens)
+
+
+@pytest.mark.parametrize("Hmask", [1, 2])
+def test_plan_parity_more_samples_than_staged(Hmask):
+    w = _many_samples(3, Hmask)
+    dp, plan = PT.gpu_plan(w)
+    PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w))
+    plan.free()
+
+
 @pytest.mark.parametrize("geom", [(64, 64), (48, 80), (128, 32), (200, 300), (16, 128), (256, 256), (128, 384)])
 @pytest.mark.parametrize("S", [700, 1024])
 def test_block_plan_parity_geometries(geom, S):

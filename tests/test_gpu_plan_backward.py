@@ -92,3 +92,16 @@ def test_forward_only_plan_has_no_backward_view():
         fa.fa_plan_export_backward(plan)
     assert ei.value.code == fa.FA_ERR_INVALID_ARG
     plan.free()
+
+
+def test_backward_view_more_samples_than_staged():
+    """1102 samples (more sample prefixes than the front stage keeps in shared
+    memory for the K2Q offset scan), empty ones at both ends."""
+    lens = np.array([0] + [int(x) for x in np.random.default_rng(11).integers(0, 300, 1100)] + [0])
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    mf = W.random_intervals(4, len(lens), 0, 0, 3, 1, lens_q=lens, lens_k=lens)
+    z = torch.zeros(int(lens.sum()), 2, 128, dtype=torch.bfloat16)
+    mx = int(lens.max())
+    w = W.Workload("many", W.LAYOUT_THD, len(lens), mx, mx, 2, 2, 128, z, z, z, 1.0, "intervals",
+                   mask_func=mf, cu_seqlens_q=cu, cu_seqlens_k=cu.copy())
+    _check(w)
