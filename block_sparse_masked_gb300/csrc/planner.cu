@@ -6,20 +6,25 @@
 //               per-row partial/full counts, endpoints validated and clamped
 //               (§3.3); block masks use the logical-block expansion E(M) of
 //               "Decoupling Logical Masks from GPU Execution for Dynamic
-//               Block-Sparse Attention" §2.  The last CTA to finish builds
-//               the §4.2 compact row prefixes with the §3.2 prefix
-//               validation and the §4.8 sequence descriptors, runs the §4.5
-//               exclusive scans and writes the 8-value allocation header,
-//               also straight into host memory for the one host read-back.
-//   k_schedule  §4.8 forward task order by bounded counting (runs while the
-//               host reads the header and allocates the plan).
+//               Block-Sparse Attention" §2.  Every CTA adds its rows'
+//               counts to the §4.5 entry totals; the last CTA to finish
+//               builds the §4.2 compact row prefixes with the §3.2 prefix
+//               validation and the §4.8 sequence descriptors and writes the
+//               8-value allocation header from the totals (for backward
+//               plans after the K2Q scans), also straight into host memory
+//               for the one host read-back.
+//   k_schedule  §4.5 exclusive scans of the per-row counts into the
+//               partial/full offsets, then the §4.8 forward task order by
+//               bounded counting (runs while the host reads the header and
+//               allocates the plan).
 //   k_back_*    one CTA per (Q tile row, mask head): exact-size copies into
 //               the plan, §4.6 partial / full CSR index lists and the §5
 //               packed predicate payload of the row's partial tiles.
 // Every GPU launch costs a few microseconds of device time on its own, so
 // the stages are fused into as few launches as their data dependences
-// allow: the counts must be scanned before anything is sized, and the plan
-// can only be written once the host has sized and allocated it.
+// allow: only the totals size the plan, so the header goes out before the
+// offsets are scanned, and the plan can only be written once the host has
+// sized and allocated it.
 #include <cuda_runtime.h>
 
 #include <atomic>

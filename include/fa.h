@@ -416,8 +416,8 @@ int fa_debug_set_work_desc(fa_plan* plan, int64_t task, int32_t field, int32_t v
  * re-enter cudaMalloc, or a loop with a strict latency budget where
  * allocation calls (which may synchronise the device) are not allowed.
  *
- * It runs the geometry, classification and scan stages of
- * fa_plan_build_intervals and writes the same 8-value header (fwd Q rows,
+ * It runs the geometry and classification stage of fa_plan_build_intervals
+ * (which also totals the entries) and writes the same 8-value header (fwd Q rows,
  * partial nnz, full nnz, 0, 0, 0, 0, error flags) to `header_out`, a
  * caller-owned device int64[8].  Nothing else is produced and nothing is
  * read back: the call is asynchronous on `stream`, and a malformed mask or
