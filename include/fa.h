@@ -43,7 +43,7 @@ enum {
   FA_ERR_ALLOC = -5,           /* device or host allocation failed            */
   FA_ERR_CUDA = -6,            /* a CUDA runtime / driver call failed         */
   FA_ERR_DEVICE_TIMEOUT = -7,  /* a bounded in-kernel wait ran out            */
-  FA_ERR_UNSUPPORTED = -8      /* valid request outside what this build runs  */
+  FA_ERR_UNSUPPORTED = -8      /* valid request outside what the library runs */
 };
 
 enum { FA_LAYOUT_BSHD = 0, FA_LAYOUT_THD = 1 };
@@ -60,7 +60,7 @@ enum { FA_MOD_SOFTCAP = 1, FA_MOD_ALIBI = 2 };
  * Coarsened mapping).  Results agree within the forward's tolerance. */
 enum { FA_FWD_ONE_TILE = 16, FA_FWD_COARSENED = 32 };
 
-/* Physical tile of this build's consumer. */
+/* Physical tile of the library's consumers. */
 #define FA_TILE_Q 128
 #define FA_TILE_K 128
 /* uint32 words of packed predicate per tile row (128 columns / 32). */
