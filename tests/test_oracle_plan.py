@@ -245,6 +245,26 @@ def test_schedule_brute_force_comparator():
     assert [tuple(x) for x in p.work_desc.tolist()] == want
 
 
+def _longest_first_violations(order, cost):
+    """Pairs (i, j), i < j, of the order that break "each task before every
+    cheaper task and before the later tasks of equal cost"."""
+    bad = []
+    for i in range(len(order)):
+        for j in range(i + 1, len(order)):
+            a, c = order[i], order[j]
+            if not (cost[a] > cost[c] or (cost[a] == cost[c] and a < c)):
+                bad.append((i, j))
+    return bad
+
+
+def _task_costs(p, Hmask):
+    cost = []
+    for (m, h, b, _) in p.work_desc.tolist():
+        hm, r = (0 if Hmask == 1 else h), int(p.cu_q_rows[b]) + m
+        cost.append(int(p.partial_count[hm, r] + p.full_count[hm, r]))
+    return cost
+
+
 @pytest.mark.parametrize("seed,Hmask", [(21, 2), (22, 1)])
 def test_consumer_order_is_longest_first(seed, Hmask):
     """The consumer order lists every work_desc position once, each task
@@ -256,17 +276,25 @@ def test_consumer_order_is_longest_first(seed, Hmask):
     p = P.build_plan(w, 128, 128)
     T = p.work_desc.shape[0]
     assert sorted(p.lpt.tolist()) == list(range(T))
-    cost = []
-    for (m, h, b, _) in p.work_desc.tolist():
-        hm, r = (0 if Hmask == 1 else h), int(p.cu_q_rows[b]) + m
-        cost.append(int(p.partial_count[hm, r] + p.full_count[hm, r]))
+    cost = _task_costs(p, Hmask)
     assert len(set(cost)) > 2  # the ordering is exercised
-    order = p.lpt.tolist()
-    for i in range(T):
-        for j in range(i + 1, T):
-            a, c = order[i], order[j]
-            assert cost[a] > cost[c] or (cost[a] == cost[c] and a < c), (i, j)
+    assert _longest_first_violations(p.lpt.tolist(), cost) == []
 
+
+def test_consumer_order_pin_catches_planted_mistakes():
+    """Orders with a plausible mistake fail the pin: equal costs in reverse
+    work_desc order (an unstable or descending-index sort), and costs
+    ascending."""
+    w = _tiny_interval_workload(seed=21, B=0, S=0, nfunc=3, Hmask=2, H=2,
+                                varlen_lens=[300, 40, 520, 129])
+    p = P.build_plan(w, 128, 128)
+    cost = _task_costs(p, 2)
+    assert any(cost.count(c) > 1 for c in set(cost))  # ties exist
+    T = len(cost)
+    reversed_ties = sorted(range(T), key=lambda i: (-cost[i], -i))
+    ascending = sorted(range(T), key=lambda i: (cost[i], i))
+    assert _longest_first_violations(reversed_ties, cost) != []
+    assert _longest_first_violations(ascending, cost) != []
 
 
 def test_block_plan_consumer_order_is_work_desc_order():
