@@ -106,6 +106,25 @@ def test_plan_parity_more_samples_than_staged(Hmask):
     plan.free()
 
 
+@pytest.mark.parametrize("Hk", [32, 1])
+def test_plan_parity_schedule_outside_shared_memory(Hk):
+    """2,000 short samples x 32 Q heads: the schedule stage's task buckets
+    (one per Q tile row and Q head) exceed its shared memory and live in the
+    workspace; with 32 K/V heads (one section per sample and K/V head) its
+    histogram and cursors do too."""
+    lens = np.random.default_rng(12).integers(1, 129, 2000)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    mf = W.random_intervals(6, len(lens), 0, 0, 3, 1, lens_q=lens, lens_k=lens)
+    z = torch.zeros(int(lens.sum()), Hk, 64, dtype=torch.bfloat16)
+    zq = torch.zeros(int(lens.sum()), 32, 64, dtype=torch.bfloat16)
+    mx = int(lens.max())
+    w = W.Workload("short_docs", W.LAYOUT_THD, len(lens), mx, mx, 32, Hk, 64, zq, z, z, 1.0, "intervals",
+                   mask_func=mf, cu_seqlens_q=cu, cu_seqlens_k=cu.copy())
+    dp, plan = PT.gpu_plan(w)
+    PT.compare_plan(fa.fa_plan_export(plan), OP.build_plan(w))
+    plan.free()
+
+
 @pytest.mark.parametrize("geom", [(64, 64), (48, 80), (128, 32), (200, 300), (16, 128), (256, 256), (128, 384)])
 @pytest.mark.parametrize("S", [700, 1024])
 def test_block_plan_parity_geometries(geom, S):
