@@ -1107,8 +1107,9 @@ __global__ void __launch_bounds__(128) k_back_k2q(K2QParams p) {
 // Integers using Multiplication", Granlund and Montgomery, 1994): with
 // L = ceil(log2 d) and m = ceil(2^(31+L) / d), m d - 2^(31+L) < 2^L, so
 // floor(x m / 2^(31+L)) = floor(x / d) for every x below 2^31.  The single
-// CTA of the schedule stage is bound by instruction issue, and a hardware-
-// less 32-bit division costs it dozens of instructions per task.
+// CTA of the schedule stage is bound by instruction issue, and a 32-bit
+// integer division, which the GPU carries out in software, costs it dozens
+// of instructions per task.
 // The multiplier costs a 64-bit division: the host forms those of divisors
 // it knows, and one thread those of the rest.
 struct InvDiv {
