@@ -124,7 +124,10 @@ typedef struct {
  * 8-value header back once (the only host/device synchronisation), then
  * allocates exact-size outputs.  Malformed endpoints return
  * FA_ERR_INVALID_MASK, malformed prefixes FA_ERR_INVALID_SEQLENS; no plan
- * is produced.  The caller owns mask_func and may reuse it after return.
+ * is produced.  Geometries with more than 2^26 Q tiles (batch x
+ * ceil(seqlen_q / 128)), or whose Q tiles times Hmask or times heads_q
+ * reach 2^31, return FA_ERR_UNSUPPORTED.  The caller owns mask_func and may
+ * reuse it after return.
  * On success *out receives a plan the caller must release with fa_plan_free.
  */
 int fa_plan_build_intervals(const fa_geometry* geom, const int32_t* mask_func,
