@@ -236,9 +236,6 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   if (int e = check_geometry(gi)) return e;
   const bsm::Geometry g = to_geom(gi);
   const int B = g.batch;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int dev = 0;
-  if (cudaError_t e = cudaGetDevice(&dev)) return cuda_fail(e, "cudaGetDevice");
 
   // upper bounds of the planner workspace (§4.5: exact sizes come from the header)
   const int nq_max = cdiv(g.seqlen_q, bsm::kTile);
@@ -250,6 +247,10 @@ int build_common(const fa_geometry* gi, const bsm::MaskArgs& margs, uint32_t fla
   if (rows_ub_ll * margs.Hmask >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles x mask heads");
   // forward tasks (Q tiles x Q heads) are indexed in 32-bit arithmetic
   if (rows_ub_ll * g.heads_q >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many Q tiles x Q heads");
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return cuda_fail(e, "cudaGetDevice");
   const int rows_ub = static_cast<int>(rows_ub_ll);
   const int words = std::max(1, cdiv(kt_ub, 32));
   const int Hmask = margs.Hmask;

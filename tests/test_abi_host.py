@@ -57,6 +57,16 @@ def test_structural_errors(L, kw, nfunc, Hmask, code):
     assert fa.fa_last_error() != ""
 
 
+@pytest.mark.parametrize("kw", [
+    dict(batch=(1 << 26) + 1, seqlen_q=1, seqlen_k=1),               # Q tiles above 2^26
+    dict(seqlen_q=1 << 30, seqlen_k=128, heads_q=256, heads_k=256),  # Q tiles x Q heads at 2^31
+])
+def test_size_limits_rejected_before_any_gpu_work(L, kw):
+    rc, plan = _build_intervals(L, _geom(**kw))
+    assert rc == fa.FA_ERR_UNSUPPORTED and plan is None
+    assert "too many Q tiles" in fa.fa_last_error()
+
+
 def test_null_geometry_and_mask(L):
     rc, plan = _build_intervals(L, None)
     assert rc == fa.FA_ERR_INVALID_ARG and plan is None
